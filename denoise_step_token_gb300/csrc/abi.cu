@@ -1,0 +1,86 @@
+// Library-wide entry points of libdllm.so: status strings, ABI checks, the
+// per-device error word and cached device facts.
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace dllm {
+namespace {
+
+// First device-side error since the last dllm_get_device_error (one per device).
+__device__ int g_error_word;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::mutex g_mu;
+
+}  // namespace
+
+int* error_word_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_sm_count[dev] <= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace dllm
+
+extern "C" const char* dllm_strerror(int code) {
+    switch (code) {
+        case DLLM_OK: return "ok";
+        case DLLM_ERR_INVAL: return "invalid argument (size, pointer or value out of range)";
+        case DLLM_ERR_ALIGN: return "alignment rule broken (logits must be 16-byte aligned, ldv a multiple of 8)";
+        case DLLM_ERR_CUDA: return "CUDA runtime call failed";
+        case DLLM_ERR_DEVICE: return "device error word set";
+        case DLLM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DLLM_ERR_UNSUPPORTED: return "shape beyond this build's limits";
+        default: return "unknown status code";
+    }
+}
+
+extern "C" int dllm_abi_version(void) { return DLLM_ABI_VERSION; }
+
+extern "C" size_t dllm_struct_size(int which) {
+    switch (which) {
+        case 0: return sizeof(dllm_step_args);
+        case 1: return sizeof(dllm_pack_args);
+        case 2: return sizeof(dllm_compact_args);
+        case 3: return sizeof(dllm_advance_args);
+        default: return 0;
+    }
+}
+
+extern "C" int dllm_get_device_error(void* stream, int32_t* code) {
+    if (!code) return DLLM_ERR_INVAL;
+    int* p = dllm::error_word_ptr();
+    if (!p) return DLLM_ERR_CUDA;
+    cudaStream_t s = dllm::as_stream(stream);
+    int v = 0;
+    DLLM_CUDA_TRY(cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s));
+    DLLM_CUDA_TRY(cudaStreamSynchronize(s));
+    if (v != 0) {
+        DLLM_CUDA_TRY(cudaMemsetAsync(p, 0, sizeof(int), s));
+        DLLM_CUDA_TRY(cudaStreamSynchronize(s));
+    }
+    *code = v;
+    return DLLM_OK;
+}

@@ -1,0 +1,412 @@
+// Mixed-state batch management around the step (S7-S9):
+//   dllm_pack_plan / dllm_admit  host planning by eq. (1) and sand-fill,
+//   dllm_pack                    the left-padded bounding box,
+//   dllm_advance                 block commit, b += 1, eviction flags,
+//   dllm_compact                 stable in-place compaction of row arrays.
+// BlockServe page ("BlockServe: 块粒度连续批处理实现高吞吐扩散大语言模型服务"),
+// sections II-C (Algorithm 1), II-D (eq. (1), sand-fill admission) and II-E
+// (logical position alignment, gather/scatter of the active block); FDFO page,
+// section "FDFO 的核心思想" (finished requests leave at once).
+//
+// These kernels move a few MB per call and are latency-bound; they are written
+// for coalesced access (consecutive threads, consecutive columns) and a grid
+// capped at a few CTAs per SM.
+
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dllm {
+namespace {
+
+// ---------------------------------------------------------------------------
+// dllm_pack
+// ---------------------------------------------------------------------------
+struct PackParams {
+    int A, L, W, pad_id;
+    const int* p;
+    const int* b;
+    const int* rid;
+    const long long* prompt_off;
+    const int* prompt_tokens;
+    const int* gen_tokens;
+    long long ld_gen;
+    const int* block_ids;
+    int* ids;
+    uint8_t* attn;
+    int* pos;
+    int* pad;
+    int* blk_start;
+    int* err;
+};
+
+__global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams P) {
+    const long long total = (long long)P.A * P.W;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(idx / P.W);
+        const int c = (int)(idx - (long long)i * P.W);
+        const int p = __ldg(P.p + i);
+        const int b = __ldg(P.b + i);
+        const long long width = (long long)p + (long long)(b + 1) * P.L;
+        if (p < 0 || b < 0 || width > P.W) {
+            if (c == 0) set_error(P.err, DLLM_DEVERR_ROW_WIDTH);
+            continue;
+        }
+        const int pad = P.W - (int)width;
+        int tok, a, ps;
+        if (c < pad) {
+            tok = P.pad_id;
+            a = 0;
+            ps = 0;
+        } else {
+            const int k = c - pad;   // logical position: cumulative index over the mask
+            a = 1;
+            ps = k;
+            const int r = __ldg(P.rid + i);
+            if (k < p) {
+                tok = __ldg(P.prompt_tokens + __ldg(P.prompt_off + r) + k);
+            } else if (k < p + b * P.L) {
+                tok = __ldg(P.gen_tokens + (long long)r * P.ld_gen + (k - p));
+            } else {
+                tok = __ldg(P.block_ids + (long long)i * P.L + (k - p - b * P.L));
+            }
+        }
+        P.ids[idx] = tok;
+        if (P.attn) P.attn[idx] = (uint8_t)a;
+        if (P.pos) P.pos[idx] = ps;
+        if (c == 0) {
+            if (P.pad) P.pad[i] = pad;
+            if (P.blk_start) P.blk_start[i] = p + b * P.L;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dllm_advance: one warp per row
+// ---------------------------------------------------------------------------
+struct AdvanceParams {
+    int A, L, mask_id;
+    const uint8_t* advance;
+    const int* rid;
+    const int* K;
+    int* b;
+    int* ids;
+    float* cs;
+    int* gen;
+    long long ld_gen;
+    uint8_t* evict;
+    int* err;
+};
+
+__global__ void __launch_bounds__(256) advance_kernel(const __grid_constant__ AdvanceParams P) {
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (i >= P.A) return;
+    if (!P.advance[i]) {
+        if (lane == 0) P.evict[i] = 0;
+        return;
+    }
+    const int r = P.rid[i];
+    const int b = P.b[i];
+    const int K = P.K[i];
+    if (b < 0 || b >= K || (long long)(b + 1) * P.L > P.ld_gen) {
+        if (lane == 0) {
+            set_error(P.err, DLLM_DEVERR_BLOCK_INDEX);
+            P.evict[i] = 0;
+        }
+        return;
+    }
+    const long long src = (long long)i * P.L;
+    const long long dst = (long long)r * P.ld_gen + (long long)b * P.L;
+    for (int j = lane; j < P.L; j += 32) P.gen[dst + j] = P.ids[src + j];
+    const bool ev = b + 1 >= K;
+    __syncwarp();
+    if (!ev) {
+        const float qnan = __int_as_float(0x7fc00000);
+        for (int j = lane; j < P.L; j += 32) {
+            P.ids[src + j] = P.mask_id;
+            P.cs[src + j] = qnan;
+        }
+    }
+    if (lane == 0) {
+        P.b[i] = b + 1;
+        P.evict[i] = ev ? 1 : 0;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dllm_compact: scatter kept rows into the workspace, then copy back
+// ---------------------------------------------------------------------------
+constexpr int kCompactRows = 256;   // rows per CTA, one per thread for the scan
+
+struct CompactParams {
+    int A, n_arrays;
+    const uint8_t* evict;
+    int* new_index;
+    int* src_row;
+    int* A_out;
+    unsigned char* arrays[DLLM_COMPACT_MAX_ARRAYS];
+    unsigned char* stage[DLLM_COMPACT_MAX_ARRAYS];
+    long long row_bytes[DLLM_COMPACT_MAX_ARRAYS];
+};
+
+__device__ __forceinline__ void copy_row(unsigned char* dst, const unsigned char* src, long long n, int t, int nt) {
+    const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src);
+    if ((n & 15) == 0 && (al & 15) == 0) {
+        for (long long k = t; k < n / 16; k += nt)
+            reinterpret_cast<uint4*>(dst)[k] = reinterpret_cast<const uint4*>(src)[k];
+    } else if ((n & 3) == 0 && (al & 3) == 0) {
+        for (long long k = t; k < n / 4; k += nt)
+            reinterpret_cast<uint32_t*>(dst)[k] = reinterpret_cast<const uint32_t*>(src)[k];
+    } else {
+        for (long long k = t; k < n; k += nt) dst[k] = src[k];
+    }
+}
+
+__global__ void __launch_bounds__(kCompactRows) compact_scatter_kernel(const __grid_constant__ CompactParams P) {
+    __shared__ int s_warp[kCompactRows / 32];
+    __shared__ int s_before;
+    __shared__ int s_new[kCompactRows];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int i0 = blockIdx.x * kCompactRows;
+    // kept rows before this CTA's range
+    int pre = 0;
+    for (int k = t; k < i0; k += kCompactRows) pre += P.evict[k] ? 0 : 1;
+    for (int off = 16; off; off >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, off);
+    if (lane == 0) s_warp[warp] = pre;
+    __syncthreads();
+    if (t == 0) {
+        int acc = 0;
+        for (int w = 0; w < kCompactRows / 32; ++w) acc += s_warp[w];
+        s_before = acc;
+    }
+    __syncthreads();
+    // stable rank inside the range
+    const int i = i0 + t;
+    const bool keep = i < P.A && !P.evict[i];
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) s_warp[warp] = __popc(bal);
+    __syncthreads();
+    int wbefore = 0, total = 0;
+    for (int w = 0; w < kCompactRows / 32; ++w) {
+        if (w < warp) wbefore += s_warp[w];
+        total += s_warp[w];
+    }
+    const int ni = keep ? s_before + wbefore + __popc(bal & ((1u << lane) - 1u)) : -1;
+    if (i < P.A) {
+        if (P.new_index) P.new_index[i] = ni;
+        if (keep && P.src_row) P.src_row[ni] = i;
+    }
+    s_new[t] = ni;
+    if (i0 + kCompactRows >= P.A && t == 0) *P.A_out = s_before + total;   // last CTA
+    __syncthreads();
+    // scatter every kept row of every array into its staging copy
+    const int rows = min(kCompactRows, P.A - i0);
+    for (int a = 0; a < P.n_arrays; ++a) {
+        const long long rb = P.row_bytes[a];
+        for (int r = warp; r < rows; r += kCompactRows / 32) {
+            const int d = s_new[r];
+            if (d < 0) continue;
+            copy_row(P.stage[a] + (long long)d * rb, P.arrays[a] + (long long)(i0 + r) * rb, rb, lane, 32);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) compact_copyback_kernel(const __grid_constant__ CompactParams P) {
+    const int n = *P.A_out;
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int a = 0; a < P.n_arrays; ++a) {
+        const long long rb = P.row_bytes[a];
+        for (int r = gw; r < n; r += nw)
+            copy_row(P.arrays[a] + (long long)r * rb, P.stage[a] + (long long)r * rb, rb, lane, 32);
+    }
+}
+
+inline size_t compact_ws_bytes(int A, int n, const int64_t* rb) {
+    size_t total = 0;
+    for (int k = 0; k < n; ++k) total += (size_t(A) * size_t(rb[k]) + 255) & ~size_t(255);
+    return total + 256;
+}
+
+// Disjoint-set "nearest free slot" finder used by the admission planner.
+struct NextFree {
+    std::vector<int> parent;
+    explicit NextFree(int n) : parent(n + 1) {
+        for (int i = 0; i <= n; ++i) parent[i] = i;
+    }
+    int find(int i) {
+        int r = i;
+        while (parent[r] != r) r = parent[r];
+        while (parent[i] != r) {
+            const int nx = parent[i];
+            parent[i] = r;
+            i = nx;
+        }
+        return r;
+    }
+};
+
+}  // namespace
+}  // namespace dllm
+
+using namespace dllm;
+
+extern "C" int dllm_pack_plan(int32_t A, const int32_t* p, const int32_t* b, int32_t L, int32_t* W, int64_t* cost) {
+    if (A < 0 || L < 1) return DLLM_ERR_INVAL;
+    if (A > 0 && (!p || !b)) return DLLM_ERR_INVAL;
+    long long w = 0;
+    for (int i = 0; i < A; ++i) {
+        if (p[i] < 0 || b[i] < 0) return DLLM_ERR_INVAL;
+        w = std::max(w, (long long)p[i] + ((long long)b[i] + 1) * L);
+    }
+    if (w > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
+    if (W) *W = (int32_t)w;
+    if (cost) *cost = (int64_t)A * w;
+    return DLLM_OK;
+}
+
+extern "C" int dllm_admit(int32_t n_pending, const int32_t* pending_p, int32_t A, const int32_t* active_p,
+                          const int32_t* active_b, int32_t L, int64_t budget, int32_t* admit_idx, int32_t* n_admit) {
+    if (n_pending < 0 || A < 0 || L < 1 || !n_admit) return DLLM_ERR_INVAL;
+    if (n_pending > 0 && (!pending_p || !admit_idx)) return DLLM_ERR_INVAL;
+    if (A > 0 && (!active_p || !active_b)) return DLLM_ERR_INVAL;
+    for (int k = 0; k < n_pending; ++k) {
+        if (pending_p[k] < 0 || (k > 0 && pending_p[k] < pending_p[k - 1])) return DLLM_ERR_INVAL;
+    }
+    long long w_cur = 0;
+    for (int i = 0; i < A; ++i) {
+        if (active_p[i] < 0 || active_b[i] < 0) return DLLM_ERR_INVAL;
+        w_cur = std::max(w_cur, (long long)active_p[i] + ((long long)active_b[i] + 1) * L);
+    }
+    long long count = A;
+    // left: slot k + 1 stands for queue entry k, slot 0 for "none"; find()
+    // gives the nearest free slot at or below.  right: find() gives the
+    // nearest free entry at or above (n_pending for "none").
+    NextFree left(n_pending), right(n_pending);
+    auto take = [&](int k) {
+        left.parent[k + 1] = k;
+        right.parent[k] = k + 1;
+    };
+    auto free_at_or_below = [&](int k) { return left.find(k + 1) - 1; };
+    auto free_at_or_above = [&](int k) { return right.find(k); };
+    int n = 0;
+    while (true) {
+        const int head = free_at_or_above(0);
+        if (head >= n_pending) break;
+        int cand = -1;
+        const long long lim = w_cur - L;   // fits without widening: p + L <= w_cur
+        if (lim >= 0) {
+            const int hi = int(std::upper_bound(pending_p, pending_p + n_pending, lim) - pending_p) - 1;
+            const int k = hi >= 0 ? free_at_or_below(hi) : -1;
+            if (k >= 0) {
+                const int lo = int(std::lower_bound(pending_p, pending_p + n_pending, pending_p[k]) - pending_p);
+                cand = free_at_or_above(lo);   // earliest free entry of the same length
+            }
+        }
+        if (cand < 0) cand = head;
+        const long long w_new = std::max(w_cur, (long long)pending_p[cand] + L);
+        if ((count + 1) * w_new > budget) break;
+        take(cand);
+        admit_idx[n++] = cand;
+        ++count;
+        w_cur = w_new;
+    }
+    *n_admit = n;
+    return DLLM_OK;
+}
+
+extern "C" int dllm_pack(const dllm_pack_args* a, void* stream) {
+    if (!a || a->A < 0 || a->L < 1 || a->W < 0) return DLLM_ERR_INVAL;
+    if (a->A == 0 || a->W == 0) return DLLM_OK;
+    if (!a->p || !a->b || !a->rid || !a->prompt_off || !a->prompt_tokens || !a->block_ids || !a->ids)
+        return DLLM_ERR_INVAL;
+    if (!a->gen_tokens || a->ld_gen < 0) return DLLM_ERR_INVAL;
+    PackParams P;
+    P.A = a->A; P.L = a->L; P.W = a->W; P.pad_id = a->pad_id;
+    P.p = a->p; P.b = a->b; P.rid = a->rid; P.prompt_off = reinterpret_cast<const long long*>(a->prompt_off);
+    P.prompt_tokens = a->prompt_tokens; P.gen_tokens = a->gen_tokens; P.ld_gen = a->ld_gen;
+    P.block_ids = a->block_ids; P.ids = a->ids; P.attn = a->attn; P.pos = a->pos; P.pad = a->pad;
+    P.blk_start = a->blk_start;
+    P.err = error_word_ptr();
+    if (!P.err) return DLLM_ERR_CUDA;
+    const long long total = (long long)a->A * a->W;
+    const int sms = sm_count();
+    long long blocks = (total + 255) / 256;
+    blocks = std::min<long long>(blocks, (long long)std::max(sms, 1) * 8);
+    pack_kernel<<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(P);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    return DLLM_OK;
+}
+
+extern "C" int dllm_advance(const dllm_advance_args* a, void* stream) {
+    if (!a || a->A < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->ld_gen < 0) return DLLM_ERR_INVAL;
+    if (a->A == 0) return DLLM_OK;
+    if (!a->advance || !a->rid || !a->K || !a->b || !a->input_ids || !a->conf_state || !a->gen_tokens || !a->evict)
+        return DLLM_ERR_INVAL;
+    AdvanceParams P;
+    P.A = a->A; P.L = a->L; P.mask_id = a->mask_id;
+    P.advance = a->advance; P.rid = a->rid; P.K = a->K; P.b = a->b; P.ids = a->input_ids;
+    P.cs = a->conf_state; P.gen = a->gen_tokens; P.ld_gen = a->ld_gen; P.evict = a->evict;
+    P.err = error_word_ptr();
+    if (!P.err) return DLLM_ERR_CUDA;
+    const int wpb = 8;
+    advance_kernel<<<(a->A + wpb - 1) / wpb, wpb * 32, 0, as_stream(stream)>>>(P);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    return DLLM_OK;
+}
+
+extern "C" size_t dllm_compact_workspace_size(int32_t A, int32_t n_arrays, const int64_t* row_bytes) {
+    if (A < 0 || n_arrays < 0 || n_arrays > DLLM_COMPACT_MAX_ARRAYS) return 0;
+    if (n_arrays > 0 && !row_bytes) return 0;
+    for (int k = 0; k < n_arrays; ++k)
+        if (row_bytes[k] <= 0) return 0;
+    return compact_ws_bytes(A, n_arrays, row_bytes);
+}
+
+extern "C" int dllm_compact(const dllm_compact_args* a, void* stream) {
+    if (!a || a->A < 0 || a->n_arrays < 0 || a->n_arrays > DLLM_COMPACT_MAX_ARRAYS) return DLLM_ERR_INVAL;
+    if (!a->A_out) return DLLM_ERR_INVAL;
+    cudaStream_t s = as_stream(stream);
+    if (a->A == 0) {
+        DLLM_CUDA_TRY(cudaMemsetAsync(a->A_out, 0, sizeof(int32_t), s));
+        return DLLM_OK;
+    }
+    if (!a->evict) return DLLM_ERR_INVAL;
+    for (int k = 0; k < a->n_arrays; ++k)
+        if (!a->arrays[k] || a->row_bytes[k] <= 0) return DLLM_ERR_INVAL;
+    const size_t need = compact_ws_bytes(a->A, a->n_arrays, a->row_bytes);
+    if (a->n_arrays > 0 && (!a->workspace || a->workspace_bytes < need)) return DLLM_ERR_WORKSPACE;
+    CompactParams P;
+    P.A = a->A; P.n_arrays = a->n_arrays; P.evict = a->evict; P.new_index = a->new_index;
+    P.src_row = a->src_row; P.A_out = a->A_out;
+    size_t off = 0;
+    unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+    for (int k = 0; k < DLLM_COMPACT_MAX_ARRAYS; ++k) {
+        P.arrays[k] = nullptr;
+        P.stage[k] = nullptr;
+        P.row_bytes[k] = 0;
+        if (k < a->n_arrays) {
+            P.arrays[k] = static_cast<unsigned char*>(a->arrays[k]);
+            P.row_bytes[k] = a->row_bytes[k];
+            P.stage[k] = ws + off;
+            off += (size_t(a->A) * size_t(a->row_bytes[k]) + 255) & ~size_t(255);
+        }
+    }
+    const int blocks = (a->A + kCompactRows - 1) / kCompactRows;
+    compact_scatter_kernel<<<blocks, kCompactRows, 0, s>>>(P);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    if (a->n_arrays > 0) {
+        const int sms = std::max(sm_count(), 1);
+        const int cb = std::min((a->A + 7) / 8, sms * 4);
+        compact_copyback_kernel<<<cb, 256, 0, s>>>(P);
+        DLLM_CUDA_TRY(cudaGetLastError());
+    }
+    return DLLM_OK;
+}

@@ -1,0 +1,788 @@
+// dllm_step and dllm_features: the denoise step of block-wise diffusion-LLM
+// serving (S1-S6), one fused, persistent kernel per call.
+//
+// Method (FDFO page "FDFO: 让 dLLM 推理从「整批等最慢」变成「谁先完成谁先走」",
+// sections "工程设计一" and "工程设计二"; DiLaServe review, sections 3.1 and
+// 4.2 item ③): for every masked position read the bf16 logits row, take the
+// softmax probability of the argmax token as its confidence, unmask the
+// positions above the request's threshold (or the single most confident one),
+// write the tokens, report done / accept_length and the confidence features.
+//
+// Kernel design (GB300, 152 SMs, one CTA per SM):
+//   S1  every CTA scans input_ids (warp ballots) to rank the masked rows and
+//       splits the masked-row element stream evenly over the grid.
+//   S2  work unit = one fixed 16384-element chunk of one masked row.  Each of
+//       the 8 warps of a CTA runs its own 3-stage pipeline of 8 KB bulk copies
+//       (cp.async.bulk, TMA engine, L2 evict-first) into shared memory and
+//       keeps a per-lane online (max, sum-exp) over 64-element batches
+//       (packed bf16x2 max, one FFMA + one MUFU.EX2 + one FADD per element).
+//       The warp's butterfly reduction gives the chunk partial (max, sum,
+//       first batch holding the max).
+//   Row finisher: the warp whose chunk completes a row (atomic counter) folds
+//       the row's chunk partials in chunk order, finds the argmax index by
+//       re-reading only the 2048-element batch that holds the first maximum,
+//       and writes conf = 1/s, lse = m + ln s, tok.
+//   Request finisher: the warp completing a request's last masked row runs
+//       S3-S6 for it with warp shuffles (selection, fallback, update, done,
+//       quantile features by rank).
+// The chunk split, lane mapping and fold order depend only on V, so results
+// are bit-identical whatever else is in the batch.  Nothing spins on another
+// CTA: counters only elect the last arriver.  input_ids is written only after
+// every CTA has finished scanning it (otherwise the grid's last CTA to exit
+// writes it), so a CTA that starts late still sees the entry state.
+
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dllm {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kCopyElems = 4096;                    // one bulk copy: 8 KB
+constexpr int kCopyBytes = kCopyElems * 2;
+constexpr int kBatchVecs = 8;                       // 16-byte vectors per lane per batch
+constexpr int kBatchElems = kBatchVecs * 8 * 32;    // 2048 contiguous elements
+constexpr int kBatchesPerCopy = kCopyElems / kBatchElems;
+constexpr int kChunkElems = 16384;                  // fixed reduction chunk of a row
+constexpr int kBatchesPerChunk = kChunkElems / kBatchElems;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;    // 4 s per bulk copy
+
+static_assert(kChunkElems % kCopyElems == 0, "chunk must hold whole copies");
+static_assert(kCopyElems % kBatchElems == 0, "copy must hold whole batches");
+
+struct Partial {
+    float m;    // chunk max
+    float s;    // sum of exp(x - m) over the chunk
+    int kb;     // first batch of the chunk holding m
+    int pad;
+};
+
+struct StepParams {
+    int B, L, V, NC, BL, mask_id, list_cap, zero_cap;
+    long long ldv;
+    const uint16_t* logits;
+    int* ids;
+    const float* thr;
+    float* cs;
+    uint8_t* done;
+    int* accept;
+    int* n_new;
+    float* feats;
+    float* conf_out;
+    float* lse_out;
+    int* tok_out;
+    int* ctl;        // [0] CTAs done scanning, [1] CTAs exited
+    int* cnt;        // [BL] row counters, [B] request counters, [B] committed flags
+    Partial* part;   // [BL * NC]
+    float* row_conf;
+    float* row_lse;
+    int* row_tok;
+    uint8_t* sel;
+    int* err;
+};
+
+// Workspace layout.  The first quarter holds everything that must be zero
+// between calls (control words and counters); per-call data sits at the end,
+// so calls of different shapes never put data on each other's counters.
+struct WsLayout {
+    size_t front, counters_bytes, data_bytes;
+    size_t off_part, off_conf, off_lse, off_tok, off_sel;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline bool ws_layout(long long B, long long L, long long V, size_t bytes, WsLayout* w) {
+    const long long BL = B * L;
+    const long long NC = (V + kChunkElems - 1) / kChunkElems;
+    w->counters_bytes = 64 + 4 * size_t(BL + 2 * B);
+    size_t d = 0;
+    w->off_part = d; d = align256(d + size_t(BL * NC) * sizeof(Partial));
+    w->off_conf = d; d = align256(d + size_t(BL) * 4);
+    w->off_lse = d;  d = align256(d + size_t(BL) * 4);
+    w->off_tok = d;  d = align256(d + size_t(BL) * 4);
+    w->off_sel = d;  d = align256(d + size_t(BL));
+    w->data_bytes = d;
+    w->front = (bytes / 4) & ~size_t(255);
+    return w->counters_bytes <= w->front && w->data_bytes + w->front <= bytes;
+}
+
+inline size_t ws_required(long long B, long long L, long long V) {
+    WsLayout w;
+    ws_layout(B, L, V, 0, &w);
+    size_t need = w.counters_bytes * 4;
+    const size_t need_data = (w.data_bytes * 4 + 2) / 3 + 256;
+    if (need_data > need) need = need_data;
+    need = align256(need + 256);
+    while (!ws_layout(B, L, V, need, &w)) need += 256;
+    return need;
+}
+
+// ---------------------------------------------------------------------------
+// Per-lane batch processing.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float max64(const uint4 (&v)[kBatchVecs]) {
+    uint32_t a = bf16x2_max(v[0].x, v[0].y), b = bf16x2_max(v[0].z, v[0].w);
+#pragma unroll
+    for (int k = 1; k < kBatchVecs; ++k) {
+        a = bf16x2_max(a, bf16x2_max(v[k].x, v[k].y));
+        b = bf16x2_max(b, bf16x2_max(v[k].z, v[k].w));
+    }
+    a = bf16x2_max(a, b);
+    return fmaxf(bf16_lo(a), bf16_hi(a));
+}
+
+// Fold one 64-element batch into the lane's running (m, s, kb).
+__device__ __forceinline__ void fold_batch(const uint4 (&v)[kBatchVecs], int kbatch, float& m, float& s,
+                                           int& kb) {
+    const float bm = max64(v);
+    if (bm > m) {
+        s *= ex2_approx((m - bm) * kLog2e);
+        m = bm;
+        kb = kbatch;
+    }
+    if (m == -INFINITY) return;   // nothing finite seen yet: the batch adds 0
+    const float nb = -m * kLog2e;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int k = 0; k < kBatchVecs; ++k) {
+        a0 += ex2_approx(fmaf(bf16_lo(v[k].x), kLog2e, nb));
+        a1 += ex2_approx(fmaf(bf16_hi(v[k].x), kLog2e, nb));
+        a2 += ex2_approx(fmaf(bf16_lo(v[k].y), kLog2e, nb));
+        a3 += ex2_approx(fmaf(bf16_hi(v[k].y), kLog2e, nb));
+        a0 += ex2_approx(fmaf(bf16_lo(v[k].z), kLog2e, nb));
+        a1 += ex2_approx(fmaf(bf16_hi(v[k].z), kLog2e, nb));
+        a2 += ex2_approx(fmaf(bf16_lo(v[k].w), kLog2e, nb));
+        a3 += ex2_approx(fmaf(bf16_hi(v[k].w), kLog2e, nb));
+    }
+    s += (a0 + a1) + (a2 + a3);
+}
+
+// Replace the elements of a bf16 pair that lie beyond the row by -inf.
+// `valid`: how many of the pair's two elements are inside the row.
+__device__ __forceinline__ uint32_t mask_word(uint32_t w, int valid) {
+    if (valid <= 0) return 0xff80ff80u;
+    if (valid == 1) return (w & 0x0000ffffu) | 0xff800000u;
+    return w;
+}
+
+// One copy (up to 4096 elements) from shared memory.
+template <bool kFull>
+__device__ __forceinline__ void process_copy(const uint4* buf, int lane, int q, int nel, float& m, float& s,
+                                             int& kb) {
+#pragma unroll
+    for (int h = 0; h < kBatchesPerCopy; ++h) {
+        uint4 v[kBatchVecs];
+#pragma unroll
+        for (int k = 0; k < kBatchVecs; ++k) {
+            const int vi = lane + 32 * (h * kBatchVecs + k);
+            if (kFull) {
+                v[k] = buf[vi];
+            } else {
+                const int valid = nel - vi * 8;   // elements of this vector inside the copy
+                if (valid >= 8) {
+                    v[k] = buf[vi];
+                } else if (valid <= 0) {
+                    v[k] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                } else {
+                    uint4 t = buf[vi];
+                    t.x = mask_word(t.x, valid);
+                    t.y = mask_word(t.y, valid - 2);
+                    t.z = mask_word(t.z, valid - 4);
+                    t.w = mask_word(t.w, valid - 6);
+                    v[k] = t;
+                }
+            }
+        }
+        fold_batch(v, q * kBatchesPerCopy + h, m, s, kb);
+    }
+}
+
+// Combine two (max, sum) pairs; exact when one side is empty (-inf, 0).
+__device__ __forceinline__ void combine(float& m, float& s, float mo, float so) {
+    const float mn = fmaxf(m, mo);
+    const float a = (m == mn) ? s : s * ex2_approx((m - mn) * kLog2e);
+    const float b = (mo == mn) ? so : so * ex2_approx((mo - mn) * kLog2e);
+    s = a + b;
+    m = mn;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) - 1u; }
+
+// ---------------------------------------------------------------------------
+// Features of one block (warp-cooperative), DiLaServe review section 4.2 ③.
+// val[k] / inU[k] describe position j = lane + 32 k.  Writes feats[0..5].
+// ---------------------------------------------------------------------------
+__device__ __noinline__ void warp_features(const float* val, const bool* inU, int nk, int L, int lane,
+                                           float* feats_out) {
+    int n = 0;
+    float sum = 0.f;
+    for (int k = 0; k < nk; ++k) {
+        if (inU[k]) {
+            ++n;
+            sum += val[k];
+        }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        n += __shfl_xor_sync(0xffffffffu, n, off);
+        sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
+    float f[6];
+    if (n == 0) {
+        f[0] = f[1] = f[2] = f[3] = f[4] = __int_as_float(0x7fc00000);
+        f[5] = 0.f;
+    } else {
+        // rank of each of my values among U (ties broken by position)
+        int rank[32];
+        for (int k = 0; k < nk; ++k) rank[k] = 0;
+        for (int jj = 0; jj < L; ++jj) {
+            const int src = jj & 31, kk = jj >> 5;
+            float vo = 0.f;
+            bool uo = false;
+            for (int k = 0; k < nk; ++k) {   // fetch slot kk of lane src
+                const float tv = __shfl_sync(0xffffffffu, val[k], src);
+                const bool tu = __shfl_sync(0xffffffffu, inU[k] ? 1 : 0, src) != 0;
+                if (k == kk) {
+                    vo = tv;
+                    uo = tu;
+                }
+            }
+            if (!uo) continue;
+            for (int k = 0; k < nk; ++k) {
+                const int j = lane + 32 * k;
+                if (inU[k] && (vo < val[k] || (vo == val[k] && jj < j))) ++rank[k];
+            }
+        }
+        // order statistics needed: rank 0 and lo / hi of the three quantiles
+        const float qs[3] = {0.25f, 0.5f, 0.75f};
+        int want[7];
+        float frac[3];
+        want[0] = 0;
+        for (int t = 0; t < 3; ++t) {
+            const float h = qs[t] * float(n - 1);
+            const int lo = int(floorf(h));
+            frac[t] = h - float(lo);
+            want[1 + 2 * t] = lo;
+            want[2 + 2 * t] = min(lo + 1, n - 1);
+        }
+        float got[7];
+        for (int t = 0; t < 7; ++t) {
+            float mine = 0.f;
+            bool have = false;
+            for (int k = 0; k < nk; ++k) {
+                if (inU[k] && rank[k] == want[t]) {
+                    mine = val[k];
+                    have = true;
+                }
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, have);
+            got[t] = __shfl_sync(0xffffffffu, mine, __ffs(bal) - 1);
+        }
+        f[0] = got[0];
+        f[1] = got[1] + frac[0] * (got[2] - got[1]);
+        f[2] = got[3] + frac[1] * (got[4] - got[3]);
+        f[3] = sum / float(n);
+        f[4] = got[5] + frac[2] * (got[6] - got[5]);
+        f[5] = float(n) / float(L);
+    }
+    if (lane < 6) feats_out[lane] = f[lane];
+}
+
+// ---------------------------------------------------------------------------
+// S3-S6 for request b (one warp).  has_masked: b had masked rows at entry
+// (then every one of them has its row results in the workspace).
+// ---------------------------------------------------------------------------
+__device__ __noinline__ void finalize_request(const StepParams& P, int b, bool has_masked, int lane) {
+    __threadfence();
+    const int L = P.L;
+    const int nk = (L + 31) >> 5;
+    const long long base = (long long)b * L;
+    const float t = P.thr[b];
+
+    int id[32], tk[32];
+    float c[32];
+    bool msk[32];
+    bool any_masked = false, any_pass = false;
+    float best_c = -INFINITY;
+    int best_j = 0x7fffffff;
+    for (int k = 0; k < nk; ++k) {
+        const int j = lane + 32 * k;
+        const bool valid = j < L;
+        id[k] = valid ? P.ids[base + j] : 0;
+        msk[k] = valid && id[k] == P.mask_id;
+        c[k] = 0.f;
+        tk[k] = -1;
+        if (msk[k]) {
+            c[k] = __ldcg(P.row_conf + base + j);
+            tk[k] = __ldcg(P.row_tok + base + j);
+            any_masked = true;
+            if (c[k] > t) any_pass = true;
+            // j grows with k, so a strict > keeps the lowest position on ties
+            if (best_j == 0x7fffffff || c[k] > best_c) {
+                best_c = c[k];
+                best_j = j;
+            }
+        }
+    }
+    any_masked = __any_sync(0xffffffffu, any_masked);
+    any_pass = __any_sync(0xffffffffu, any_pass);
+    int fb_j = -1;
+    if (any_masked && !any_pass) {
+        // most confident masked position, lowest position on ties
+        float bc = best_c;
+        int bj = best_j;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const float oc = __shfl_xor_sync(0xffffffffu, bc, off);
+            const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+            if (oj != 0x7fffffff && (bj == 0x7fffffff || oc > bc || (oc == bc && oj < bj))) {
+                bc = oc;
+                bj = oj;
+            }
+        }
+        fb_j = bj;
+    }
+
+    float val[32];
+    bool inU[32];
+    bool selk[32];
+    int n_sel = 0;
+    bool still = false;
+    for (int k = 0; k < nk; ++k) {
+        const int j = lane + 32 * k;
+        const bool valid = j < L;
+        const bool s = msk[k] && (c[k] > t || j == fb_j);
+        selk[k] = s;
+        const int new_id = s ? tk[k] : id[k];
+        float new_cs = 0.f;
+        if (valid) {
+            new_cs = s ? c[k] : P.cs[base + j];
+            if (s) P.cs[base + j] = c[k];
+            if (has_masked) P.sel[base + j] = s ? 1 : 0;
+            if (!msk[k]) {
+                if (P.conf_out) P.conf_out[base + j] = __int_as_float(0x7fc00000);
+                if (P.lse_out) P.lse_out[base + j] = __int_as_float(0x7fc00000);
+                if (P.tok_out) P.tok_out[base + j] = -1;
+            }
+        }
+        n_sel += s ? 1 : 0;
+        still |= valid && new_id == P.mask_id;
+        inU[k] = valid && new_id != P.mask_id;
+        val[k] = new_cs;
+        id[k] = new_id;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) n_sel += __shfl_xor_sync(0xffffffffu, n_sel, off);
+    const bool done = !__any_sync(0xffffffffu, still);
+    if (lane == 0) {
+        P.done[b] = done ? 1 : 0;
+        P.accept[b] = done ? L : 0;
+        P.n_new[b] = n_sel;
+    }
+    if (P.feats) warp_features(val, inU, nk, L, lane, P.feats + (long long)b * DLLM_NUM_FEATURES);
+
+    // S4 commit of input_ids: only once every CTA has finished its scan.
+    int* committed = P.cnt + P.BL + P.B;
+    if (!has_masked) {
+        if (lane == 0) committed[b] = 1;
+        return;
+    }
+    __syncwarp();
+    const int scanned = (lane == 0) ? ld_acquire_gpu(P.ctl) : 0;
+    if (__shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
+        for (int k = 0; k < nk; ++k) {
+            if (selk[k]) P.ids[base + lane + 32 * k] = id[k];
+        }
+        if (lane == 0) committed[b] = 1;
+    }
+    if (lane == 0) P.cnt[P.BL + b] = 0;   // request counter back to rest
+}
+
+// ---------------------------------------------------------------------------
+// Row finisher: fold the chunk partials of `row`, locate the argmax, write
+// the row results; then count the row towards its request.
+// ---------------------------------------------------------------------------
+__device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) {
+    __threadfence();
+    const int NC = P.NC;
+    float M = -INFINITY, S = 0.f;
+    int cstar = 0, kbstar = 0;
+    for (int c0 = 0; c0 < NC; c0 += 32) {
+        float pm = -INFINITY, ps = 0.f;
+        int pk = 0;
+        if (c0 + lane < NC) {
+            const float4 raw = __ldcg(reinterpret_cast<const float4*>(P.part + (long long)row * NC + c0 + lane));
+            pm = raw.x;
+            ps = raw.y;
+            pk = __float_as_int(raw.z);
+        }
+        const int n = min(32, NC - c0);
+        for (int i = 0; i < n; ++i) {
+            const float mc = __shfl_sync(0xffffffffu, pm, i);
+            const float sc = __shfl_sync(0xffffffffu, ps, i);
+            const int kbc = __shfl_sync(0xffffffffu, pk, i);
+            if (mc > M) {
+                cstar = c0 + i;
+                kbstar = kbc;
+            }
+            combine(M, S, mc, sc);
+        }
+    }
+    if (kbstar >= kBatchesPerChunk) kbstar = 0;
+    // argmax: first element equal to M inside batch kbstar of chunk cstar
+    const long long start = (long long)cstar * kChunkElems + (long long)kbstar * kBatchElems;
+    const uint16_t* rp = P.logits + (long long)row * P.ldv;
+    unsigned best = 0xffffffffu;
+    for (int k = 0; k < kBatchVecs; ++k) {
+        const long long e = start + (long long)(lane + 32 * k) * 8;
+        if (e >= P.V) break;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + e));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int h = 0; h < 8; ++h) {
+            const float x = (h & 1) ? bf16_hi(w[h >> 1]) : bf16_lo(w[h >> 1]);
+            if (e + h < P.V && x == M) {
+                best = (unsigned)(e + h);
+                break;
+            }
+        }
+        if (best != 0xffffffffu) break;
+    }
+    best = __reduce_min_sync(0xffffffffu, best);
+    const float conf = __fdiv_rn(1.0f, S);
+    const float lse = M + logf(S);
+    const int b = row / P.L;
+    // masked rows of this request (its input_ids are unmodified until its
+    // own finisher commits, which happens after this count)
+    int mb = 0;
+    for (int j0 = 0; j0 < P.L; j0 += 32) {
+        const int j = j0 + lane;
+        const bool mk = j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id;
+        mb += __popc(__ballot_sync(0xffffffffu, mk));
+    }
+    int old = 0;
+    if (lane == 0) {
+        P.row_conf[row] = conf;
+        P.row_lse[row] = lse;
+        P.row_tok[row] = (int)best;
+        if (P.conf_out) P.conf_out[row] = conf;
+        if (P.lse_out) P.lse_out[row] = lse;
+        if (P.tok_out) P.tok_out[row] = (int)best;
+        P.cnt[row] = 0;
+        __threadfence();
+        old = atomicAdd(P.cnt + P.BL + b, 1);
+    }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == mb - 1) finalize_request(P, b, true, lane);
+}
+
+// ---------------------------------------------------------------------------
+// The step kernel.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kCopyBytes);
+    int* s_list = reinterpret_cast<int*>(bars + kWarps * kStages);
+    int* s_zero = s_list + P.list_cap;
+    __shared__ int s_warp_cnt[kWarps];
+    __shared__ int s_nzero;
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = gridDim.x, cta = blockIdx.x;
+
+    if (tid < kWarps * kStages) mbar_init(smem_addr(&bars[tid]), 1);
+    if (tid == 0) s_nzero = 0;
+    if (tid < kWarps * kStages) mbar_fence_init();
+
+    // ---- S1: rank the masked rows (entry state of input_ids) -------------
+    const int BL = P.BL;
+    const int seg = (((BL + kWarps - 1) / kWarps) + 31) & ~31;
+    const int s0 = min(BL, warp * seg), s1 = min(BL, s0 + seg);
+    int wcnt = 0;
+    for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        const bool mk = i < s1 && P.ids[i] == P.mask_id;
+        wcnt += __popc(__ballot_sync(0xffffffffu, mk));
+    }
+    if (lane == 0) s_warp_cnt[warp] = wcnt;
+    __syncthreads();
+    int before = 0, M = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int cw = s_warp_cnt[w];
+        if (w < warp) before += cw;
+        M += cw;
+    }
+    const int NC = P.NC;
+    const long long V = P.V;
+    const long long U = (long long)M * NC;
+    const long long E = (long long)M * V;
+    auto first_unit = [&](long long T) -> long long {
+        if (T >= E) return U;
+        long long r = T / V;
+        const long long rem = T - r * V;
+        long long cc = (rem + kChunkElems - 1) / kChunkElems;
+        if (cc >= NC) {
+            r += 1;
+            cc = 0;
+        }
+        return r * NC + cc;
+    };
+    const long long u0 = first_unit(E * cta / G);
+    const long long u1 = first_unit(E * (cta + 1) / G);
+    const long long r_lo = u0 / NC;
+    const long long r_hi = (u1 > u0) ? (u1 - 1) / NC : r_lo - 1;
+    int rank = before;
+    for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        const bool mk = i < s1 && P.ids[i] == P.mask_id;
+        const unsigned bal = __ballot_sync(0xffffffffu, mk);
+        const int my = rank + __popc(bal & lanemask_lt(lane));
+        if (mk && my >= r_lo && my <= r_hi) s_list[my - r_lo] = i;
+        rank += __popc(bal);
+    }
+    // requests of this CTA (b = cta + G*k) with no masked position
+    for (int k = warp; cta + (long long)G * k < P.B; k += kWarps) {
+        const int b = cta + G * k;
+        bool anym = false;
+        for (int j0 = 0; j0 < P.L; j0 += 32) {
+            const int j = j0 + lane;
+            anym |= __any_sync(0xffffffffu, j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id);
+        }
+        if (!anym && lane == 0) s_zero[atomicAdd(&s_nzero, 1)] = b;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(P.ctl, 1);   // this CTA no longer reads input_ids' entry state
+    }
+
+    // ---- S2: stream the masked rows, chunk by chunk -----------------------
+    const uint32_t stage0 = smem_addr(stages + warp * kStages * kCopyBytes);
+    const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
+    const uint64_t pol = l2_policy_evict_first();
+    const int V32 = P.V;
+    long long pu = u0 + warp;
+    int pq = 0;
+    uint32_t issued = 0, consumed = 0;
+    bool failed = false;
+
+    auto issue = [&]() {
+        if (pu >= u1) return;
+        const int cidx = (int)(pu % NC);
+        const int row = s_list[(int)(pu / NC - r_lo)];
+        const int clen = min(kChunkElems, V32 - cidx * kChunkElems);
+        const int e0 = cidx * kChunkElems + pq * kCopyElems;
+        const int nel = min(kCopyElems, clen - pq * kCopyElems);
+        const uint32_t bytes = (uint32_t)((nel * 2 + 15) & ~15);
+        const int slot = issued % kStages;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar0 + slot * 8, bytes);
+            bulk_g2s(stage0 + slot * kCopyBytes, P.logits + (long long)row * P.ldv + e0, bytes, bar0 + slot * 8,
+                     pol);
+        }
+        ++issued;
+        if (++pq * kCopyElems >= clen) {
+            pq = 0;
+            pu += kWarps;
+        }
+    };
+#pragma unroll 1
+    for (int st = 0; st < kStages; ++st) issue();
+
+#pragma unroll 1
+    for (long long u = u0 + warp; u < u1 && !failed; u += kWarps) {
+        const int cidx = (int)(u % NC);
+        const int row = s_list[(int)(u / NC - r_lo)];
+        const int clen = min(kChunkElems, V32 - cidx * kChunkElems);
+        const int ncp = (clen + kCopyElems - 1) / kCopyElems;
+        float m = -INFINITY, s = 0.f;
+        int kb = kBatchesPerChunk;
+#pragma unroll 1
+        for (int q = 0; q < ncp; ++q) {
+            const int slot = consumed % kStages;
+            const uint32_t par = (consumed / kStages) & 1u;
+            if (!mbar_wait_bounded(bar0 + slot * 8, par, kWaitLimitNs)) {
+                failed = true;
+                break;
+            }
+            const int nel = min(kCopyElems, clen - q * kCopyElems);
+            const uint4* buf = reinterpret_cast<const uint4*>(stages + (warp * kStages + slot) * kCopyBytes);
+            if (nel == kCopyElems) process_copy<true>(buf, lane, q, nel, m, s, kb);
+            else process_copy<false>(buf, lane, q, nel, m, s, kb);
+            __syncwarp();
+            ++consumed;
+            issue();
+        }
+        if (failed) break;
+        const float m_lane = m;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+            const float so = __shfl_xor_sync(0xffffffffu, s, off);
+            combine(m, s, mo, so);
+        }
+        const unsigned kbm =
+            __reduce_min_sync(0xffffffffu, (m_lane == m) ? (unsigned)kb : (unsigned)kBatchesPerChunk);
+        int old = 0;
+        if (lane == 0) {
+            float4 rec;
+            rec.x = m;
+            rec.y = s;
+            rec.z = __int_as_float((int)kbm);
+            rec.w = 0.f;
+            *reinterpret_cast<float4*>(P.part + (long long)row * NC + cidx) = rec;
+            __threadfence();
+            old = atomicAdd(P.cnt + row, 1);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == NC - 1) finish_row(P, row, lane);
+    }
+    if (failed) {
+        if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
+        // let this warp's copies in flight land before shared memory goes away
+        while (consumed < issued) {
+            const int slot = consumed % kStages;
+            if (!mbar_wait_bounded(bar0 + slot * 8, (consumed / kStages) & 1u, 100000000ull)) break;
+            ++consumed;
+        }
+    }
+
+    // ---- requests without masked rows -------------------------------------
+    __syncthreads();
+    for (int k = warp; k < s_nzero; k += kWarps) finalize_request(P, s_zero[k], false, lane);
+
+    // ---- exit: the last CTA commits deferred requests and resets ----------
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        s_last = (atomicAdd(P.ctl + 1, 1) == G - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        int* committed = P.cnt + P.BL + P.B;
+        for (long long idx = tid; idx < BL; idx += kThreads) {
+            const int b = (int)(idx / P.L);
+            if (__ldcg(committed + b) == 0 && P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
+        }
+        __syncthreads();
+        for (int b = tid; b < P.B; b += kThreads) committed[b] = 0;
+        if (tid == 0) {
+            P.ctl[0] = 0;
+            P.ctl[1] = 0;
+        }
+    }
+}
+
+// Standalone features: one warp per request.
+__global__ void __launch_bounds__(256) features_kernel(int B, int L, int mask_id, const int* ids, const float* cs,
+                                                      float* feats) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= B) return;
+    const int nk = (L + 31) >> 5;
+    float val[32];
+    bool inU[32];
+    for (int k = 0; k < nk; ++k) {
+        const int j = lane + 32 * k;
+        const bool valid = j < L;
+        const int id = valid ? ids[(long long)b * L + j] : mask_id;
+        inU[k] = valid && id != mask_id;
+        val[k] = valid ? cs[(long long)b * L + j] : 0.f;
+    }
+    warp_features(val, inU, nk, L, lane, feats + (long long)b * DLLM_NUM_FEATURES);
+}
+
+int g_smem_configured[64];
+
+}  // namespace
+}  // namespace dllm
+
+using namespace dllm;
+
+extern "C" size_t dllm_step_workspace_size(int32_t B, int32_t L, int32_t V) {
+    if (B < 0 || L < 1 || L > DLLM_MAX_L || V < 1) return 0;
+    return ws_required(B, L, V);
+}
+
+extern "C" int dllm_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (!workspace && bytes) return DLLM_ERR_INVAL;
+    if (!bytes) return DLLM_OK;
+    DLLM_CUDA_TRY(cudaMemsetAsync(workspace, 0, bytes, as_stream(stream)));
+    return DLLM_OK;
+}
+
+extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
+    if (!a) return DLLM_ERR_INVAL;
+    if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
+    if (a->B == 0) return DLLM_OK;
+    if ((long long)a->B * a->L > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
+    if (!a->logits || !a->input_ids || !a->thr || !a->conf_state || !a->done || !a->accept_len || !a->n_new)
+        return DLLM_ERR_INVAL;
+    if ((a->ldv % 8) != 0 || (reinterpret_cast<uintptr_t>(a->logits) & 15u) != 0) return DLLM_ERR_ALIGN;
+    if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return DLLM_ERR_WORKSPACE;
+    WsLayout w;
+    if (!ws_layout(a->B, a->L, a->V, a->workspace_bytes, &w)) return DLLM_ERR_WORKSPACE;
+
+    int dev = 0;
+    DLLM_CUDA_TRY(cudaGetDevice(&dev));
+    const int G = sm_count();
+    if (G <= 0) return DLLM_ERR_CUDA;
+    const int BL = a->B * a->L;
+    const int NC = (a->V + kChunkElems - 1) / kChunkElems;
+    const int list_cap = BL / G + 3;
+    const int zero_cap = a->B / G + 1;
+    const size_t smem = size_t(kWarps) * kStages * kCopyBytes + size_t(kWarps) * kStages * 8 +
+                        size_t(list_cap + zero_cap) * 4;
+    int max_optin = 0;
+    DLLM_CUDA_TRY(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    if (smem + 64 > size_t(max_optin)) return DLLM_ERR_UNSUPPORTED;
+    if (dev >= 0 && dev < 64) {
+        if (g_smem_configured[dev] < (int)smem) {
+            DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin));
+            g_smem_configured[dev] = max_optin;
+        }
+    } else {
+        DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    }
+
+    unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+    unsigned char* data = ws + ((a->workspace_bytes - w.data_bytes) & ~size_t(255));
+    StepParams P;
+    P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
+    P.list_cap = list_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
+    P.logits = a->logits; P.ids = a->input_ids; P.thr = a->thr; P.cs = a->conf_state;
+    P.done = a->done; P.accept = a->accept_len; P.n_new = a->n_new; P.feats = a->feats;
+    P.conf_out = a->conf_out; P.lse_out = a->lse_out; P.tok_out = a->tok_out;
+    P.ctl = reinterpret_cast<int*>(ws);
+    P.cnt = reinterpret_cast<int*>(ws + 64);
+    P.part = reinterpret_cast<Partial*>(data + w.off_part);
+    P.row_conf = reinterpret_cast<float*>(data + w.off_conf);
+    P.row_lse = reinterpret_cast<float*>(data + w.off_lse);
+    P.row_tok = reinterpret_cast<int*>(data + w.off_tok);
+    P.sel = data + w.off_sel;
+    P.err = error_word_ptr();
+    if (!P.err) return DLLM_ERR_CUDA;
+    step_kernel<<<G, kThreads, smem, as_stream(stream)>>>(P);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    return DLLM_OK;
+}
+
+extern "C" int dllm_features(int32_t B, int32_t L, int32_t mask_id, const int32_t* input_ids,
+                             const float* conf_state, float* feats, void* stream) {
+    if (B < 0 || L < 1 || L > DLLM_MAX_L) return DLLM_ERR_INVAL;
+    if (B == 0) return DLLM_OK;
+    if (!input_ids || !conf_state || !feats) return DLLM_ERR_INVAL;
+    const int wpb = 8;
+    features_kernel<<<(B + wpb - 1) / wpb, wpb * 32, 0, as_stream(stream)>>>(B, L, mask_id, input_ids, conf_state,
+                                                                          feats);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    return DLLM_OK;
+}

@@ -1,0 +1,286 @@
+/*
+ * dllm.h -- C ABI of libdllm.so: the data-parallel hot path of block-wise
+ * diffusion-LLM serving on one GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   FDFO page      "FDFO: 让 dLLM 推理从「整批等最慢」变成「谁先完成谁先走」"
+ *                  (write-up of SGLang PRs #27551 / #27877)
+ *   BlockServe     "BlockServe: 块粒度连续批处理实现高吞吐扩散大语言模型服务"
+ *   DiLaServe      "DiLaServe: High SLO Attainment Serving for Diffusion
+ *                  Language Models" (paper review)
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns int: DLLM_OK (0) or a negative DLLM_ERR_* code.
+ *     Nothing is thrown across the ABI.  dllm_strerror() names a code.
+ *   - "device" pointers are caller-owned CUDA device memory on the current
+ *     device; "host" pointers are ordinary host memory.  The library never
+ *     allocates or frees memory and never keeps a pointer after returning.
+ *   - Device entry points are asynchronous on `stream` (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream).  Only
+ *     dllm_get_device_error() synchronises.
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and changes nothing.
+ *   - Conditions only the device can see (an inconsistent row width in
+ *     dllm_pack, an expired wait) are recorded in a per-device error word,
+ *     read and cleared by dllm_get_device_error().  Kernels never trap.
+ *   - Integer widths are fixed (int32_t / int64_t); bf16 data is passed as
+ *     raw 16-bit patterns (uint16_t).
+ */
+#ifndef DLLM_H
+#define DLLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DLLM_ABI_VERSION 1
+
+#define DLLM_OK 0
+#define DLLM_ERR_INVAL (-1)       /* a size, pointer or value is out of range */
+#define DLLM_ERR_ALIGN (-2)       /* a pointer or stride breaks an alignment rule */
+#define DLLM_ERR_CUDA (-3)        /* a CUDA runtime call failed */
+#define DLLM_ERR_DEVICE (-4)      /* the device error word was set (see below) */
+#define DLLM_ERR_WORKSPACE (-5)   /* workspace missing or too small */
+#define DLLM_ERR_UNSUPPORTED (-6) /* shape beyond this build's limits */
+
+/* Device error word values (read with dllm_get_device_error). */
+#define DLLM_DEVERR_NONE 0
+#define DLLM_DEVERR_TIMEOUT 1     /* a bounded wait on a bulk copy expired */
+#define DLLM_DEVERR_ROW_WIDTH 2   /* dllm_pack: p + (b + 1) * L > W for a row */
+#define DLLM_DEVERR_BLOCK_INDEX 3 /* dllm_advance: block index outside [0, K) or output row too short */
+
+#define DLLM_MAX_L 1024
+#define DLLM_NUM_FEATURES 6
+#define DLLM_COMPACT_MAX_ARRAYS 16
+
+/* Describe a status code (static string; never NULL). */
+const char* dllm_strerror(int code);
+
+/* ABI version of the loaded library (DLLM_ABI_VERSION). */
+int dllm_abi_version(void);
+
+/* sizeof() of the argument structs below, for binding self-checks:
+ * which = 0 dllm_step_args, 1 dllm_pack_args, 2 dllm_compact_args,
+ * 3 dllm_advance_args.  Returns 0 for an unknown `which`. */
+size_t dllm_struct_size(int which);
+
+/* Synchronise `stream`, then return in *code the first device error
+ * recorded on the current device since the last call (DLLM_DEVERR_*), and
+ * clear it.  Returns DLLM_ERR_CUDA if the synchronisation fails. */
+int dllm_get_device_error(void* stream, int32_t* code);
+
+/* ======================================================================
+ * dllm_step -- one denoise step over a mixed-state batch (S1-S6).
+ *
+ * FDFO page, section "工程设计一": step(forward_batch, full_logits, states)
+ * -> done_flags reads the current logits, updates forward_batch.input_ids
+ * by the algorithm's rule and reports, per block, whether it is complete.
+ * The rule is LowConfidence (same section; DiLaServe review, section 3.1):
+ * for every masked position take the softmax probability of the argmax
+ * token as its confidence; unmask positions whose confidence exceeds the
+ * request's threshold; if none does, unmask the single most confident one.
+ *
+ * Per request b (row block of L positions) and masked position j
+ * (input_ids[b][j] == mask_id at entry), over x = logits row b*L + j:
+ *   m = max_v x_v; tok = lowest v with x_v == m;
+ *   s = sum_v exp(x_v - m); conf = 1 / s; lse = m + ln(s).
+ * Selection: sel = { masked j : conf_j > thr[b] } (strict, float32); if sel
+ *   is empty and some position is masked, sel = { the masked j of largest
+ *   conf, lowest j on ties }.
+ * Update: input_ids[b][j] = tok_j and conf_state[b][j] = conf_j for j in sel.
+ * Outputs (FDFO page, section "工程设计二": accept_length is 0 while the
+ * block continues and block_size once it can be committed):
+ *   n_new[b]      = |sel|
+ *   done[b]       = 1 iff no position of block b holds mask_id afterwards
+ *   accept_len[b] = done[b] ? L : 0
+ *   feats[b][0..5] (DiLaServe review, section 4.2 item ③) over the block's
+ *     positions not holding mask_id afterwards, values conf_state[b][j]:
+ *     min, q25, median, mean, q75 (linear interpolation at rank q*(n-1) of
+ *     the ascending values) and n / L; NaN x5 and 0 when n == 0.
+ *   conf_out / lse_out / tok_out (optional): per position, the row results
+ *     for positions masked at entry, NaN / NaN / -1 elsewhere.
+ *
+ * Only rows of positions masked at entry are read; other logits rows may
+ * hold anything.  Rows must hold at least one finite value.  The reduction
+ * order of every row depends only on V, so a request's results are
+ * bit-identical whatever else is in the batch.
+ * ====================================================================== */
+typedef struct dllm_step_args {
+    int32_t B;                  /* requests (>= 0) */
+    int32_t L;                  /* block length, 1..DLLM_MAX_L */
+    int32_t V;                  /* vocabulary size (>= 1) */
+    int32_t mask_id;            /* token id marking a masked position */
+    int64_t ldv;                /* logits row stride in elements: >= V, multiple of 8 */
+    const uint16_t* logits;     /* device bf16 [B*L][ldv]; row b*L+j = position j of request b;
+                                   16-byte aligned; all B*L*ldv elements addressable */
+    int32_t* input_ids;         /* device [B][L], in/out (the block's tokens) */
+    const float* thr;           /* device [B] per-request threshold */
+    float* conf_state;          /* device [B][L], in/out: confidence recorded at unmask time
+                                   (the per-request algorithm state carried between rounds);
+                                   finite wherever input_ids != mask_id */
+    uint8_t* done;              /* device [B] out */
+    int32_t* accept_len;        /* device [B] out */
+    int32_t* n_new;             /* device [B] out */
+    float* feats;               /* device [B][6] out, or NULL */
+    float* conf_out;            /* device [B][L] out, or NULL */
+    float* lse_out;             /* device [B][L] out, or NULL */
+    int32_t* tok_out;           /* device [B][L] out, or NULL */
+    void* workspace;            /* device, >= dllm_step_workspace_size() bytes, 256-byte aligned,
+                                   zero-filled before first use (dllm_workspace_init); every
+                                   completed call leaves it ready for the next */
+    size_t workspace_bytes;
+} dllm_step_args;
+
+/* Workspace bytes dllm_step needs for this shape (0 if the shape is invalid).
+ * A workspace sized for (B, L, V) also serves every call with B' <= B,
+ * B'*L' <= B*L and B'*L'*ceil(V'/16384) <= B*L*ceil(V/16384): its first
+ * quarter holds the counters that must be zero between calls and the
+ * rest the per-call data, so no call's data lands on another's counters.
+ * Calls sharing a workspace must be ordered on one stream.  After a device
+ * error (DLLM_DEVERR_TIMEOUT) re-initialise it. */
+size_t dllm_step_workspace_size(int32_t B, int32_t L, int32_t V);
+
+/* cudaMemsetAsync(workspace, 0, bytes) on `stream`. */
+int dllm_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Run S1-S6.  Errors: DLLM_ERR_INVAL (shape, NULL required pointer),
+ * DLLM_ERR_ALIGN (logits not 16-byte aligned, ldv % 8 != 0),
+ * DLLM_ERR_WORKSPACE, DLLM_ERR_UNSUPPORTED, DLLM_ERR_CUDA.  A NaN threshold
+ * never passes.  input_ids and conf_state may not alias any output. */
+int dllm_step(const dllm_step_args* args, void* stream);
+
+/* S6 alone: feats[b][0..5] from input_ids / conf_state as defined above
+ * (DiLaServe review, section 4.2 item ③).  All pointers device. */
+int dllm_features(int32_t B, int32_t L, int32_t mask_id, const int32_t* input_ids,
+                  const float* conf_state, float* feats, void* stream);
+
+/* ======================================================================
+ * Bounding-box planning and admission (host functions).
+ *
+ * BlockServe page, section II-D, eq. (1):
+ *   Cost(A) = |A| * max_{i in A} (p_i + (b_i + 1) * L).
+ * ====================================================================== */
+
+/* Host.  W = max_i (p[i] + (b[i] + 1) * L) (0 when A == 0) and
+ * cost = A * W.  p, b: host [A], p >= 0, b >= 0.  W and cost may be NULL. */
+int dllm_pack_plan(int32_t A, const int32_t* p, const int32_t* b, int32_t L,
+                   int32_t* W, int64_t* cost);
+
+/* Host.  Length-aware greedy ("sand-fill") admission, BlockServe page,
+ * section II-D and Algorithm 1 (section II-C):
+ *   repeat: let W_cur be the active box width; among the remaining pending
+ *   requests whose starting width p + L fits within W_cur, take the longest
+ *   prompt (earliest in the queue on ties); if none fits, take the head of
+ *   the queue; admit it iff Cost(A plus it, at b = 0) <= budget, else stop.
+ * pending_p: host [n_pending], sorted ascending (the queue order).
+ * active_p, active_b: host [A] of the active set (may be NULL when A == 0).
+ * admit_idx: host [n_pending] out, indices into pending_p in admission
+ * order; *n_admit receives their count. */
+int dllm_admit(int32_t n_pending, const int32_t* pending_p, int32_t A,
+               const int32_t* active_p, const int32_t* active_b, int32_t L,
+               int64_t budget, int32_t* admit_idx, int32_t* n_admit);
+
+/* ======================================================================
+ * dllm_pack -- materialise the box (S7), BlockServe page, section II-E
+ * ("逻辑位置对齐" and "向量化混合调度执行").
+ *
+ * Row i (request rid[i], prompt length p[i], block index b[i]):
+ *   width_i = p[i] + (b[i] + 1) * L;  pad_i = W - width_i
+ *   ids[i]  = [pad_id x pad_i, prompt tokens, gen_tokens[rid][0 : b*L],
+ *              block_ids[i][0 : L]]
+ *   attn[i][c] = c >= pad_i;  pos[i][c] = max(c - pad_i, 0)
+ *     (the cumulative index over the attention mask, first real token at 0)
+ *   blk_start[i] = p[i] + b[i] * L, the logical position of the active
+ *     block, which always occupies box columns [W - L, W) (the gather /
+ *     scatter region of every row).
+ * A row with width_i > W is skipped and sets DLLM_DEVERR_ROW_WIDTH.
+ * ====================================================================== */
+typedef struct dllm_pack_args {
+    int32_t A;                    /* rows */
+    int32_t L;                    /* block length */
+    int32_t W;                    /* box width (dllm_pack_plan) */
+    int32_t pad_id;
+    const int32_t* p;             /* device [A] prompt length per row */
+    const int32_t* b;             /* device [A] block index per row */
+    const int32_t* rid;           /* device [A] request id per row */
+    const int64_t* prompt_off;    /* device [R + 1]: prompt of request r is
+                                     prompt_tokens[prompt_off[r] : prompt_off[r] + p] */
+    const int32_t* prompt_tokens; /* device */
+    const int32_t* gen_tokens;    /* device [R][ld_gen]: committed blocks of request r */
+    int64_t ld_gen;
+    const int32_t* block_ids;     /* device [A][L]: current block of each row */
+    int32_t* ids;                 /* device [A][W] out */
+    uint8_t* attn;                /* device [A][W] out, or NULL */
+    int32_t* pos;                 /* device [A][W] out, or NULL */
+    int32_t* pad;                 /* device [A] out, or NULL */
+    int32_t* blk_start;           /* device [A] out, or NULL */
+} dllm_pack_args;
+
+int dllm_pack(const dllm_pack_args* args, void* stream);
+
+/* ======================================================================
+ * dllm_advance -- commit finished blocks (BlockServe Algorithm 1: update
+ * r_i's outputs with its block, b_i <- b_i + 1, evict when b_i >= K_i;
+ * FDFO page, section "FDFO 的核心思想": a request whose block is done
+ * commits at once).
+ *
+ * For every row i with advance[i] != 0:
+ *   gen_tokens[rid[i]][b[i]*L : (b[i]+1)*L] = input_ids[i][0 : L];
+ *   b[i] += 1;  evict[i] = (b[i] >= K[i]);
+ *   if not evicted: input_ids[i][:] = mask_id, conf_state[i][:] = NaN
+ *   (every block starts fully masked, BlockServe section II-E).
+ * Rows with advance[i] == 0 get evict[i] = 0 and are untouched.
+ * ====================================================================== */
+typedef struct dllm_advance_args {
+    int32_t A;
+    int32_t L;
+    int32_t mask_id;
+    int32_t pad0;
+    const uint8_t* advance;   /* device [A] */
+    const int32_t* rid;       /* device [A] */
+    const int32_t* K;         /* device [A] blocks to generate */
+    int32_t* b;               /* device [A] in/out */
+    int32_t* input_ids;       /* device [A][L] in/out */
+    float* conf_state;        /* device [A][L] in/out */
+    int32_t* gen_tokens;      /* device [R][ld_gen] out (rows of advanced requests) */
+    int64_t ld_gen;           /* >= K * L for every request */
+    uint8_t* evict;           /* device [A] out */
+} dllm_advance_args;
+
+int dllm_advance(const dllm_advance_args* args, void* stream);
+
+/* ======================================================================
+ * dllm_compact -- stable compaction for FDFO eviction (S9).
+ *
+ * keep[i] = !evict[i];  new_index[i] = number of kept rows before i (or -1
+ * when evicted);  src_row[k] = the k-th kept row;  *A_out = kept rows.
+ * Every listed row-major array is compacted in place: row k becomes old row
+ * src_row[k] for k < A_out (rows >= A_out are left unspecified).  Survivors
+ * keep their order; refills are appended after them by the caller.
+ * ====================================================================== */
+typedef struct dllm_compact_args {
+    int32_t A;                                   /* rows */
+    int32_t n_arrays;                            /* 0..DLLM_COMPACT_MAX_ARRAYS */
+    const uint8_t* evict;                        /* device [A] */
+    int32_t* new_index;                          /* device [A] out, or NULL */
+    int32_t* src_row;                            /* device [A] out (first A_out valid), or NULL */
+    int32_t* A_out;                              /* device [1] out */
+    void* arrays[DLLM_COMPACT_MAX_ARRAYS];       /* device, A rows each */
+    int64_t row_bytes[DLLM_COMPACT_MAX_ARRAYS];  /* bytes per row (> 0) */
+    void* workspace;                             /* device, dllm_compact_workspace_size() bytes */
+    size_t workspace_bytes;
+} dllm_compact_args;
+
+/* Workspace bytes for dllm_compact over these arrays (0 if invalid). */
+size_t dllm_compact_workspace_size(int32_t A, int32_t n_arrays, const int64_t* row_bytes);
+
+int dllm_compact(const dllm_compact_args* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLLM_H */
