@@ -1,0 +1,118 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, the binding's structs match, host-side validation rejects
+bad arguments before any CUDA call, and the native host planners
+(eq. (1), sand-fill admission) agree with the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import denoise_step_token_gb300 as dllm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(dllm_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function():
+    lib = dllm.load()
+    names = declared_functions()
+    assert "dllm_step" in names and "dllm_pack" in names and "dllm_compact" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(dllm.exported_symbols()) <= set(names)
+    assert lib.dllm_abi_version() == 1
+
+
+def test_struct_sizes_match_binding():
+    lib = dllm.load()
+    for which, cls in enumerate((dllm.StepArgs, dllm.PackArgs, dllm.CompactArgs, dllm.AdvanceArgs)):
+        assert lib.dllm_struct_size(which) == ctypes.sizeof(cls)
+    assert lib.dllm_struct_size(99) == 0
+
+
+def test_strerror():
+    lib = dllm.load()
+    for code in (0, -1, -2, -3, -4, -5, -6, 17):
+        assert lib.dllm_strerror(code)
+
+
+def _args(**kw):
+    base = dict(B=2, L=4, V=16, mask_id=15, ldv=16, logits=0x10000, input_ids=0x20000, thr=0x30000,
+                conf_state=0x40000, done=0x50000, accept_len=0x60000, n_new=0x70000, workspace=0x100000,
+                workspace_bytes=1 << 20)
+    base.update(kw)
+    return dllm.StepArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(L=0), -1), (dict(L=1025), -1), (dict(V=0), -1), (dict(ldv=8), -1), (dict(B=-1), -1),
+    (dict(logits=None), -1), (dict(thr=None), -1), (dict(done=None), -1),
+    (dict(ldv=20), -2), (dict(logits=0x10002), -2),
+    (dict(workspace=None), -5), (dict(workspace=0x100010), -5), (dict(workspace_bytes=64), -5),
+])
+def test_step_host_validation(kw, code):
+    lib = dllm.load()
+    assert lib.dllm_step(ctypes.byref(_args(**kw)), None) == code
+
+
+def test_step_empty_batch_is_a_no_op():
+    lib = dllm.load()
+    assert lib.dllm_step(ctypes.byref(_args(B=0, logits=None, input_ids=None)), None) == 0
+
+
+def test_workspace_size_shape_rules():
+    lib = dllm.load()
+    assert lib.dllm_step_workspace_size(0, 0, 10) == 0
+    a = lib.dllm_step_workspace_size(128, 32, 151936)
+    b = lib.dllm_step_workspace_size(512, 64, 151936)
+    assert 0 < a < b and a % 256 == 0
+
+
+def test_pack_plan_matches_eq1():
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        A = int(rng.integers(0, 20))
+        p = rng.integers(0, 2000, A)
+        b = rng.integers(0, 9, A)
+        L = int(rng.integers(1, 64))
+        W, cost = dllm.pack_plan(p, b, L)
+        assert W == oracle.box_width(list(p), list(b), L)
+        assert cost == oracle.cost(list(p), list(b), L)
+
+
+def test_admit_matches_oracle_random():
+    rng = np.random.default_rng(2)
+    for trial in range(300):
+        n = int(rng.integers(0, 40))
+        pend = np.sort(rng.integers(0, 300, n))
+        if trial % 3 == 0:
+            pend = np.sort(rng.integers(0, 8, n) * 16)     # many equal lengths
+        A = int(rng.integers(0, 6))
+        ap = rng.integers(0, 300, A)
+        ab = rng.integers(0, 4, A)
+        L = int(rng.choice([4, 8, 32]))
+        budget = int(rng.integers(0, 6000))
+        got = dllm.admit(pend, ap, ab, L, budget)
+        want = oracle.admit(list(pend), list(ap), list(ab), L, budget)
+        assert got == want, (trial, pend, ap, ab, L, budget)
+
+
+def test_admit_rejects_unsorted_queue():
+    lib = dllm.load()
+    pend = np.array([5, 3], dtype=np.int32)
+    idx = np.zeros(2, dtype=np.int32)
+    n = ctypes.c_int32(0)
+    rc = lib.dllm_admit(2, pend.ctypes.data, 0, None, None, 4, 100, idx.ctypes.data, ctypes.byref(n))
+    assert rc == -1

@@ -1,0 +1,210 @@
+"""GPU parity of dllm_step / dllm_features against the CPU oracle, through
+the C ABI (Python binding).
+
+Bar: tokens, selections, input_ids, done, accept_len and n_new bit-exact;
+confidences, conf_state and features within 1e-5 absolute, lse within
+1e-5 * max(1, |lse|).  Cases carry 1e-4 decision margins (tests/helpers.py).
+"""
+import numpy as np
+import pytest
+
+import synth
+from helpers import (CONF_TOL, compare_step, device_logits, device_state, enforce_margins, oracle_step)
+
+pytestmark = pytest.mark.gpu
+
+SMALL_CASES = {
+    "tiny": synth.STEP_CONFIGS["tiny"],
+    # three reduction chunks, a partial last copy and a partial last vector;
+    # row stride wider than V
+    "ragged": synth.StepConfig("ragged", 8, 32, 40001, 12.0, "fraction", synth.THRESHOLD_SET, ldv=40016),
+    # two positions per lane in the request finisher
+    "l64": synth.StepConfig("l64", 16, 64, 33000, 12.0, "fraction", synth.THRESHOLD_SET),
+    "l1": synth.StepConfig("l1", 5, 1, 9, 4.0, "half", (0.5,)),
+    "wide_block": synth.StepConfig("wide_block", 2, 1024, 300, 8.0, "fraction", (0.7,)),
+    "v_small": synth.StepConfig("v_small", 7, 8, 13, 6.0, "fraction", synth.THRESHOLD_SET),
+    "all_masked": synth.StepConfig("all_masked", 6, 32, 20000, 12.0, "all", synth.THRESHOLD_SET),
+}
+
+
+def run_gpu(dllm, inp, device, **kw):
+    logits = device_logits(inp, device)
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step(logits, ids, thr, cs, V=inp.cfg.V, mask_id=inp.cfg.mask_id, debug=True, **kw)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    return got, ids.cpu().numpy(), cs.cpu().numpy()
+
+
+@pytest.fixture(scope="module")
+def device(dllm):
+    import torch
+    return torch.device("cuda", 0)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_CASES))
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_step_parity_small(dllm, device, name, seed):
+    cfg = SMALL_CASES[name]
+    inp = synth.make_step_state(cfg, seed)
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    got, ids, cs = run_gpu(dllm, inp, device)
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids, cs)
+
+
+@pytest.mark.parametrize("name", ["llada", "dream", "stress"])
+def test_step_parity_full_size_sampled(dllm, device, name):
+    """Full-size batch on the GPU; the oracle recomputes a sample of requests
+    (the step is per-request, so a sub-batch is an exact reference)."""
+    cfg = synth.STEP_CONFIGS[name]
+    inp = synth.make_step_state(cfg, 7)
+    rng = np.random.default_rng(3)
+    sample = sorted(rng.choice(cfg.B, size=12, replace=False).tolist())
+    enforce_margins(inp, sample)
+    ref = oracle_step(inp, sample)
+    got, ids, cs = run_gpu(dllm, inp, device)
+    compare_step(ref, got, sample, cfg.L, ids, cs)
+    # properties over every request
+    m_in = inp.masked
+    m_out = ids == cfg.mask_id
+    assert not (m_out & ~m_in).any()
+    assert np.array_equal(got["n_new"], (m_in & ~m_out).sum(axis=1))
+    assert np.array_equal(got["done"], (~m_out.any(axis=1)).astype(np.uint8))
+    assert np.array_equal(got["accept_len"], np.where(got["done"] == 1, cfg.L, 0))
+    has = m_in.any(axis=1)
+    assert (got["n_new"][has] >= 1).all()
+    chg = m_in & ~m_out
+    assert np.array_equal(ids[chg], got["tok"][chg])
+    assert ((got["conf"][m_in] > 0) & (got["conf"][m_in] <= 1.0 + 1e-6)).all()
+
+
+def test_thresholds_zero_and_above_one(dllm, device):
+    cfg = SMALL_CASES["ragged"]
+    inp = synth.make_step_state(cfg, 11)
+    inp.thr[:] = 0.0
+    got, ids, _ = run_gpu(dllm, inp, device)
+    assert not (ids == cfg.mask_id).any()
+    assert (got["done"] == 1).all()
+    inp.thr[:] = 1.5
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    got, ids, cs = run_gpu(dllm, inp, device)
+    assert np.array_equal(got["n_new"], inp.masked.any(axis=1).astype(np.int32))
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids, cs)
+
+
+def test_batch_invariance(dllm, device):
+    """A request's results are bit-identical alone or inside any batch."""
+    cfg = synth.StepConfig("inv", 12, 32, 70000, 12.0, "fraction", synth.THRESHOLD_SET)
+    inp = synth.make_step_state(cfg, 5)
+    full, ids_full, cs_full = run_gpu(dllm, inp, device)
+    for sub in ([3], [0, 7], [11, 2, 5]):
+        part = synth.StepInputs(cfg, inp.seed, inp.input_ids[sub].copy(), inp.thr[sub].copy(),
+                                inp.conf_state[sub].copy(), inp.salt[sub].copy())
+        # the sub-batch keeps each request's own logits rows
+        import torch
+        L = cfg.L
+        rows = np.array([b * L + j for b in sub for j in range(L)])
+        logits_full = device_logits(inp, device)
+        logits = logits_full[torch.from_numpy(rows).to(device)].contiguous()
+        ids, thr, cs = device_state(part, device)
+        out = dllm.step(logits, ids, thr, cs, V=cfg.V, mask_id=cfg.mask_id, debug=True)
+        for k in ("conf", "lse", "tok", "feats", "done", "n_new", "accept_len"):
+            a = out[k].cpu().numpy()
+            b = full[k][sub]
+            assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                                  b.view(np.uint32) if b.dtype == np.float32 else b), k
+        assert np.array_equal(ids.cpu().numpy(), ids_full[sub])
+
+
+def test_no_masked_position_anywhere(dllm, device):
+    cfg = synth.StepConfig("none", 9, 32, 5000, 8.0, "half", (0.9,))
+    inp = synth.make_step_state(cfg, 2)
+    inp.input_ids[inp.masked] = 5
+    inp.conf_state[np.isnan(inp.conf_state)] = 0.95
+    ref = oracle_step(inp)
+    got, ids, cs = run_gpu(dllm, inp, device)
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids, cs)
+    assert (got["done"] == 1).all() and (got["n_new"] == 0).all()
+
+
+def test_ties_and_negative_infinity(dllm, device):
+    """Equal logits (argmax ties to the lowest index, conf = 1/V) and rows
+    with -inf entries."""
+    import torch
+    V, L, B = 5000, 4, 2
+    rows = np.zeros((B * L, V), dtype=np.float32)
+    rows[1, :] = 0.5                      # all equal: tok 0, conf 1/V
+    rows[2, 100] = rows[2, 4000] = 3.0    # tie between 100 and 4000
+    rows[3, :2500] = -np.inf              # half of the row at -inf
+    rows[3, 3000] = 1.0
+    rows[5, 7] = 2.0
+    rows[6, :] = -np.inf
+    rows[6, 4999] = -1.0                  # single finite value, at the end
+    bits = synth.f32_to_bf16_bits(rows)
+    mask_id = V + 10                     # a token id no row predicts
+    ids = np.full((B, L), mask_id, dtype=np.int32)
+    cs = np.full((B, L), np.nan, dtype=np.float32)
+    thr = np.array([0.0, 0.0], dtype=np.float32)
+    import oracle
+    ref = oracle.step(bits, V, ids, thr, cs, mask_id)
+    d_logits = torch.from_numpy(np.ascontiguousarray(np.pad(bits, ((0, 0), (0, 8 - V % 8 if V % 8 else 0)))
+                                                     .view(np.int16))).to(device)
+    d_ids = torch.from_numpy(ids).to(device)
+    d_cs = torch.from_numpy(cs).to(device)
+    out = dllm.step(d_logits, d_ids, torch.from_numpy(thr).to(device), d_cs, V=V, mask_id=mask_id, debug=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    compare_step(ref, got, [0, 1], L, d_ids.cpu().numpy(), d_cs.cpu().numpy())
+    assert got["tok"][0, 1] == 0 and got["tok"][0, 2] == 100 and got["tok"][1, 2] == 4999
+    assert got["conf"][0, 1] == pytest.approx(1.0 / V, abs=CONF_TOL)
+
+
+def test_workspace_reuse_across_shapes(dllm, device):
+    """One workspace serves calls of different shapes back to back."""
+    import torch
+    big = synth.StepConfig("big", 40, 32, 60000, 12.0, "fraction", synth.THRESHOLD_SET)
+    nbytes = dllm.step_workspace_size(big.B, big.L, big.V)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+    shapes = [big, SMALL_CASES["tiny"], SMALL_CASES["l64"], big, SMALL_CASES["ragged"]]
+    for k, cfg in enumerate(shapes):
+        inp = synth.make_step_state(cfg, 20 + k)
+        enforce_margins(inp)
+        ref = oracle_step(inp)
+        got, ids, cs = run_gpu(dllm, inp, device, workspace=ws)
+        compare_step(ref, got, list(range(cfg.B)), cfg.L, ids, cs)
+
+
+def test_features_kernel(dllm, device):
+    import torch
+    import oracle
+    cfg = SMALL_CASES["l64"]
+    inp = synth.make_step_state(cfg, 4)
+    ids = torch.from_numpy(inp.input_ids).to(device)
+    cs = torch.from_numpy(inp.conf_state).to(device)
+    got = dllm.features(ids, cs, mask_id=cfg.mask_id).cpu().numpy()
+    ref = oracle.features(inp.input_ids, inp.conf_state, cfg.mask_id)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=CONF_TOL, equal_nan=True)
+
+
+def test_repeated_steps_to_completion(dllm, device):
+    """Step the same batch with fresh logits each step until every block is
+    done; the oracle follows in lockstep."""
+    import oracle
+    cfg = synth.StepConfig("rep", 6, 32, 9000, 12.0, "fraction", synth.THRESHOLD_SET)
+    inp = synth.make_step_state(cfg, 9)
+    ids_d, thr_d, cs_d = device_state(inp, device)
+    for step_no in range(40):
+        inp.seed = 9 + 1000 * (step_no + 1)        # new logits per step
+        inp.salt[:] = 0
+        inp.input_ids = ids_d.cpu().numpy()
+        inp.conf_state = cs_d.cpu().numpy()
+        if not inp.masked.any():
+            break
+        enforce_margins(inp)
+        ref = oracle_step(inp)
+        logits = device_logits(inp, device)
+        out = dllm.step(logits, ids_d, thr_d, cs_d, V=cfg.V, mask_id=cfg.mask_id, debug=True)
+        got = {k: v.cpu().numpy() for k, v in out.items()}
+        compare_step(ref, got, list(range(cfg.B)), cfg.L, ids_d.cpu().numpy(), cs_d.cpu().numpy())
+    assert not (ids_d.cpu().numpy() == cfg.mask_id).any()
