@@ -82,6 +82,7 @@ _lock = threading.Lock()
 _SIGNATURES = {
     "dllm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "dllm_abi_version": (ctypes.c_int, []),
+    "dllm_last_cuda_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_char_p)]),
     "dllm_struct_size": (_sz, [ctypes.c_int]),
     "dllm_get_device_error": (ctypes.c_int, [_p, ctypes.POINTER(_i32)]),
     "dllm_step_workspace_size": (_sz, [_i32, _i32, _i32]),
@@ -137,7 +138,13 @@ def load(build=True):
 
 def _check(fn, rc):
     if rc != DLLM_OK:
-        raise DllmError(fn, rc, load().dllm_strerror(rc).decode())
+        lib = load()
+        msg = lib.dllm_strerror(rc).decode()
+        if rc == -3:
+            name = ctypes.c_char_p()
+            code = lib.dllm_last_cuda_error(ctypes.byref(name))
+            msg += f": cudaError {code} {name.value.decode() if name.value else ''}"
+        raise DllmError(fn, rc, msg)
 
 
 # ---------------------------------------------------------------------------

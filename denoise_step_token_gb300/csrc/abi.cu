@@ -18,13 +18,21 @@ std::mutex g_mu;
 
 }  // namespace
 
+thread_local int t_last_cuda_error = 0;
+
+void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
 int* error_word_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_err_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return nullptr;
+        }
         g_err_ptr[dev] = static_cast<int*>(p);
     }
     return g_err_ptr[dev];
@@ -36,7 +44,11 @@ int sm_count() {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_sm_count[dev] <= 0) {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        const cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return -1;
+        }
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
@@ -58,6 +70,12 @@ extern "C" const char* dllm_strerror(int code) {
 }
 
 extern "C" int dllm_abi_version(void) { return DLLM_ABI_VERSION; }
+
+extern "C" int dllm_last_cuda_error(const char** name) {
+    const int e = dllm::t_last_cuda_error;
+    if (name) *name = cudaGetErrorName(static_cast<cudaError_t>(e));
+    return e;
+}
 
 extern "C" size_t dllm_struct_size(int which) {
     switch (which) {

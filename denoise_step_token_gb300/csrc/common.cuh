@@ -12,10 +12,16 @@ namespace dllm {
 // ---------------------------------------------------------------------------
 // Host helpers.
 // ---------------------------------------------------------------------------
-#define DLLM_CUDA_TRY(expr)                          \
-    do {                                             \
-        cudaError_t _e = (expr);                     \
-        if (_e != cudaSuccess) return DLLM_ERR_CUDA; \
+// Remember the failing CUDA status for dllm_last_cuda_error().
+void note_cuda_error(cudaError_t e);
+
+#define DLLM_CUDA_TRY(expr)                     \
+    do {                                        \
+        cudaError_t _e = (expr);                \
+        if (_e != cudaSuccess) {                \
+            ::dllm::note_cuda_error(_e);        \
+            return DLLM_ERR_CUDA;               \
+        }                                       \
     } while (0)
 
 // Device address of the current device's error word (set up once per device).

@@ -743,14 +743,12 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
                         size_t(list_cap + zero_cap) * 4;
     int max_optin = 0;
     DLLM_CUDA_TRY(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-    if (smem + 64 > size_t(max_optin)) return DLLM_ERR_UNSUPPORTED;
-    if (dev >= 0 && dev < 64) {
-        if (g_smem_configured[dev] < (int)smem) {
-            DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin));
-            g_smem_configured[dev] = max_optin;
-        }
-    } else {
+    cudaFuncAttributes fa;
+    DLLM_CUDA_TRY(cudaFuncGetAttributes(&fa, step_kernel));
+    if (smem + fa.sharedSizeBytes > size_t(max_optin)) return DLLM_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= 64 || g_smem_configured[dev] < (int)smem) {
         DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (dev >= 0 && dev < 64) g_smem_configured[dev] = (int)smem;
     }
 
     unsigned char* ws = static_cast<unsigned char*>(a->workspace);

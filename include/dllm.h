@@ -62,6 +62,11 @@ const char* dllm_strerror(int code);
 /* ABI version of the loaded library (DLLM_ABI_VERSION). */
 int dllm_abi_version(void);
 
+/* The cudaError_t of the last CUDA runtime call that failed inside this
+ * library on the calling thread (0 if none), and its name in *name when
+ * name is not NULL.  Explains a DLLM_ERR_CUDA return. */
+int dllm_last_cuda_error(const char** name);
+
 /* sizeof() of the argument structs below, for binding self-checks:
  * which = 0 dllm_step_args, 1 dllm_pack_args, 2 dllm_compact_args,
  * 3 dllm_advance_args.  Returns 0 for an unknown `which`. */
