@@ -53,6 +53,8 @@ TAG_CONF_STATE = 5
 TAG_PROMPT_LEN = 6
 TAG_LOGITS = 7
 TAG_PROMPT_TOKEN = 8
+TAG_BLOCK_INDEX = 9
+TAG_GEN_TOKEN = 10
 
 THRESHOLD_SET = (0.5, 0.6, 0.7, 0.8, 0.9)
 
@@ -375,3 +377,15 @@ def make_loop_requests(cfg: LoopConfig, seed: int, R=None):
     K = np.full(R, cfg.K, dtype=np.int32)
     thr = np.full(R, cfg.threshold, dtype=np.float32)
     return LoopRequests(cfg, seed, p, K, off, toks, thr)
+
+
+def mixed_block_index(seed, R, K):
+    """Block index b_i ~ U{0..K-1} per request: a mixed-state batch in which
+    requests sit at different blocks (BlockServe page, section II-A)."""
+    return uniform_int(chain(seed, TAG_BLOCK_INDEX), np.arange(R, dtype=np.int64), 0, K - 1).astype(np.int32)
+
+
+def committed_tokens(seed, R, n, V):
+    """Tokens of already committed blocks, [R, n] (never the mask or pad id)."""
+    idx = np.arange(R * n, dtype=np.int64)
+    return uniform_int(chain(seed, TAG_GEN_TOKEN), idx, 0, V - 3).astype(np.int32).reshape(R, n)
