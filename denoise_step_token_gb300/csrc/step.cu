@@ -39,12 +39,31 @@
 namespace dllm {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
-constexpr int kCopyElems = 4096;                    // one bulk copy: 8 KB
+// Pipeline shape (tunable at build time; the defaults are the measured best).
+#ifndef DLLM_STEP_WARPS
+#define DLLM_STEP_WARPS 8
+#endif
+#ifndef DLLM_STEP_STAGES
+#define DLLM_STEP_STAGES 3
+#endif
+#ifndef DLLM_STEP_COPY_ELEMS
+#define DLLM_STEP_COPY_ELEMS 4096
+#endif
+#ifndef DLLM_STEP_BATCH_VECS
+#define DLLM_STEP_BATCH_VECS 8
+#endif
+
+#ifndef DLLM_STEP_FINISHERS
+#define DLLM_STEP_FINISHERS 2
+#endif
+constexpr int kStreamWarps = DLLM_STEP_WARPS;         // warps streaming logits
+constexpr int kFinishWarps = DLLM_STEP_FINISHERS;     // warps finishing rows and requests
+constexpr int kWarpsTotal = kStreamWarps + kFinishWarps;
+constexpr int kThreads = kWarpsTotal * 32;
+constexpr int kStages = DLLM_STEP_STAGES;
+constexpr int kCopyElems = DLLM_STEP_COPY_ELEMS;    // one bulk copy
 constexpr int kCopyBytes = kCopyElems * 2;
-constexpr int kBatchVecs = 8;                       // 16-byte vectors per lane per batch
+constexpr int kBatchVecs = DLLM_STEP_BATCH_VECS;    // 16-byte vectors per lane per batch
 constexpr int kBatchElems = kBatchVecs * 8 * 32;    // 2048 contiguous elements
 constexpr int kBatchesPerCopy = kCopyElems / kBatchElems;
 constexpr int kChunkElems = 16384;                  // fixed reduction chunk of a row
@@ -211,8 +230,6 @@ __device__ __forceinline__ void combine(float& m, float& s, float mo, float so) 
     m = mn;
 }
 
-__device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) - 1u; }
-
 // ---------------------------------------------------------------------------
 // Features of one block (warp-cooperative), DiLaServe review section 4.2 ③.
 // val[k] / inU[k] describe position j = lane + 32 k.  Writes feats[0..5].
@@ -298,28 +315,33 @@ __device__ __noinline__ void warp_features(const float* val, const bool* inU, in
 // (then every one of them has its row results in the workspace).
 // ---------------------------------------------------------------------------
 __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool has_masked, int lane) {
-    __threadfence();
+    // The caller's acquire (the request counter, or the launch itself for
+    // requests without masked rows) makes every row result of b visible.
     const int L = P.L;
     const int nk = (L + 31) >> 5;
     const long long base = (long long)b * L;
     const float t = P.thr[b];
+    const int scanned = (lane == 0 && has_masked) ? ld_acquire_gpu(P.ctl) : 0;
 
     int id[32], tk[32];
-    float c[32];
+    float c[32], cs_old[32];
     bool msk[32];
     bool any_masked = false, any_pass = false;
     float best_c = -INFINITY;
     int best_j = 0x7fffffff;
+    // issue every load of the block first, then decide
     for (int k = 0; k < nk; ++k) {
         const int j = lane + 32 * k;
         const bool valid = j < L;
         id[k] = valid ? P.ids[base + j] : 0;
-        msk[k] = valid && id[k] == P.mask_id;
-        c[k] = 0.f;
-        tk[k] = -1;
+        cs_old[k] = valid ? P.cs[base + j] : 0.f;
+        c[k] = (valid && has_masked) ? __ldcg(P.row_conf + base + j) : 0.f;
+        tk[k] = (valid && has_masked) ? __ldcg(P.row_tok + base + j) : -1;
+    }
+    for (int k = 0; k < nk; ++k) {
+        const int j = lane + 32 * k;
+        msk[k] = j < L && id[k] == P.mask_id;
         if (msk[k]) {
-            c[k] = __ldcg(P.row_conf + base + j);
-            tk[k] = __ldcg(P.row_tok + base + j);
             any_masked = true;
             if (c[k] > t) any_pass = true;
             // j grows with k, so a strict > keeps the lowest position on ties
@@ -327,6 +349,9 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
                 best_c = c[k];
                 best_j = j;
             }
+        } else {
+            c[k] = 0.f;
+            tk[k] = -1;
         }
     }
     any_masked = __any_sync(0xffffffffu, any_masked);
@@ -361,7 +386,7 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
         const int new_id = s ? tk[k] : id[k];
         float new_cs = 0.f;
         if (valid) {
-            new_cs = s ? c[k] : P.cs[base + j];
+            new_cs = s ? c[k] : cs_old[k];
             if (s) P.cs[base + j] = c[k];
             if (has_masked) P.sel[base + j] = s ? 1 : 0;
             if (!msk[k]) {
@@ -392,8 +417,7 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
         if (lane == 0) committed[b] = 1;
         return;
     }
-    __syncwarp();
-    const int scanned = (lane == 0) ? ld_acquire_gpu(P.ctl) : 0;
+    __syncwarp();   // lane 0's acquire of the scan count orders the warp's writes
     if (__shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
         for (int k = 0; k < nk; ++k) {
             if (selk[k]) P.ids[base + lane + 32 * k] = id[k];
@@ -408,8 +432,20 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
 // the row results; then count the row towards its request.
 // ---------------------------------------------------------------------------
 __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) {
-    __threadfence();
+    // Visibility of every chunk partial of the row comes from the acquire
+    // chain: each chunk's release-add on the row counter, the completing
+    // warp's acquire-release add, its release store into the CTA queue and
+    // the finisher's acquire load of that entry.
     const int NC = P.NC;
+    const int b = row / P.L;
+    // masked rows of this request (its input_ids are unmodified until its
+    // own finisher commits, which happens after this count)
+    int mb = 0;
+    for (int j0 = 0; j0 < P.L; j0 += 32) {
+        const int j = j0 + lane;
+        const bool mk = j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id;
+        mb += __popc(__ballot_sync(0xffffffffu, mk));
+    }
     float M = -INFINITY, S = 0.f;
     int cstar = 0, kbstar = 0;
     for (int c0 = 0; c0 < NC; c0 += 32) {
@@ -434,36 +470,31 @@ __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) 
         }
     }
     if (kbstar >= kBatchesPerChunk) kbstar = 0;
-    // argmax: first element equal to M inside batch kbstar of chunk cstar
+    // argmax: first element equal to M inside batch kbstar of chunk cstar;
+    // all of this lane's vectors are loaded at once, then scanned in order
     const long long start = (long long)cstar * kChunkElems + (long long)kbstar * kBatchElems;
     const uint16_t* rp = P.logits + (long long)row * P.ldv;
-    unsigned best = 0xffffffffu;
+    uint4 v[kBatchVecs];
+#pragma unroll
     for (int k = 0; k < kBatchVecs; ++k) {
         const long long e = start + (long long)(lane + 32 * k) * 8;
-        if (e >= P.V) break;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + e));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        v[k] = (e < P.V) ? __ldg(reinterpret_cast<const uint4*>(rp + e))
+                         : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+    unsigned best = 0xffffffffu;
+#pragma unroll
+    for (int k = 0; k < kBatchVecs; ++k) {
+        const long long e = start + (long long)(lane + 32 * k) * 8;
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
         for (int h = 0; h < 8; ++h) {
             const float x = (h & 1) ? bf16_hi(w[h >> 1]) : bf16_lo(w[h >> 1]);
-            if (e + h < P.V && x == M) {
-                best = (unsigned)(e + h);
-                break;
-            }
+            if (best == 0xffffffffu && e + h < P.V && x == M) best = (unsigned)(e + h);
         }
-        if (best != 0xffffffffu) break;
     }
     best = __reduce_min_sync(0xffffffffu, best);
     const float conf = __fdiv_rn(1.0f, S);
     const float lse = M + logf(S);
-    const int b = row / P.L;
-    // masked rows of this request (its input_ids are unmodified until its
-    // own finisher commits, which happens after this count)
-    int mb = 0;
-    for (int j0 = 0; j0 < P.L; j0 += 32) {
-        const int j = j0 + lane;
-        const bool mk = j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id;
-        mb += __popc(__ballot_sync(0xffffffffu, mk));
-    }
     int old = 0;
     if (lane == 0) {
         P.row_conf[row] = conf;
@@ -473,52 +504,122 @@ __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) 
         if (P.lse_out) P.lse_out[row] = lse;
         if (P.tok_out) P.tok_out[row] = (int)best;
         P.cnt[row] = 0;
-        __threadfence();
-        old = atomicAdd(P.cnt + P.BL + b, 1);
+        old = atom_add_acqrel_gpu(P.cnt + P.BL + b, 1);
     }
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == mb - 1) finalize_request(P, b, true, lane);
+    if (old == mb - 1) {
+        __syncwarp();   // lane 0's acquire-release add orders the whole warp's reads
+        finalize_request(P, b, true, lane);
+    }
 }
 
 // ---------------------------------------------------------------------------
-// The step kernel.
+// Finish queue: rows this CTA completed, drained in order by the finisher
+// warps and, once they are done streaming, by the streaming warps too.  A
+// warp claims the next slot, waits for it to be filled, and stops once every
+// streaming warp is done and its slot stayed empty.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void drain_queue(const StepParams& P, int* s_queue, int* s_qhead, const int* s_ndone,
+                                            int lane) {
+    uint32_t idle = 0;
+    const uint64_t t0 = globaltimer_ns();
+    int h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
+    h = __shfl_sync(0xffffffffu, h, 0);
+    while (h < P.list_cap) {
+        int v = (lane == 0) ? ld_acquire_cta_shared(&s_queue[h]) : 0;
+        v = __shfl_sync(0xffffffffu, v, 0);
+        if (v != 0) {
+            __syncwarp();   // lane 0's acquire orders the whole warp's reads
+            finish_row(P, v - 1, lane);
+            h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
+            h = __shfl_sync(0xffffffffu, h, 0);
+            continue;
+        }
+        int nd = (lane == 0) ? ld_acquire_cta_shared(s_ndone) : 0;
+        nd = __shfl_sync(0xffffffffu, nd, 0);
+        if (nd == kStreamWarps) {
+            // every completed row is queued: slot h is filled now or never
+            int v2 = (lane == 0) ? ld_acquire_cta_shared(&s_queue[h]) : 0;
+            if (__shfl_sync(0xffffffffu, v2, 0) != 0) continue;
+            break;
+        }
+        __nanosleep(64);
+        if ((++idle & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
+            break;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The step kernel: kStreamWarps streaming warps and kFinishWarps finishers.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kCopyBytes);
-    int* s_list = reinterpret_cast<int*>(bars + kWarps * kStages);
-    int* s_zero = s_list + P.list_cap;
-    __shared__ int s_warp_cnt[kWarps];
-    __shared__ int s_nzero;
-    __shared__ int s_last;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStreamWarps * kStages * kCopyBytes);
+    int* s_list = reinterpret_cast<int*>(bars + kStreamWarps * kStages);
+    int* s_queue = s_list + P.list_cap;   // rows this CTA completed, for the finishers
+    int* s_zero = s_queue + P.list_cap;   // this CTA's requests without masked rows
+    uint16_t* s_gmask = reinterpret_cast<uint16_t*>(s_zero + P.zero_cap);   // masked bits, 16 positions each
+    __shared__ int s_wsum[kWarpsTotal];
+    __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = gridDim.x, cta = blockIdx.x;
 
-    if (tid < kWarps * kStages) mbar_init(smem_addr(&bars[tid]), 1);
-    if (tid == 0) s_nzero = 0;
-    if (tid < kWarps * kStages) mbar_fence_init();
-
-    // ---- S1: rank the masked rows (entry state of input_ids) -------------
-    const int BL = P.BL;
-    const int seg = (((BL + kWarps - 1) / kWarps) + 31) & ~31;
-    const int s0 = min(BL, warp * seg), s1 = min(BL, s0 + seg);
-    int wcnt = 0;
-    for (int i0 = s0; i0 < s1; i0 += 32) {
-        const int i = i0 + lane;
-        const bool mk = i < s1 && P.ids[i] == P.mask_id;
-        wcnt += __popc(__ballot_sync(0xffffffffu, mk));
+    if (tid < kStreamWarps * kStages) mbar_init(smem_addr(&bars[tid]), 1);
+    if (tid == 0) {
+        s_nzero = 0;
+        s_qtail = 0;
+        s_qhead = 0;
+        s_ndone = 0;
     }
-    if (lane == 0) s_warp_cnt[warp] = wcnt;
-    __syncthreads();
-    int before = 0, M = 0;
+    for (int i = tid; i < P.list_cap; i += kThreads) s_queue[i] = 0;
+    if (tid < kStreamWarps * kStages) mbar_fence_init();
+
+    // ---- S1: masked bits of the entry state, 16 positions per thread ------
+    const int BL = P.BL;
+    const int ngroups = (BL + 15) >> 4;
+    const bool ids_vec = (reinterpret_cast<uintptr_t>(P.ids) & 15u) == 0;
+    for (int g = tid; g < ngroups; g += kThreads) {
+        const int p0 = g << 4;
+        unsigned bits = 0;
+        if (ids_vec && p0 + 16 <= BL) {
+            const int4* q = reinterpret_cast<const int4*>(P.ids + p0);
+            const int4 a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3];
+            const int v[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                               a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const int cw = s_warp_cnt[w];
-        if (w < warp) before += cw;
+            for (int i = 0; i < 16; ++i) bits |= (v[i] == P.mask_id ? 1u : 0u) << i;
+        } else {
+            for (int i = 0; i < 16; ++i)
+                if (p0 + i < BL && P.ids[p0 + i] == P.mask_id) bits |= 1u << i;
+        }
+        s_gmask[g] = (uint16_t)bits;
+    }
+    __syncthreads();
+    // ranks: each thread owns a contiguous run of groups; block-wide scan
+    const int gper = (ngroups + kThreads - 1) / kThreads;
+    const int g0 = min(ngroups, tid * gper), g1 = min(ngroups, g0 + gper);
+    int cnt = 0;
+    for (int g = g0; g < g1; ++g) cnt += __popc((unsigned)s_gmask[g]);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0, M = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsTotal; ++w) {
+        const int cw = s_wsum[w];
+        if (w < warp) wbase += cw;
         M += cw;
     }
+    const int before = wbase + incl - cnt;
     const int NC = P.NC;
     const long long V = P.V;
     const long long U = (long long)M * NC;
@@ -539,23 +640,27 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const long long r_lo = u0 / NC;
     const long long r_hi = (u1 > u0) ? (u1 - 1) / NC : r_lo - 1;
     int rank = before;
-    for (int i0 = s0; i0 < s1; i0 += 32) {
-        const int i = i0 + lane;
-        const bool mk = i < s1 && P.ids[i] == P.mask_id;
-        const unsigned bal = __ballot_sync(0xffffffffu, mk);
-        const int my = rank + __popc(bal & lanemask_lt(lane));
-        if (mk && my >= r_lo && my <= r_hi) s_list[my - r_lo] = i;
-        rank += __popc(bal);
-    }
-    // requests of this CTA (b = cta + G*k) with no masked position
-    for (int k = warp; cta + (long long)G * k < P.B; k += kWarps) {
-        const int b = cta + G * k;
-        bool anym = false;
-        for (int j0 = 0; j0 < P.L; j0 += 32) {
-            const int j = j0 + lane;
-            anym |= __any_sync(0xffffffffu, j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id);
+    for (int g = g0; g < g1 && rank <= r_hi; ++g) {
+        unsigned bits = s_gmask[g];
+        while (bits) {
+            const int i = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (rank >= r_lo && rank <= r_hi) s_list[rank - r_lo] = (g << 4) + i;
+            ++rank;
         }
-        if (!anym && lane == 0) s_zero[atomicAdd(&s_nzero, 1)] = b;
+    }
+    // this CTA's requests (b = cta + G*k) without a masked position
+    for (long long k = tid; cta + (long long)G * k < P.B; k += kThreads) {
+        const int b = cta + G * (int)k;
+        const int p0 = b * P.L, p1 = p0 + P.L;
+        bool anym = false;
+        for (int g = p0 >> 4; g <= ((p1 - 1) >> 4) && !anym; ++g) {
+            unsigned bits = s_gmask[g];
+            const int lo = max(p0 - (g << 4), 0), hi = min(p1 - (g << 4), 16);
+            bits &= ((hi >= 16) ? 0xffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+            anym = bits != 0;
+        }
+        if (!anym) s_zero[atomicAdd(&s_nzero, 1)] = b;
     }
     __syncthreads();
     if (tid == 0) {
@@ -563,100 +668,124 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         atomicAdd(P.ctl, 1);   // this CTA no longer reads input_ids' entry state
     }
 
-    // ---- S2: stream the masked rows, chunk by chunk -----------------------
-    const uint32_t stage0 = smem_addr(stages + warp * kStages * kCopyBytes);
-    const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
-    const uint64_t pol = l2_policy_evict_first();
-    const int V32 = P.V;
-    long long pu = u0 + warp;
-    int pq = 0;
-    uint32_t issued = 0, consumed = 0;
-    bool failed = false;
-
-    auto issue = [&]() {
-        if (pu >= u1) return;
-        const int cidx = (int)(pu % NC);
-        const int row = s_list[(int)(pu / NC - r_lo)];
-        const int clen = min(kChunkElems, V32 - cidx * kChunkElems);
-        const int e0 = cidx * kChunkElems + pq * kCopyElems;
-        const int nel = min(kCopyElems, clen - pq * kCopyElems);
-        const uint32_t bytes = (uint32_t)((nel * 2 + 15) & ~15);
-        const int slot = issued % kStages;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar0 + slot * 8, bytes);
-            bulk_g2s(stage0 + slot * kCopyBytes, P.logits + (long long)row * P.ldv + e0, bytes, bar0 + slot * 8,
-                     pol);
+    if (warp >= kStreamWarps) {
+        // ---- finisher warps: requests without masked rows, then the queue -
+        for (int k = warp - kStreamWarps; k < s_nzero; k += kFinishWarps) finalize_request(P, s_zero[k], false, lane);
+        drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);
+    } else {
+        // ---- S2: stream the masked rows, chunk by chunk -------------------
+        // This warp takes units u0 + warp + kStreamWarps * k, walked as
+        // (row slot, chunk) pairs without divisions.
+        const uint32_t stage0 = smem_addr(stages + warp * kStages * kCopyBytes);
+        const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
+        const uint64_t pol = l2_policy_evict_first();
+        const int V32 = P.V;
+        const long long span = u1 - u0;
+        const int n_my = span > warp ? (int)((span - warp + kStreamWarps - 1) / kStreamWarps) : 0;
+        int r_first = 0, c_first = 0;
+        if (n_my > 0) {
+            const long long uf = u0 + warp;
+            r_first = (int)(uf / NC - r_lo);
+            c_first = (int)(uf % NC);
         }
-        ++issued;
-        if (++pq * kCopyElems >= clen) {
-            pq = 0;
-            pu += kWarps;
-        }
-    };
-#pragma unroll 1
-    for (int st = 0; st < kStages; ++st) issue();
-
-#pragma unroll 1
-    for (long long u = u0 + warp; u < u1 && !failed; u += kWarps) {
-        const int cidx = (int)(u % NC);
-        const int row = s_list[(int)(u / NC - r_lo)];
-        const int clen = min(kChunkElems, V32 - cidx * kChunkElems);
-        const int ncp = (clen + kCopyElems - 1) / kCopyElems;
-        float m = -INFINITY, s = 0.f;
-        int kb = kBatchesPerChunk;
-#pragma unroll 1
-        for (int q = 0; q < ncp; ++q) {
-            const int slot = consumed % kStages;
-            const uint32_t par = (consumed / kStages) & 1u;
-            if (!mbar_wait_bounded(bar0 + slot * 8, par, kWaitLimitNs)) {
-                failed = true;
-                break;
+        auto next_unit = [&](int& r, int& c) {
+            c += kStreamWarps;
+            while (c >= NC) {
+                c -= NC;
+                ++r;
             }
-            const int nel = min(kCopyElems, clen - q * kCopyElems);
-            const uint4* buf = reinterpret_cast<const uint4*>(stages + (warp * kStages + slot) * kCopyBytes);
-            if (nel == kCopyElems) process_copy<true>(buf, lane, q, nel, m, s, kb);
-            else process_copy<false>(buf, lane, q, nel, m, s, kb);
-            __syncwarp();
-            ++consumed;
-            issue();
-        }
-        if (failed) break;
-        const float m_lane = m;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-            const float so = __shfl_xor_sync(0xffffffffu, s, off);
-            combine(m, s, mo, so);
-        }
-        const unsigned kbm =
-            __reduce_min_sync(0xffffffffu, (m_lane == m) ? (unsigned)kb : (unsigned)kBatchesPerChunk);
-        int old = 0;
-        if (lane == 0) {
-            float4 rec;
-            rec.x = m;
-            rec.y = s;
-            rec.z = __int_as_float((int)kbm);
-            rec.w = 0.f;
-            *reinterpret_cast<float4*>(P.part + (long long)row * NC + cidx) = rec;
-            __threadfence();
-            old = atomicAdd(P.cnt + row, 1);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == NC - 1) finish_row(P, row, lane);
-    }
-    if (failed) {
-        if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
-        // let this warp's copies in flight land before shared memory goes away
-        while (consumed < issued) {
-            const int slot = consumed % kStages;
-            if (!mbar_wait_bounded(bar0 + slot * 8, (consumed / kStages) & 1u, 100000000ull)) break;
-            ++consumed;
-        }
-    }
+        };
+        int p_left = n_my, pr = r_first, pc = c_first, pq = 0;
+        uint32_t issued = 0, consumed = 0;
+        bool failed = false;
 
-    // ---- requests without masked rows -------------------------------------
-    __syncthreads();
-    for (int k = warp; k < s_nzero; k += kWarps) finalize_request(P, s_zero[k], false, lane);
+        auto issue = [&]() {
+            if (p_left <= 0) return;
+            const int row = s_list[pr];
+            const int clen = min(kChunkElems, V32 - pc * kChunkElems);
+            const int e0 = pc * kChunkElems + pq * kCopyElems;
+            const int nel = min(kCopyElems, clen - pq * kCopyElems);
+            const uint32_t bytes = (uint32_t)((nel * 2 + 15) & ~15);
+            const int slot = issued % kStages;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar0 + slot * 8, bytes);
+                bulk_g2s(stage0 + slot * kCopyBytes, P.logits + (long long)row * P.ldv + e0, bytes,
+                         bar0 + slot * 8, pol);
+            }
+            ++issued;
+            if (++pq * kCopyElems >= clen) {
+                pq = 0;
+                --p_left;
+                next_unit(pr, pc);
+            }
+        };
+#pragma unroll 1
+        for (int st = 0; st < kStages; ++st) issue();
+
+        int cr = r_first, cc = c_first;
+#pragma unroll 1
+        for (int k = 0; k < n_my; ++k, next_unit(cr, cc)) {
+            const int row = s_list[cr];
+            const int clen = min(kChunkElems, V32 - cc * kChunkElems);
+            const int ncp = (clen + kCopyElems - 1) / kCopyElems;
+            float m = -INFINITY, s = 0.f;
+            int kb = kBatchesPerChunk;
+#pragma unroll 1
+            for (int q = 0; q < ncp; ++q) {
+                const int slot = consumed % kStages;
+                const uint32_t par = (consumed / kStages) & 1u;
+                if (!mbar_wait_bounded(bar0 + slot * 8, par, kWaitLimitNs)) {
+                    failed = true;
+                    break;
+                }
+                const int nel = min(kCopyElems, clen - q * kCopyElems);
+                const uint4* buf = reinterpret_cast<const uint4*>(stages + (warp * kStages + slot) * kCopyBytes);
+                if (nel == kCopyElems) process_copy<true>(buf, lane, q, nel, m, s, kb);
+                else process_copy<false>(buf, lane, q, nel, m, s, kb);
+                __syncwarp();
+                ++consumed;
+                issue();
+            }
+            if (failed) break;
+            const float m_lane = m;
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+                const float so = __shfl_xor_sync(0xffffffffu, s, off);
+                combine(m, s, mo, so);
+            }
+            const unsigned kbm =
+                __reduce_min_sync(0xffffffffu, (m_lane == m) ? (unsigned)kb : (unsigned)kBatchesPerChunk);
+            // publish the chunk partial (lane 1: lane 0 owns the bulk copies)
+            if (lane == 1) {
+                float4 rec;
+                rec.x = m;
+                rec.y = s;
+                rec.z = __int_as_float((int)kbm);
+                rec.w = 0.f;
+                *reinterpret_cast<float4*>(P.part + (long long)row * NC + cc) = rec;
+                if (atom_add_acqrel_gpu(P.cnt + row, 1) == NC - 1) {
+                    // this chunk completed the row: hand it to the finisher warp
+                    st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], row + 1);
+                }
+            }
+        }
+        if (failed) {
+            if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
+            // let this warp's copies in flight land before shared memory goes away
+            while (consumed < issued) {
+                const int slot = consumed % kStages;
+                if (!mbar_wait_bounded(bar0 + slot * 8, (consumed / kStages) & 1u, 100000000ull)) break;
+                ++consumed;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            atomicAdd(&s_ndone, 1);
+        }
+        drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);   // help with the backlog
+    }
 
     // ---- exit: the last CTA commits deferred requests and resets ----------
     __syncthreads();
@@ -668,12 +797,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (s_last) {
         __threadfence();
         int* committed = P.cnt + P.BL + P.B;
-        for (long long idx = tid; idx < BL; idx += kThreads) {
-            const int b = (int)(idx / P.L);
-            if (__ldcg(committed + b) == 0 && P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
+        for (int b = tid; b < P.B; b += kThreads) {
+            if (__ldcg(committed + b) == 0) {   // its finisher ran before every CTA had scanned
+                for (int j = 0; j < P.L; ++j) {
+                    const long long idx = (long long)b * P.L + j;
+                    if (P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
+                }
+            }
+            committed[b] = 0;
         }
-        __syncthreads();
-        for (int b = tid; b < P.B; b += kThreads) committed[b] = 0;
         if (tid == 0) {
             P.ctl[0] = 0;
             P.ctl[1] = 0;
@@ -739,8 +871,8 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     const int NC = (a->V + kChunkElems - 1) / kChunkElems;
     const int list_cap = BL / G + 3;
     const int zero_cap = a->B / G + 1;
-    const size_t smem = size_t(kWarps) * kStages * kCopyBytes + size_t(kWarps) * kStages * 8 +
-                        size_t(list_cap + zero_cap) * 4;
+    const size_t smem = size_t(kStreamWarps) * kStages * kCopyBytes + size_t(kStreamWarps) * kStages * 8 +
+                        size_t(2 * list_cap + zero_cap) * 4 + size_t((BL + 15) / 16) * 2;
     int max_optin = 0;
     DLLM_CUDA_TRY(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
     cudaFuncAttributes fa;
