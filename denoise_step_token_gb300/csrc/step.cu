@@ -8,28 +8,29 @@
 // positions above the request's threshold (or the single most confident one),
 // write the tokens, report done / accept_length and the confidence features.
 //
-// Kernel design (GB300, 152 SMs, one CTA per SM):
-//   S1  every CTA scans input_ids (warp ballots) to rank the masked rows and
-//       splits the masked-row element stream evenly over the grid.
-//   S2  work unit = one fixed 16384-element chunk of one masked row.  Each of
-//       the 8 warps of a CTA runs its own 3-stage pipeline of 8 KB bulk copies
-//       (cp.async.bulk, TMA engine, L2 evict-first) into shared memory and
-//       keeps a per-lane online (max, sum-exp) over 64-element batches
-//       (packed bf16x2 max, one FFMA + one MUFU.EX2 + one FADD per element).
-//       The warp's butterfly reduction gives the chunk partial (max, sum,
-//       first batch holding the max).
-//   Row finisher: the warp whose chunk completes a row (atomic counter) folds
-//       the row's chunk partials in chunk order, finds the argmax index by
-//       re-reading only the 2048-element batch that holds the first maximum,
-//       and writes conf = 1/s, lse = m + ln s, tok.
-//   Request finisher: the warp completing a request's last masked row runs
-//       S3-S6 for it with warp shuffles (selection, fallback, update, done,
-//       quantile features by rank).
-// The chunk split, lane mapping and fold order depend only on V, so results
-// are bit-identical whatever else is in the batch.  Nothing spins on another
-// CTA: counters only elect the last arriver.  input_ids is written only after
-// every CTA has finished scanning it (otherwise the grid's last CTA to exit
-// writes it), so a CTA that starts late still sees the entry state.
+// Kernel design (GB300: 152 SMs, one CTA per SM, warp-specialised):
+//   S1  every CTA scans input_ids once into shared bitmasks, ranks the masked
+//       rows and takes an equal share of the masked-row element stream.
+//   S2  work unit = one fixed 4096-element chunk of one masked row.  Each
+//       streaming warp takes chunks from the CTA's pool (a shared counter)
+//       and runs its own ring of bulk copies (cp.async.bulk, the TMA engine,
+//       L2 evict-first) into shared memory; being the only reader of its
+//       ring, it sees every barrier phase in order.  Each lane folds its
+//       elements into an online (max, sum of exp, first argmax) with a packed
+//       bf16x2 max and one FFMA + MUFU.EX2 + FADD per element; the warp then
+//       publishes the chunk partial with an acquire-release add on the row's
+//       counter.
+//   Rows: the chunk that completes a row queues it for the CTA's finisher
+//       warps, which fold the row's partials in a fixed order, write
+//       conf = 1/s, lse = m + ln s and the argmax token, and count the row
+//       towards its request; the request's last row runs S3-S6 for it
+//       (selection, fallback, update, done, quantile features by rank).
+// The chunk split, lane mapping and fold order depend only on V, so a
+// request's results are bit-identical whatever else is in the batch.  No
+// CTA waits for another: counters only elect the last arriver.  input_ids is
+// written only after every CTA has finished scanning it (otherwise the
+// grid's last CTA to exit writes it), so a CTA that starts late still sees
+// the entry state.  Every wait inside a CTA is bounded in time.
 
 #include <math.h>
 #include <stdint.h>
@@ -41,38 +42,44 @@ namespace {
 
 // Pipeline shape (tunable at build time; the defaults are the measured best).
 #ifndef DLLM_STEP_WARPS
-#define DLLM_STEP_WARPS 8
+#define DLLM_STEP_WARPS 20
 #endif
-#ifndef DLLM_STEP_STAGES
-#define DLLM_STEP_STAGES 3
-#endif
-#ifndef DLLM_STEP_COPY_ELEMS
-#define DLLM_STEP_COPY_ELEMS 4096
-#endif
-#ifndef DLLM_STEP_BATCH_VECS
-#define DLLM_STEP_BATCH_VECS 8
-#endif
-
 #ifndef DLLM_STEP_FINISHERS
 #define DLLM_STEP_FINISHERS 2
 #endif
+#ifndef DLLM_STEP_STAGES
+#define DLLM_STEP_STAGES 2
+#endif
+#ifndef DLLM_STEP_COPY_ELEMS
+#define DLLM_STEP_COPY_ELEMS 2048
+#endif
+#ifndef DLLM_STEP_CHUNK_ELEMS
+#define DLLM_STEP_CHUNK_ELEMS 8192
+#endif
+#ifndef DLLM_STEP_GROUP
+#define DLLM_STEP_GROUP 2
+#endif
+
 constexpr int kStreamWarps = DLLM_STEP_WARPS;         // warps streaming logits
 constexpr int kFinishWarps = DLLM_STEP_FINISHERS;     // warps finishing rows and requests
+constexpr int kFirstFinisher = kStreamWarps;
 constexpr int kWarpsTotal = kStreamWarps + kFinishWarps;
 constexpr int kThreads = kWarpsTotal * 32;
-constexpr int kStages = DLLM_STEP_STAGES;
-constexpr int kCopyElems = DLLM_STEP_COPY_ELEMS;    // one bulk copy
+constexpr int kStages = DLLM_STEP_STAGES;             // bulk copies in flight per streaming warp
+constexpr int kCopyElems = DLLM_STEP_COPY_ELEMS;      // one bulk copy
 constexpr int kCopyBytes = kCopyElems * 2;
-constexpr int kBatchVecs = DLLM_STEP_BATCH_VECS;    // 16-byte vectors per lane per batch
-constexpr int kBatchElems = kBatchVecs * 8 * 32;    // 2048 contiguous elements
+constexpr int kChunkElems = DLLM_STEP_CHUNK_ELEMS;    // fixed reduction chunk of a row
+constexpr int kGroup = DLLM_STEP_GROUP;               // chunks of one row taken at once
+constexpr int kBatchVecs = 8;                         // 16-byte vectors per lane per batch
+constexpr int kBatchElems = kBatchVecs * 8 * 32;      // 2048 contiguous elements
 constexpr int kBatchesPerCopy = kCopyElems / kBatchElems;
-constexpr int kChunkElems = 16384;                  // fixed reduction chunk of a row
 constexpr int kBatchesPerChunk = kChunkElems / kBatchElems;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;    // 4 s per bulk copy
+constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s for any single wait
 
-static_assert(kChunkElems % kCopyElems == 0, "chunk must hold whole copies");
-static_assert(kCopyElems % kBatchElems == 0, "copy must hold whole batches");
+static_assert(kCopyElems % kBatchElems == 0, "a copy holds whole batches");
+static_assert(kChunkElems % kCopyElems == 0, "a chunk holds whole copies");
+static_assert(kStages >= 1 && kStages <= 8, "pipeline depth");
 
 struct Partial {
     float m;    // chunk max
@@ -144,21 +151,22 @@ inline size_t ws_required(long long B, long long L, long long V) {
 // ---------------------------------------------------------------------------
 // Per-lane batch processing.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float max64(const uint4 (&v)[kBatchVecs]) {
-    uint32_t a = bf16x2_max(v[0].x, v[0].y), b = bf16x2_max(v[0].z, v[0].w);
+// Packed per-vector maxima of a lane's batch, and the batch maximum.
+__device__ __forceinline__ float batch_max(const uint4 (&v)[kBatchVecs], uint32_t (&vm)[kBatchVecs]) {
 #pragma unroll
-    for (int k = 1; k < kBatchVecs; ++k) {
-        a = bf16x2_max(a, bf16x2_max(v[k].x, v[k].y));
-        b = bf16x2_max(b, bf16x2_max(v[k].z, v[k].w));
-    }
-    a = bf16x2_max(a, b);
+    for (int k = 0; k < kBatchVecs; ++k) vm[k] = bf16x2_max(bf16x2_max(v[k].x, v[k].y), bf16x2_max(v[k].z, v[k].w));
+    uint32_t a = vm[0];
+#pragma unroll
+    for (int k = 1; k < kBatchVecs; ++k) a = bf16x2_max(a, vm[k]);
     return fmaxf(bf16_lo(a), bf16_hi(a));
 }
 
-// Fold one 64-element batch into the lane's running (m, s, kb).
-__device__ __forceinline__ void fold_batch(const uint4 (&v)[kBatchVecs], int kbatch, float& m, float& s,
-                                           int& kb) {
-    const float bm = max64(v);
+// Fold one batch into the lane's running (m, s, kb): kb is the chunk batch
+// holding the lane's first element equal to m.  A lane visits its batches
+// in increasing position, so only a strictly larger maximum moves kb.
+__device__ __forceinline__ void fold_batch(const uint4 (&v)[kBatchVecs], int kbatch, float& m, float& s, int& kb) {
+    uint32_t vm[kBatchVecs];
+    const float bm = batch_max(v, vm);
     if (bm > m) {
         s *= ex2_approx((m - bm) * kLog2e);
         m = bm;
@@ -189,7 +197,8 @@ __device__ __forceinline__ uint32_t mask_word(uint32_t w, int valid) {
     return w;
 }
 
-// One copy (up to 4096 elements) from shared memory.
+// One copy (up to kCopyElems elements) from shared memory; q is the copy's
+// index inside its chunk.
 template <bool kFull>
 __device__ __forceinline__ void process_copy(const uint4* buf, int lane, int q, int nel, float& m, float& s,
                                              int& kb) {
@@ -428,8 +437,8 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
 }
 
 // ---------------------------------------------------------------------------
-// Row finisher: fold the chunk partials of `row`, locate the argmax, write
-// the row results; then count the row towards its request.
+// Row finisher: fold the chunk partials of `row` in a fixed order, write the
+// row results, then count the row towards its request.
 // ---------------------------------------------------------------------------
 __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) {
     // Visibility of every chunk partial of the row comes from the acquire
@@ -446,33 +455,31 @@ __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) 
         const bool mk = j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id;
         mb += __popc(__ballot_sync(0xffffffffu, mk));
     }
+    // acquire every chunk's release-add on the row counter: all partials of
+    // the row are visible after this load
+    if (lane == 0) (void)ld_acquire_gpu(P.cnt + row);
+    __syncwarp();
+    // each lane folds chunks lane, lane + 32, ... in order, then the lanes
+    // combine in a fixed butterfly; the order depends only on NC
     float M = -INFINITY, S = 0.f;
-    int cstar = 0, kbstar = 0;
-    for (int c0 = 0; c0 < NC; c0 += 32) {
-        float pm = -INFINITY, ps = 0.f;
-        int pk = 0;
-        if (c0 + lane < NC) {
-            const float4 raw = __ldcg(reinterpret_cast<const float4*>(P.part + (long long)row * NC + c0 + lane));
-            pm = raw.x;
-            ps = raw.y;
-            pk = __float_as_int(raw.z);
-        }
-        const int n = min(32, NC - c0);
-        for (int i = 0; i < n; ++i) {
-            const float mc = __shfl_sync(0xffffffffu, pm, i);
-            const float sc = __shfl_sync(0xffffffffu, ps, i);
-            const int kbc = __shfl_sync(0xffffffffu, pk, i);
-            if (mc > M) {
-                cstar = c0 + i;
-                kbstar = kbc;
-            }
-            combine(M, S, mc, sc);
-        }
+    long long key = 0x7fffffffffffffffLL;   // chunk * batches + batch of the first maximum
+    for (int c = lane; c < NC; c += 32) {
+        const float4 raw = __ldcg(reinterpret_cast<const float4*>(P.part + (long long)row * NC + c));
+        const long long kc = (long long)c * kBatchesPerChunk + min(__float_as_int(raw.z), kBatchesPerChunk - 1);
+        if (raw.x > M) key = kc;
+        combine(M, S, raw.x, raw.y);
     }
-    if (kbstar >= kBatchesPerChunk) kbstar = 0;
-    // argmax: first element equal to M inside batch kbstar of chunk cstar;
-    // all of this lane's vectors are loaded at once, then scanned in order
-    const long long start = (long long)cstar * kChunkElems + (long long)kbstar * kBatchElems;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, M, off);
+        const float so = __shfl_xor_sync(0xffffffffu, S, off);
+        const long long ko = __shfl_xor_sync(0xffffffffu, key, off);
+        if (mo > M || (mo == M && ko < key)) key = ko;
+        combine(M, S, mo, so);
+    }
+    // argmax: first element equal to M inside that 2048-element batch; each
+    // lane loads all of its vectors at once, then scans them in order
+    const long long start = key * kBatchElems;
     const uint16_t* rp = P.logits + (long long)row * P.ldv;
     uint4 v[kBatchVecs];
 #pragma unroll
@@ -483,13 +490,13 @@ __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) 
     }
     unsigned best = 0xffffffffu;
 #pragma unroll
-    for (int k = 0; k < kBatchVecs; ++k) {
+    for (int k = kBatchVecs - 1; k >= 0; --k) {
         const long long e = start + (long long)(lane + 32 * k) * 8;
         const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
+        for (int h = 7; h >= 0; --h) {
             const float x = (h & 1) ? bf16_hi(w[h >> 1]) : bf16_lo(w[h >> 1]);
-            if (best == 0xffffffffu && e + h < P.V && x == M) best = (unsigned)(e + h);
+            if (e + h < P.V && x == M) best = (unsigned)(e + h);
         }
     }
     best = __reduce_min_sync(0xffffffffu, best);
@@ -515,9 +522,9 @@ __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) 
 
 // ---------------------------------------------------------------------------
 // Finish queue: rows this CTA completed, drained in order by the finisher
-// warps and, once they are done streaming, by the streaming warps too.  A
-// warp claims the next slot, waits for it to be filled, and stops once every
-// streaming warp is done and its slot stayed empty.
+// warps and, once they are done streaming, by the streaming warps too.  A warp claims
+// the next slot, waits for it to be filled, and stops once every streaming
+// warp is done and its slot stayed empty.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void drain_queue(const StepParams& P, int* s_queue, int* s_qhead, const int* s_ndone,
                                             int lane) {
@@ -552,24 +559,26 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, int* s_queue, i
 }
 
 // ---------------------------------------------------------------------------
-// The step kernel: kStreamWarps streaming warps and kFinishWarps finishers.
+// The step kernel: kStreamWarps streaming warps and kFinishWarps finisher
+// warps per CTA.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStreamWarps * kStages * kCopyBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStreamWarps) * kStages * kCopyBytes);
     int* s_list = reinterpret_cast<int*>(bars + kStreamWarps * kStages);
     int* s_queue = s_list + P.list_cap;   // rows this CTA completed, for the finishers
     int* s_zero = s_queue + P.list_cap;   // this CTA's requests without masked rows
     uint16_t* s_gmask = reinterpret_cast<uint16_t*>(s_zero + P.zero_cap);   // masked bits, 16 positions each
     __shared__ int s_wsum[kWarpsTotal];
-    __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last;
+    __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last, s_next;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = gridDim.x, cta = blockIdx.x;
 
     if (tid < kStreamWarps * kStages) mbar_init(smem_addr(&bars[tid]), 1);
     if (tid == 0) {
+        s_next = 0;
         s_nzero = 0;
         s_qtail = 0;
         s_qhead = 0;
@@ -663,113 +672,210 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if (!anym) s_zero[atomicAdd(&s_nzero, 1)] = b;
     }
     __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        atomicAdd(P.ctl, 1);   // this CTA no longer reads input_ids' entry state
-    }
 
-    if (warp >= kStreamWarps) {
-        // ---- finisher warps: requests without masked rows, then the queue -
-        for (int k = warp - kStreamWarps; k < s_nzero; k += kFinishWarps) finalize_request(P, s_zero[k], false, lane);
-        drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);
-    } else {
-        // ---- S2: stream the masked rows, chunk by chunk -------------------
-        // This warp takes units u0 + warp + kStreamWarps * k, walked as
-        // (row slot, chunk) pairs without divisions.
-        const uint32_t stage0 = smem_addr(stages + warp * kStages * kCopyBytes);
+    const int n_units = (int)(u1 - u0);   // this CTA's chunks: unit k is chunk u0 + k
+    const int u_first = (int)u0;          // M * NC < 2^31 (checked on the host)
+    const int r_lo32 = (int)r_lo;
+    const int V32 = P.V;
+
+    if (warp < kStreamWarps) {
+        // ---- S2: stream groups of chunks through this warp's ring ----------
+        // A group is up to kGroup consecutive chunks of one row, taken from
+        // the CTA's pool; near the end of the pool groups shrink to one chunk
+        // so that the warps finish together.  Each chunk keeps its own
+        // partial (the reduction order depends only on V); the group's
+        // partials are reduced across the warp together and published with
+        // one add on the row counter.
+        const uint32_t stage0 = smem_addr(stages + size_t(warp) * kStages * kCopyBytes);
         const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
         const uint64_t pol = l2_policy_evict_first();
-        const int V32 = P.V;
-        const long long span = u1 - u0;
-        const int n_my = span > warp ? (int)((span - warp + kStreamWarps - 1) / kStreamWarps) : 0;
-        int r_first = 0, c_first = 0;
-        if (n_my > 0) {
-            const long long uf = u0 + warp;
-            r_first = (int)(uf / NC - r_lo);
-            c_first = (int)(uf % NC);
-        }
-        auto next_unit = [&](int& r, int& c) {
-            c += kStreamWarps;
-            while (c >= NC) {
-                c -= NC;
-                ++r;
+        const int tail_units = 2 * kStreamWarps;   // single-chunk grabs below this many left
+
+        // Take the next group: returns its first unit (or -1) and its size.
+        auto grab = [&](int& k) -> int {
+            int got = -1, kk = 0;
+            if (lane == 0) {
+                int cur = *reinterpret_cast<volatile int*>(&s_next);
+                while (cur < n_units) {
+                    const int gu = u_first + cur;
+                    const int row_end = (gu / NC + 1) * NC - u_first;   // first unit of the next row
+                    const int left = n_units - cur;
+                    int want = left > tail_units ? kGroup : 1;
+                    want = min(want, min(row_end - cur, left));
+                    const int old = atomicCAS(&s_next, cur, cur + want);
+                    if (old == cur) {
+                        got = cur;
+                        kk = want;
+                        break;
+                    }
+                    cur = old;
+                }
             }
+            k = __shfl_sync(0xffffffffu, kk, 0);
+            return __shfl_sync(0xffffffffu, got, 0);
         };
-        int p_left = n_my, pr = r_first, pc = c_first, pq = 0;
+
+        // producer side: the chunk being issued
+        int p_unit = 0, p_left = 0, p_q = 0, p_len = 0;
+        long long p_src = 0;
+        bool p_done = false;
+        // groups whose copies are issued but not yet folded, oldest first
+        int fifo_u[kStages + 1], fifo_k[kStages + 1];
+        int nfifo = 0;
         uint32_t issued = 0, consumed = 0;
         bool failed = false;
 
+        auto start_chunk = [&](int u) {
+            const int gu = u_first + u;
+            const int rr = gu / NC;
+            const int c = gu - rr * NC;
+            const int row = s_list[rr - r_lo32];
+            p_unit = u;
+            p_q = 0;
+            p_len = min(kChunkElems, V32 - c * kChunkElems);
+            p_src = (long long)row * P.ldv + (long long)c * kChunkElems;
+        };
         auto issue = [&]() {
-            if (p_left <= 0) return;
-            const int row = s_list[pr];
-            const int clen = min(kChunkElems, V32 - pc * kChunkElems);
-            const int e0 = pc * kChunkElems + pq * kCopyElems;
-            const int nel = min(kCopyElems, clen - pq * kCopyElems);
+            if (p_done) return;
+            if (p_q * kCopyElems >= p_len) {   // current chunk fully issued
+                if (p_left > 0) {
+                    --p_left;
+                    start_chunk(p_unit + 1);
+                } else {
+                    int k = 0;
+                    const int u = grab(k);
+                    if (u < 0) {
+                        p_done = true;
+                        return;
+                    }
+#pragma unroll
+                    for (int i = 0; i <= kStages; ++i)
+                        if (i == nfifo) {
+                            fifo_u[i] = u;
+                            fifo_k[i] = k;
+                        }
+                    ++nfifo;
+                    p_left = k - 1;
+                    start_chunk(u);
+                }
+            }
+            const int nel = min(kCopyElems, p_len - p_q * kCopyElems);
             const uint32_t bytes = (uint32_t)((nel * 2 + 15) & ~15);
             const int slot = issued % kStages;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar0 + slot * 8, bytes);
-                bulk_g2s(stage0 + slot * kCopyBytes, P.logits + (long long)row * P.ldv + e0, bytes,
+                bulk_g2s(stage0 + slot * kCopyBytes, P.logits + p_src + (long long)p_q * kCopyElems, bytes,
                          bar0 + slot * 8, pol);
             }
             ++issued;
-            if (++pq * kCopyElems >= clen) {
-                pq = 0;
-                --p_left;
-                next_unit(pr, pc);
-            }
+            ++p_q;
         };
+        // lane 1's last row-counter add, tested one group later so that its
+        // round trip overlaps the next group's work
+        int pend_old = -1, pend_k = 0, pend_row = 0;
+        auto flush_pending = [&]() {
+            if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC) {
+                // that group completed the row: hand it to the finishers
+                st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], pend_row + 1);
+            }
+            pend_old = -1;
+        };
+
 #pragma unroll 1
         for (int st = 0; st < kStages; ++st) issue();
 
-        int cr = r_first, cc = c_first;
 #pragma unroll 1
-        for (int k = 0; k < n_my; ++k, next_unit(cr, cc)) {
-            const int row = s_list[cr];
-            const int clen = min(kChunkElems, V32 - cc * kChunkElems);
-            const int ncp = (clen + kCopyElems - 1) / kCopyElems;
-            float m = -INFINITY, s = 0.f;
-            int kb = kBatchesPerChunk;
+        while (consumed < issued && !failed) {
+            const int u = fifo_u[0], k = fifo_k[0];
+#pragma unroll
+            for (int i = 0; i < kStages; ++i) {
+                fifo_u[i] = fifo_u[i + 1];
+                fifo_k[i] = fifo_k[i + 1];
+            }
+            --nfifo;
+            const int gu = u_first + u;
+            const int rr = gu / NC;
+            const int c0 = gu - rr * NC;
+            const int row = s_list[rr - r_lo32];
+            float gm[kGroup], gs[kGroup];
+            int gi[kGroup];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) {
+                gm[j] = -INFINITY;
+                gs[j] = 0.f;
+                gi[j] = kBatchesPerChunk;
+            }
 #pragma unroll 1
-            for (int q = 0; q < ncp; ++q) {
-                const int slot = consumed % kStages;
-                const uint32_t par = (consumed / kStages) & 1u;
-                if (!mbar_wait_bounded(bar0 + slot * 8, par, kWaitLimitNs)) {
-                    failed = true;
-                    break;
+            for (int j = 0; j < k && !failed; ++j) {
+                const int clen = min(kChunkElems, V32 - (c0 + j) * kChunkElems);
+                const int ncp = (clen + kCopyElems - 1) / kCopyElems;
+                float m = -INFINITY, s = 0.f;
+                int kb = kBatchesPerChunk;
+#pragma unroll 1
+                for (int q = 0; q < ncp; ++q) {
+                    const int slot = consumed % kStages;
+                    const uint32_t par = (consumed / kStages) & 1u;
+                    if (!mbar_wait_bounded(bar0 + slot * 8, par, kWaitLimitNs)) {
+                        failed = true;
+                        break;
+                    }
+                    const int nel = min(kCopyElems, clen - q * kCopyElems);
+                    const uint4* buf =
+                        reinterpret_cast<const uint4*>(stages + (size_t(warp) * kStages + slot) * kCopyBytes);
+                    if (nel == kCopyElems) process_copy<true>(buf, lane, q, nel, m, s, kb);
+                    else process_copy<false>(buf, lane, q, nel, m, s, kb);
+                    __syncwarp();
+                    ++consumed;
+                    issue();
                 }
-                const int nel = min(kCopyElems, clen - q * kCopyElems);
-                const uint4* buf = reinterpret_cast<const uint4*>(stages + (warp * kStages + slot) * kCopyBytes);
-                if (nel == kCopyElems) process_copy<true>(buf, lane, q, nel, m, s, kb);
-                else process_copy<false>(buf, lane, q, nel, m, s, kb);
-                __syncwarp();
-                ++consumed;
-                issue();
+                // keep the chunk's partial in registers (constant indices only)
+#pragma unroll
+                for (int jj = 0; jj < kGroup; ++jj) {
+                    if (jj == j) {
+                        gm[jj] = m;
+                        gs[jj] = s;
+                        gi[jj] = kb;
+                    }
+                }
             }
             if (failed) break;
-            const float m_lane = m;
+            // the group's warp reductions, interleaved
+            float lm[kGroup];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) lm[j] = gm[j];
 #pragma unroll
             for (int off = 16; off; off >>= 1) {
-                const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-                const float so = __shfl_xor_sync(0xffffffffu, s, off);
-                combine(m, s, mo, so);
-            }
-            const unsigned kbm =
-                __reduce_min_sync(0xffffffffu, (m_lane == m) ? (unsigned)kb : (unsigned)kBatchesPerChunk);
-            // publish the chunk partial (lane 1: lane 0 owns the bulk copies)
-            if (lane == 1) {
-                float4 rec;
-                rec.x = m;
-                rec.y = s;
-                rec.z = __int_as_float((int)kbm);
-                rec.w = 0.f;
-                *reinterpret_cast<float4*>(P.part + (long long)row * NC + cc) = rec;
-                if (atom_add_acqrel_gpu(P.cnt + row, 1) == NC - 1) {
-                    // this chunk completed the row: hand it to the finisher warp
-                    st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], row + 1);
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, gm[j], off);
+                    const float so = __shfl_xor_sync(0xffffffffu, gs[j], off);
+                    combine(gm[j], gs[j], mo, so);
                 }
             }
+            unsigned first[kGroup];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j)
+                first[j] = __reduce_min_sync(0xffffffffu, (lm[j] == gm[j]) ? (unsigned)gi[j] : (unsigned)kBatchesPerChunk);
+            // publish the group's partials (lane 1: lane 0 owns the bulk copies)
+            flush_pending();
+            if (lane == 1) {
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) {
+                    if (j < k) {
+                        float4 rec;
+                        rec.x = gm[j];
+                        rec.y = gs[j];
+                        rec.z = __int_as_float((int)first[j]);
+                        rec.w = 0.f;
+                        *reinterpret_cast<float4*>(P.part + (long long)row * NC + c0 + j) = rec;
+                    }
+                }
+                pend_old = atom_add_release_gpu(P.cnt + row, k);
+                pend_k = k;
+                pend_row = row;
+            }
         }
+        flush_pending();
         if (failed) {
             if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
             // let this warp's copies in flight land before shared memory goes away
@@ -785,6 +891,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             atomicAdd(&s_ndone, 1);
         }
         drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);   // help with the backlog
+    } else {
+        // ---- finisher warps: scan signal, requests without masked rows, queue
+        if (warp == kFirstFinisher && lane == 0) {
+            __threadfence();
+            atomicAdd(P.ctl, 1);   // this CTA no longer reads input_ids' entry state
+        }
+        for (int k = warp - kFirstFinisher; k < s_nzero; k += kFinishWarps) finalize_request(P, s_zero[k], false, lane);
+        drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);
     }
 
     // ---- exit: the last CTA commits deferred requests and resets ----------
@@ -869,6 +983,7 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     if (G <= 0) return DLLM_ERR_CUDA;
     const int BL = a->B * a->L;
     const int NC = (a->V + kChunkElems - 1) / kChunkElems;
+    if ((long long)BL * NC > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
     const int list_cap = BL / G + 3;
     const int zero_cap = a->B / G + 1;
     const size_t smem = size_t(kStreamWarps) * kStages * kCopyBytes + size_t(kStreamWarps) * kStages * 8 +
