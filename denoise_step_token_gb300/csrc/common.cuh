@@ -148,6 +148,8 @@ __device__ __forceinline__ int atom_add_release_gpu(int* p, int v) {
     return old;
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
     asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }

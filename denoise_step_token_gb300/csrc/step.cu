@@ -241,13 +241,17 @@ __device__ __forceinline__ void combine(float& m, float& s, float mo, float so) 
 
 // ---------------------------------------------------------------------------
 // Features of one block (warp-cooperative), DiLaServe review section 4.2 ③.
-// val[k] / inU[k] describe position j = lane + 32 k.  Writes feats[0..5].
+// val[k] / inU[k] describe position j = lane + 32 k (k < NK, j < L).
+// Writes feats[0..5].  NK is a compile-time bound so that every array
+// index is a constant and the arrays stay in registers.
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void warp_features(const float* val, const bool* inU, int nk, int L, int lane,
-                                           float* feats_out) {
+template <int NK>
+__device__ __forceinline__ void warp_features(const float (&val)[NK], const bool (&inU)[NK], int L, int lane,
+                                              float* feats_out) {
     int n = 0;
     float sum = 0.f;
-    for (int k = 0; k < nk; ++k) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
         if (inU[k]) {
             ++n;
             sum += val[k];
@@ -264,24 +268,22 @@ __device__ __noinline__ void warp_features(const float* val, const bool* inU, in
         f[5] = 0.f;
     } else {
         // rank of each of my values among U (ties broken by position)
-        int rank[32];
-        for (int k = 0; k < nk; ++k) rank[k] = 0;
-        for (int jj = 0; jj < L; ++jj) {
-            const int src = jj & 31, kk = jj >> 5;
-            float vo = 0.f;
-            bool uo = false;
-            for (int k = 0; k < nk; ++k) {   // fetch slot kk of lane src
-                const float tv = __shfl_sync(0xffffffffu, val[k], src);
-                const bool tu = __shfl_sync(0xffffffffu, inU[k] ? 1 : 0, src) != 0;
-                if (k == kk) {
-                    vo = tv;
-                    uo = tu;
+        int rank[NK];
+#pragma unroll
+        for (int k = 0; k < NK; ++k) rank[k] = 0;
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+#pragma unroll 4
+            for (int src = 0; src < 32; ++src) {
+                const int jj = src + 32 * kk;
+                const float vo = __shfl_sync(0xffffffffu, val[kk], src);
+                const bool uo = __shfl_sync(0xffffffffu, inU[kk] ? 1 : 0, src) != 0;
+                if (!uo || jj >= L) continue;
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    const int j = lane + 32 * k;
+                    if (inU[k] && (vo < val[k] || (vo == val[k] && jj < j))) ++rank[k];
                 }
-            }
-            if (!uo) continue;
-            for (int k = 0; k < nk; ++k) {
-                const int j = lane + 32 * k;
-                if (inU[k] && (vo < val[k] || (vo == val[k] && jj < j))) ++rank[k];
             }
         }
         // order statistics needed: rank 0 and lo / hi of the three quantiles
@@ -289,6 +291,7 @@ __device__ __noinline__ void warp_features(const float* val, const bool* inU, in
         int want[7];
         float frac[3];
         want[0] = 0;
+#pragma unroll
         for (int t = 0; t < 3; ++t) {
             const float h = qs[t] * float(n - 1);
             const int lo = int(floorf(h));
@@ -297,10 +300,12 @@ __device__ __noinline__ void warp_features(const float* val, const bool* inU, in
             want[2 + 2 * t] = min(lo + 1, n - 1);
         }
         float got[7];
+#pragma unroll
         for (int t = 0; t < 7; ++t) {
             float mine = 0.f;
             bool have = false;
-            for (int k = 0; k < nk; ++k) {
+#pragma unroll
+            for (int k = 0; k < NK; ++k) {
                 if (inU[k] && rank[k] == want[t]) {
                     mine = val[k];
                     have = true;
@@ -320,26 +325,28 @@ __device__ __noinline__ void warp_features(const float* val, const bool* inU, in
 }
 
 // ---------------------------------------------------------------------------
-// S3-S6 for request b (one warp).  has_masked: b had masked rows at entry
-// (then every one of them has its row results in the workspace).
+// S3-S6 for request b (one warp), for L <= 32 * NK.  has_masked: b had masked
+// rows at entry (then every one of them has its row results in the
+// workspace).
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void finalize_request(const StepParams& P, int b, bool has_masked, int lane) {
+template <int NK>
+__device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool has_masked, int lane) {
     // The caller's acquire (the request counter, or the launch itself for
     // requests without masked rows) makes every row result of b visible.
     const int L = P.L;
-    const int nk = (L + 31) >> 5;
     const long long base = (long long)b * L;
     const float t = P.thr[b];
     const int scanned = (lane == 0 && has_masked) ? ld_acquire_gpu(P.ctl) : 0;
 
-    int id[32], tk[32];
-    float c[32], cs_old[32];
-    bool msk[32];
+    int id[NK], tk[NK];
+    float c[NK], cs_old[NK];
+    bool msk[NK];
     bool any_masked = false, any_pass = false;
     float best_c = -INFINITY;
     int best_j = 0x7fffffff;
     // issue every load of the block first, then decide
-    for (int k = 0; k < nk; ++k) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
         const bool valid = j < L;
         id[k] = valid ? P.ids[base + j] : 0;
@@ -347,7 +354,8 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
         c[k] = (valid && has_masked) ? __ldcg(P.row_conf + base + j) : 0.f;
         tk[k] = (valid && has_masked) ? __ldcg(P.row_tok + base + j) : -1;
     }
-    for (int k = 0; k < nk; ++k) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
         msk[k] = j < L && id[k] == P.mask_id;
         if (msk[k]) {
@@ -382,12 +390,13 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
         fb_j = bj;
     }
 
-    float val[32];
-    bool inU[32];
-    bool selk[32];
+    float val[NK];
+    bool inU[NK];
+    bool selk[NK];
     int n_sel = 0;
     bool still = false;
-    for (int k = 0; k < nk; ++k) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
         const bool valid = j < L;
         const bool s = msk[k] && (c[k] > t || j == fb_j);
@@ -418,7 +427,7 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
         P.accept[b] = done ? L : 0;
         P.n_new[b] = n_sel;
     }
-    if (P.feats) warp_features(val, inU, nk, L, lane, P.feats + (long long)b * DLLM_NUM_FEATURES);
+    if (P.feats) warp_features<NK>(val, inU, L, lane, P.feats + (long long)b * DLLM_NUM_FEATURES);
 
     // S4 commit of input_ids: only once every CTA has finished its scan.
     int* committed = P.cnt + P.BL + P.B;
@@ -428,7 +437,8 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
     }
     __syncwarp();   // lane 0's acquire of the scan count orders the warp's writes
     if (__shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
-        for (int k = 0; k < nk; ++k) {
+#pragma unroll
+        for (int k = 0; k < NK; ++k) {
             if (selk[k]) P.ids[base + lane + 32 * k] = id[k];
         }
         if (lane == 0) committed[b] = 1;
@@ -436,29 +446,38 @@ __device__ __noinline__ void finalize_request(const StepParams& P, int b, bool h
     if (lane == 0) P.cnt[P.BL + b] = 0;   // request counter back to rest
 }
 
+__device__ __forceinline__ void finalize_request(const StepParams& P, int b, bool has_masked, int lane) {
+    const int nk = (P.L + 31) >> 5;
+    if (nk <= 1) finalize_request_t<1>(P, b, has_masked, lane);
+    else if (nk <= 2) finalize_request_t<2>(P, b, has_masked, lane);
+    else if (nk <= 4) finalize_request_t<4>(P, b, has_masked, lane);
+    else finalize_request_t<32>(P, b, has_masked, lane);
+}
+
 // ---------------------------------------------------------------------------
 // Row finisher: fold the chunk partials of `row` in a fixed order, write the
 // row results, then count the row towards its request.
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) {
+__device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_gmask, int row, int lane) {
     // Visibility of every chunk partial of the row comes from the acquire
-    // chain: each chunk's release-add on the row counter, the completing
-    // warp's acquire-release add, its release store into the CTA queue and
-    // the finisher's acquire load of that entry.
+    // chain: each chunk group's release-add on the row counter, the
+    // completing lane's fence after its add, its release store into the CTA
+    // queue and the finisher's acquire load of that entry.
     const int NC = P.NC;
     const int b = row / P.L;
-    // masked rows of this request (its input_ids are unmodified until its
-    // own finisher commits, which happens after this count)
+    // masked rows of this request at entry, from this CTA's scan bitmask
     int mb = 0;
-    for (int j0 = 0; j0 < P.L; j0 += 32) {
-        const int j = j0 + lane;
-        const bool mk = j < P.L && P.ids[(long long)b * P.L + j] == P.mask_id;
-        mb += __popc(__ballot_sync(0xffffffffu, mk));
+    {
+        const int p0 = b * P.L, p1 = p0 + P.L;
+        for (int g = (p0 >> 4) + lane; g <= ((p1 - 1) >> 4); g += 32) {
+            unsigned bits = s_gmask[g];
+            const int lo = max(p0 - (g << 4), 0), hi = min(p1 - (g << 4), 16);
+            bits &= ((hi >= 16) ? 0xffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+            mb += __popc(bits);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) mb += __shfl_xor_sync(0xffffffffu, mb, off);
     }
-    // acquire every chunk's release-add on the row counter: all partials of
-    // the row are visible after this load
-    if (lane == 0) (void)ld_acquire_gpu(P.cnt + row);
-    __syncwarp();
     // each lane folds chunks lane, lane + 32, ... in order, then the lanes
     // combine in a fixed butterfly; the order depends only on NC
     float M = -INFINITY, S = 0.f;
@@ -526,8 +545,8 @@ __device__ __noinline__ void finish_row(const StepParams& P, int row, int lane) 
 // the next slot, waits for it to be filled, and stops once every streaming
 // warp is done and its slot stayed empty.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void drain_queue(const StepParams& P, int* s_queue, int* s_qhead, const int* s_ndone,
-                                            int lane) {
+__device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t* s_gmask, int* s_queue, int* s_qhead,
+                                            const int* s_ndone, int lane) {
     uint32_t idle = 0;
     const uint64_t t0 = globaltimer_ns();
     int h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
@@ -537,7 +556,7 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, int* s_queue, i
         v = __shfl_sync(0xffffffffu, v, 0);
         if (v != 0) {
             __syncwarp();   // lane 0's acquire orders the whole warp's reads
-            finish_row(P, v - 1, lane);
+            finish_row(P, s_gmask, v - 1, lane);
             h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
             h = __shfl_sync(0xffffffffu, h, 0);
             continue;
@@ -632,22 +651,28 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const int NC = P.NC;
     const long long V = P.V;
     const long long U = (long long)M * NC;
-    const long long E = (long long)M * V;
-    auto first_unit = [&](long long T) -> long long {
-        if (T >= E) return U;
-        long long r = T / V;
-        const long long rem = T - r * V;
-        long long cc = (rem + kChunkElems - 1) / kChunkElems;
+    // CTA k's share of the masked-row element stream starts at element
+    // floor(M * V * k / G) = V * a + e with a = floor(M k / G) and
+    // e = floor(V * (M k mod G) / G) < V: row a, element e of that row.  Its
+    // first unit is the first chunk starting there or later.  Only 32-bit
+    // divisions (M * G and V * G fit in 32 bits, checked on the host).
+    auto first_unit = [&](int k) -> long long {
+        if (k >= G) return U;
+        const int mk = M * k;
+        int r = mk / G;
+        const int e = (int)(((long long)V * (mk - r * G)) / G);
+        int cc = (e + kChunkElems - 1) / kChunkElems;
         if (cc >= NC) {
             r += 1;
             cc = 0;
         }
-        return r * NC + cc;
+        return (long long)r * NC + cc;
     };
-    const long long u0 = first_unit(E * cta / G);
-    const long long u1 = first_unit(E * (cta + 1) / G);
-    const long long r_lo = u0 / NC;
-    const long long r_hi = (u1 > u0) ? (u1 - 1) / NC : r_lo - 1;
+    const long long u0 = first_unit(cta);
+    const long long u1 = first_unit(cta + 1);
+    const int r_lo32i = (int)u0 / NC;   // units fit in 32 bits (checked on the host)
+    const long long r_lo = r_lo32i;
+    const long long r_hi = (u1 > u0) ? (long long)((int)(u1 - 1) / NC) : r_lo - 1;
     int rank = before;
     for (int g = g0; g < g1 && rank <= r_hi; ++g) {
         unsigned bits = s_gmask[g];
@@ -775,7 +800,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         int pend_old = -1, pend_k = 0, pend_row = 0;
         auto flush_pending = [&]() {
             if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC) {
-                // that group completed the row: hand it to the finishers
+                // that group completed the row: acquire the other groups'
+                // partials, then hand the row to the finishers
+                fence_acq_rel_gpu();
                 st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], pend_row + 1);
             }
             pend_old = -1;
@@ -890,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             __threadfence_block();
             atomicAdd(&s_ndone, 1);
         }
-        drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);   // help with the backlog
+        drain_queue(P, s_gmask, s_queue, &s_qhead, &s_ndone, lane);   // help with the backlog
     } else {
         // ---- finisher warps: scan signal, requests without masked rows, queue
         if (warp == kFirstFinisher && lane == 0) {
@@ -898,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             atomicAdd(P.ctl, 1);   // this CTA no longer reads input_ids' entry state
         }
         for (int k = warp - kFirstFinisher; k < s_nzero; k += kFinishWarps) finalize_request(P, s_zero[k], false, lane);
-        drain_queue(P, s_queue, &s_qhead, &s_ndone, lane);
+        drain_queue(P, s_gmask, s_queue, &s_qhead, &s_ndone, lane);
     }
 
     // ---- exit: the last CTA commits deferred requests and resets ----------
@@ -928,22 +955,32 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 }
 
 // Standalone features: one warp per request.
-__global__ void __launch_bounds__(256) features_kernel(int B, int L, int mask_id, const int* ids, const float* cs,
-                                                      float* feats) {
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (b >= B) return;
-    const int nk = (L + 31) >> 5;
-    float val[32];
-    bool inU[32];
-    for (int k = 0; k < nk; ++k) {
+template <int NK>
+__device__ __forceinline__ void features_one(int b, int L, int mask_id, const int* ids, const float* cs, float* feats,
+                                             int lane) {
+    float val[NK];
+    bool inU[NK];
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
         const bool valid = j < L;
         const int id = valid ? ids[(long long)b * L + j] : mask_id;
         inU[k] = valid && id != mask_id;
         val[k] = valid ? cs[(long long)b * L + j] : 0.f;
     }
-    warp_features(val, inU, nk, L, lane, feats + (long long)b * DLLM_NUM_FEATURES);
+    warp_features<NK>(val, inU, L, lane, feats + (long long)b * DLLM_NUM_FEATURES);
+}
+
+__global__ void __launch_bounds__(256) features_kernel(int B, int L, int mask_id, const int* ids, const float* cs,
+                                                      float* feats) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= B) return;
+    const int nk = (L + 31) >> 5;
+    if (nk <= 1) features_one<1>(b, L, mask_id, ids, cs, feats, lane);
+    else if (nk <= 2) features_one<2>(b, L, mask_id, ids, cs, feats, lane);
+    else if (nk <= 4) features_one<4>(b, L, mask_id, ids, cs, feats, lane);
+    else features_one<32>(b, L, mask_id, ids, cs, feats, lane);
 }
 
 int g_smem_configured[64];
@@ -983,7 +1020,9 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     if (G <= 0) return DLLM_ERR_CUDA;
     const int BL = a->B * a->L;
     const int NC = (a->V + kChunkElems - 1) / kChunkElems;
-    if ((long long)BL * NC > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
+    if ((long long)BL * NC > 0x7fffffffLL || (long long)BL * G > 0x7fffffffLL ||
+        (long long)a->V * G > 0x7fffffffLL)
+        return DLLM_ERR_UNSUPPORTED;
     const int list_cap = BL / G + 3;
     const int zero_cap = a->B / G + 1;
     const size_t smem = size_t(kStreamWarps) * kStages * kCopyBytes + size_t(kStreamWarps) * kStages * 8 +
