@@ -88,6 +88,8 @@ _SIGNATURES = {
     "dllm_step_workspace_size": (_sz, [_i32, _i32, _i32]),
     "dllm_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
     "dllm_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
+    "dllm_step_noalloc": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
+    "dllm_step_noalloc_capacity": (_sz, []),
     "dllm_features": (ctypes.c_int, [_i32, _i32, _i32, _p, _p, _p, _p]),
     "dllm_pack_plan": (ctypes.c_int, [_i32, _p, _p, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "dllm_admit": (ctypes.c_int, [_i32, _p, _i32, _p, _p, _i32, _i64, _p, ctypes.POINTER(_i32)]),

@@ -65,6 +65,7 @@ extern "C" const char* dllm_strerror(int code) {
         case DLLM_ERR_DEVICE: return "device error word set";
         case DLLM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case DLLM_ERR_UNSUPPORTED: return "shape beyond this build's limits";
+        case DLLM_ERR_SCRATCH_LIMIT: return "shape needs more scratch than dllm_step_noalloc's built-in buffer holds";
         default: return "unknown status code";
     }
 }

@@ -35,6 +35,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dllm {
@@ -1069,4 +1071,64 @@ extern "C" int dllm_features(int32_t B, int32_t L, int32_t mask_id, const int32_
                                                                           feats);
     DLLM_CUDA_TRY(cudaGetLastError());
     return DLLM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// dllm_step_noalloc: dllm_step with a built-in scratch buffer.
+//
+// Some callers cannot allocate device memory for the step's workspace: a
+// serving engine that has already handed every byte of HBM to its own pool,
+// a plain C host with no allocator of its own, or a latency-critical loop
+// where a cudaMalloc (which may synchronise the device) is not allowed.
+// For them the workspace lives in this file-scope array instead.  Every GPU
+// that loads the library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+namespace dllm {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(16) << 20;   // 16 MiB per device
+
+static __device__ __align__(256) unsigned char g_step_scratch[kNoallocScratchBytes];
+
+void* g_scratch_dev_ptr[64];
+std::mutex g_scratch_mu;
+
+// Device address of this device's scratch array; looked up once per device
+// with that device current.  nullptr if the lookup fails.
+void* scratch_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_dev_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return nullptr;
+        }
+        g_scratch_dev_ptr[dev] = p;
+    }
+    return g_scratch_dev_ptr[dev];
+}
+
+}  // namespace
+}  // namespace dllm
+
+extern "C" size_t dllm_step_noalloc_capacity(void) { return dllm::kNoallocScratchBytes; }
+
+extern "C" int dllm_step_noalloc(const dllm_step_args* a, void* stream) {
+    if (!a) return DLLM_ERR_INVAL;
+    if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1) return DLLM_ERR_INVAL;
+    if (a->B == 0) return DLLM_OK;
+    dllm::WsLayout w;
+    if (!dllm::ws_layout(a->B, a->L, a->V, dllm::kNoallocScratchBytes, &w)) return DLLM_ERR_SCRATCH_LIMIT;
+    void* scratch = dllm::scratch_ptr();
+    if (!scratch) return DLLM_ERR_CUDA;
+    // The array keeps whatever the previous call left; the step needs its
+    // counter region at zero, so clear exactly that part first.
+    DLLM_CUDA_TRY(cudaMemsetAsync(scratch, 0, w.counters_bytes, dllm::as_stream(stream)));
+    dllm_step_args b = *a;
+    b.workspace = scratch;
+    b.workspace_bytes = dllm::kNoallocScratchBytes;
+    return dllm_step(&b, stream);
 }

@@ -45,6 +45,7 @@ extern "C" {
 #define DLLM_ERR_DEVICE (-4)      /* the device error word was set (see below) */
 #define DLLM_ERR_WORKSPACE (-5)   /* workspace missing or too small */
 #define DLLM_ERR_UNSUPPORTED (-6) /* shape beyond this build's limits */
+#define DLLM_ERR_SCRATCH_LIMIT (-7) /* shape needs more than dllm_step_noalloc's built-in scratch */
 
 /* Device error word values (read with dllm_get_device_error). */
 #define DLLM_DEVERR_NONE 0
@@ -156,6 +157,33 @@ int dllm_workspace_init(void* workspace, size_t bytes, void* stream);
  * DLLM_ERR_WORKSPACE, DLLM_ERR_UNSUPPORTED, DLLM_ERR_CUDA.  A NaN threshold
  * never passes.  input_ids and conf_state may not alias any output. */
 int dllm_step(const dllm_step_args* args, void* stream);
+
+/* dllm_step without a caller workspace (the pages have no counterpart; this
+ * is a deployment convenience).  It runs exactly dllm_step, but its scratch
+ * is a fixed buffer of dllm_step_noalloc_capacity() bytes (16 MiB) that the
+ * library holds on every device it is loaded on, until the process exits.
+ * It is meant for callers that cannot allocate device memory: an engine
+ * whose memory pool already owns all of HBM, a plain C host without an
+ * allocator, or a loop where an allocation (which may synchronise the
+ * device) is not allowed.  args->workspace and args->workspace_bytes are
+ * ignored; everything else is as for dllm_step.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Each call clears the buffer's counter region (an asynchronous memset
+ *     on `stream`) and then launches the step; nothing is allocated or
+ *     freed, by this library or any library it calls.
+ *   - All calls on a device share the one buffer, which keeps the previous
+ *     call's contents: calls whose execution can overlap on the GPU (other
+ *     streams, other host threads without ordering) race and corrupt each
+ *     other.  Order them on one stream.
+ *   - Shapes whose workspace exceeds the buffer (dllm_step_workspace_size
+ *     layout, e.g. B * L * ceil(V / 8192) above roughly 700k) return
+ *     DLLM_ERR_SCRATCH_LIMIT and launch nothing. */
+int dllm_step_noalloc(const dllm_step_args* args, void* stream);
+
+/* Bytes of dllm_step_noalloc's built-in scratch buffer per device. */
+size_t dllm_step_noalloc_capacity(void);
 
 /* S6 alone: feats[b][0..5] from input_ids / conf_state as defined above
  * (DiLaServe review, section 4.2 item ③).  All pointers device. */
