@@ -26,7 +26,7 @@ import numpy as np
 
 from . import _build
 
-__all__ = ["load", "step", "step_host", "features", "pack_plan", "admit", "pack", "advance", "compact",
+__all__ = ["load", "step", "step_host", "features", "pack_plan", "admit", "pack", "advance", "compact", "refill",
            "get_device_error", "DllmError", "NUM_FEATURES", "LIB_PATH"]
 
 LIB_PATH = _build.LIB_PATH
@@ -75,6 +75,12 @@ class AdvanceArgs(ctypes.Structure):
                 ("gen_tokens", _p), ("ld_gen", _i64), ("evict", _p)]
 
 
+class RefillArgs(ctypes.Structure):
+    _fields_ = [("A0", _i32), ("n", _i32), ("L", _i32), ("mask_id", _i32),
+                ("new_rid", _p), ("new_p", _p), ("new_K", _p), ("new_thr", _p),
+                ("rid", _p), ("p", _p), ("b", _p), ("K", _p), ("thr", _p), ("input_ids", _p), ("conf_state", _p)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -97,6 +103,7 @@ _SIGNATURES = {
     "dllm_advance": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), _p]),
     "dllm_compact_workspace_size": (_sz, [_i32, _i32, _p]),
     "dllm_compact": (ctypes.c_int, [ctypes.POINTER(CompactArgs), _p]),
+    "dllm_refill": (ctypes.c_int, [ctypes.POINTER(RefillArgs), _p]),
 }
 
 
@@ -130,7 +137,7 @@ def load(build=True):
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs)):
+        for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs)):
             if lib.dllm_struct_size(which) != ctypes.sizeof(cls):
                 raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {lib.dllm_struct_size(which)} "
                                    f"bytes, binding {ctypes.sizeof(cls)}")
@@ -392,3 +399,13 @@ def compact(evict, arrays, *, new_index=None, src_row=None, A_out=None):
                     workspace_bytes=ws.numel())
     _check("dllm_compact", lib.dllm_compact(ctypes.byref(a), _stream(dev)))
     return new_index, src_row, A_out
+
+
+def refill(A0, new_rid, new_p, new_K, new_thr, rid, p, b, K, thr, input_ids, conf_state, *, mask_id):
+    """Initialise rows [A0, A0 + n) for admitted requests (dllm_refill)."""
+    dev = _require_cuda(new_rid, new_p, new_K, new_thr, rid, p, b, K, thr, input_ids, conf_state)
+    n = new_rid.numel()
+    a = RefillArgs(A0=A0, n=n, L=input_ids.shape[1], mask_id=mask_id, new_rid=_ptr(new_rid), new_p=_ptr(new_p),
+                   new_K=_ptr(new_K), new_thr=_ptr(new_thr), rid=_ptr(rid), p=_ptr(p), b=_ptr(b), K=_ptr(K),
+                   thr=_ptr(thr), input_ids=_ptr(input_ids), conf_state=_ptr(conf_state))
+    _check("dllm_refill", load().dllm_refill(ctypes.byref(a), _stream(dev)))

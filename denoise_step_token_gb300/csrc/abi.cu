@@ -84,6 +84,7 @@ extern "C" size_t dllm_struct_size(int which) {
         case 1: return sizeof(dllm_pack_args);
         case 2: return sizeof(dllm_compact_args);
         case 3: return sizeof(dllm_advance_args);
+        case 4: return sizeof(dllm_refill_args);
         default: return 0;
     }
 }

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
         const int p = __ldg(P.p + i);
         const int b = __ldg(P.b + i);
         const long long width = (long long)p + (long long)(b + 1) * P.L;
-        if (p < 0 || b < 0 || width > P.W) {
+        if (p < 0 || b < 0 || width > P.W || (p > 0 && !P.prompt_tokens) || (b > 0 && !P.gen_tokens)) {
             if (c == 0) set_error(P.err, DLLM_DEVERR_ROW_WIDTH);
             continue;
         }
@@ -155,16 +155,34 @@ struct CompactParams {
     long long row_bytes[DLLM_COMPACT_MAX_ARRAYS];
 };
 
-__device__ __forceinline__ void copy_row(unsigned char* dst, const unsigned char* src, long long n, int t, int nt) {
+// Copy `rows` rows of one array, all rows in flight at once: thread t of
+// nt handles 32-bit words (or bytes, when a row is not word-sized or the
+// pointers are not word-aligned) t, t + nt, ... of the flattened rows.
+// dst_row(r) < 0 skips row r.
+template <typename DstRow>
+__device__ __forceinline__ void copy_rows(unsigned char* dst, const unsigned char* src, long long rb, int rows,
+                                          DstRow dst_row, long long src_row0, int t, int nt) {
     const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src);
-    if ((n & 15) == 0 && (al & 15) == 0) {
-        for (long long k = t; k < n / 16; k += nt)
-            reinterpret_cast<uint4*>(dst)[k] = reinterpret_cast<const uint4*>(src)[k];
-    } else if ((n & 3) == 0 && (al & 3) == 0) {
-        for (long long k = t; k < n / 4; k += nt)
-            reinterpret_cast<uint32_t*>(dst)[k] = reinterpret_cast<const uint32_t*>(src)[k];
+    if ((rb & 3) == 0 && (al & 3) == 0) {
+        const long long wpr = rb >> 2;
+        const long long total = wpr * rows;
+        for (long long k = t; k < total; k += nt) {
+            const int r = (int)(k / wpr);
+            const long long w = k - (long long)r * wpr;
+            const int d = dst_row(r);
+            if (d < 0) continue;
+            reinterpret_cast<uint32_t*>(dst)[(long long)d * wpr + w] =
+                reinterpret_cast<const uint32_t*>(src)[(src_row0 + r) * wpr + w];
+        }
     } else {
-        for (long long k = t; k < n; k += nt) dst[k] = src[k];
+        const long long total = rb * rows;
+        for (long long k = t; k < total; k += nt) {
+            const int r = (int)(k / rb);
+            const long long w = k - (long long)r * rb;
+            const int d = dst_row(r);
+            if (d < 0) continue;
+            dst[(long long)d * rb + w] = src[(src_row0 + r) * rb + w];
+        }
     }
 }
 
@@ -207,25 +225,53 @@ __global__ void __launch_bounds__(kCompactRows) compact_scatter_kernel(const __g
     __syncthreads();
     // scatter every kept row of every array into its staging copy
     const int rows = min(kCompactRows, P.A - i0);
-    for (int a = 0; a < P.n_arrays; ++a) {
-        const long long rb = P.row_bytes[a];
-        for (int r = warp; r < rows; r += kCompactRows / 32) {
-            const int d = s_new[r];
-            if (d < 0) continue;
-            copy_row(P.stage[a] + (long long)d * rb, P.arrays[a] + (long long)(i0 + r) * rb, rb, lane, 32);
-        }
-    }
+    for (int a = 0; a < P.n_arrays; ++a)
+        copy_rows(P.stage[a], P.arrays[a], P.row_bytes[a], rows, [&](int r) { return s_new[r]; }, i0, t,
+                  kCompactRows);
 }
 
 __global__ void __launch_bounds__(256) compact_copyback_kernel(const __grid_constant__ CompactParams P) {
     const int n = *P.A_out;
-    const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int nw = gridDim.x * (blockDim.x >> 5);
-    for (int a = 0; a < P.n_arrays; ++a) {
-        const long long rb = P.row_bytes[a];
-        for (int r = gw; r < n; r += nw)
-            copy_row(P.arrays[a] + (long long)r * rb, P.stage[a] + (long long)r * rb, rb, lane, 32);
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int nt = gridDim.x * blockDim.x;
+    for (int a = 0; a < P.n_arrays; ++a)
+        copy_rows(P.arrays[a], P.stage[a], P.row_bytes[a], n, [](int r) { return r; }, 0, t, nt);
+}
+
+// ---------------------------------------------------------------------------
+// dllm_refill: initialise appended rows
+// ---------------------------------------------------------------------------
+struct RefillParams {
+    int A0, n, L, mask_id;
+    const int* new_rid;
+    const int* new_p;
+    const int* new_K;
+    const float* new_thr;
+    int* rid;
+    int* p;
+    int* b;
+    int* K;
+    float* thr;
+    int* ids;
+    float* cs;
+};
+
+__global__ void __launch_bounds__(256) refill_kernel(const __grid_constant__ RefillParams P) {
+    const long long total = (long long)P.n * P.L;
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < total;
+         k += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(k / P.L);
+        const long long dst = (long long)(P.A0 + r) * P.L + (k - (long long)r * P.L);
+        P.ids[dst] = P.mask_id;
+        P.cs[dst] = __int_as_float(0x7fc00000);
+        if (k - (long long)r * P.L == 0) {
+            const int row = P.A0 + r;
+            P.rid[row] = P.new_rid[r];
+            P.p[row] = P.new_p[r];
+            P.b[row] = 0;
+            P.K[row] = P.new_K[r];
+            P.thr[row] = P.new_thr[r];
+        }
     }
 }
 
@@ -325,9 +371,8 @@ extern "C" int dllm_admit(int32_t n_pending, const int32_t* pending_p, int32_t A
 extern "C" int dllm_pack(const dllm_pack_args* a, void* stream) {
     if (!a || a->A < 0 || a->L < 1 || a->W < 0) return DLLM_ERR_INVAL;
     if (a->A == 0 || a->W == 0) return DLLM_OK;
-    if (!a->p || !a->b || !a->rid || !a->prompt_off || !a->prompt_tokens || !a->block_ids || !a->ids)
-        return DLLM_ERR_INVAL;
-    if (!a->gen_tokens || a->ld_gen < 0) return DLLM_ERR_INVAL;
+    if (!a->p || !a->b || !a->rid || !a->prompt_off || !a->block_ids || !a->ids) return DLLM_ERR_INVAL;
+    if (a->ld_gen < 0) return DLLM_ERR_INVAL;
     PackParams P;
     P.A = a->A; P.L = a->L; P.W = a->W; P.pad_id = a->pad_id;
     P.p = a->p; P.b = a->b; P.rid = a->rid; P.prompt_off = reinterpret_cast<const long long*>(a->prompt_off);
@@ -403,10 +448,30 @@ extern "C" int dllm_compact(const dllm_compact_args* a, void* stream) {
     compact_scatter_kernel<<<blocks, kCompactRows, 0, s>>>(P);
     DLLM_CUDA_TRY(cudaGetLastError());
     if (a->n_arrays > 0) {
+        long long words = 0;
+        for (int k = 0; k < a->n_arrays; ++k) words += (long long)a->A * ((a->row_bytes[k] + 3) / 4);
         const int sms = std::max(sm_count(), 1);
-        const int cb = std::min((a->A + 7) / 8, sms * 4);
+        const int cb = (int)std::max(1LL, std::min((words + 255) / 256, (long long)sms * 4));
         compact_copyback_kernel<<<cb, 256, 0, s>>>(P);
         DLLM_CUDA_TRY(cudaGetLastError());
     }
+    return DLLM_OK;
+}
+
+extern "C" int dllm_refill(const dllm_refill_args* a, void* stream) {
+    if (!a || a->A0 < 0 || a->n < 0 || a->L < 1 || a->L > DLLM_MAX_L) return DLLM_ERR_INVAL;
+    if (a->n == 0) return DLLM_OK;
+    if (!a->new_rid || !a->new_p || !a->new_K || !a->new_thr || !a->rid || !a->p || !a->b || !a->K || !a->thr ||
+        !a->input_ids || !a->conf_state)
+        return DLLM_ERR_INVAL;
+    RefillParams P;
+    P.A0 = a->A0; P.n = a->n; P.L = a->L; P.mask_id = a->mask_id;
+    P.new_rid = a->new_rid; P.new_p = a->new_p; P.new_K = a->new_K; P.new_thr = a->new_thr;
+    P.rid = a->rid; P.p = a->p; P.b = a->b; P.K = a->K; P.thr = a->thr; P.ids = a->input_ids; P.cs = a->conf_state;
+    const long long total = (long long)a->n * a->L;
+    const int sms = std::max(sm_count(), 1);
+    const int blocks = (int)std::max(1LL, std::min((total + 255) / 256, (long long)sms * 4));
+    refill_kernel<<<blocks, 256, 0, as_stream(stream)>>>(P);
+    DLLM_CUDA_TRY(cudaGetLastError());
     return DLLM_OK;
 }

@@ -70,7 +70,7 @@ int dllm_last_cuda_error(const char** name);
 
 /* sizeof() of the argument structs below, for binding self-checks:
  * which = 0 dllm_step_args, 1 dllm_pack_args, 2 dllm_compact_args,
- * 3 dllm_advance_args.  Returns 0 for an unknown `which`. */
+ * 3 dllm_advance_args, 4 dllm_refill_args.  Returns 0 for an unknown `which`. */
 size_t dllm_struct_size(int which);
 
 /* Synchronise `stream`, then return in *code the first device error
@@ -229,7 +229,9 @@ int dllm_admit(int32_t n_pending, const int32_t* pending_p, int32_t A,
  *   blk_start[i] = p[i] + b[i] * L, the logical position of the active
  *     block, which always occupies box columns [W - L, W) (the gather /
  *     scatter region of every row).
- * A row with width_i > W is skipped and sets DLLM_DEVERR_ROW_WIDTH.
+ * A row with width_i > W, or one that needs prompt_tokens or gen_tokens
+ * while that pointer is NULL, is skipped and sets DLLM_DEVERR_ROW_WIDTH.
+ * (prompt_tokens may be NULL when every p is 0, gen_tokens when every b is 0.)
  * ====================================================================== */
 typedef struct dllm_pack_args {
     int32_t A;                    /* rows */
@@ -311,6 +313,36 @@ typedef struct dllm_compact_args {
 size_t dllm_compact_workspace_size(int32_t A, int32_t n_arrays, const int64_t* row_bytes);
 
 int dllm_compact(const dllm_compact_args* args, void* stream);
+
+/* ======================================================================
+ * dllm_refill -- append admitted requests (S9 refill).
+ *
+ * BlockServe page, section II-D (refill from the pending queue) and
+ * section II-E (every block starts fully masked); survivors keep their rows
+ * and admitted requests are appended after them, in admission order.
+ * Rows [A0, A0 + n) of the row arrays receive request new_rid[r] with prompt
+ * length new_p[r], new_K[r] blocks to generate and threshold new_thr[r];
+ * their block index becomes 0, input_ids becomes mask_id and conf_state NaN.
+ * ====================================================================== */
+typedef struct dllm_refill_args {
+    int32_t A0;               /* first appended row */
+    int32_t n;                /* rows appended */
+    int32_t L;
+    int32_t mask_id;
+    const int32_t* new_rid;   /* device [n] */
+    const int32_t* new_p;     /* device [n] */
+    const int32_t* new_K;     /* device [n] */
+    const float* new_thr;     /* device [n] */
+    int32_t* rid;             /* device row arrays, >= A0 + n rows */
+    int32_t* p;
+    int32_t* b;
+    int32_t* K;
+    float* thr;
+    int32_t* input_ids;       /* device [rows][L] */
+    float* conf_state;        /* device [rows][L] */
+} dllm_refill_args;
+
+int dllm_refill(const dllm_refill_args* args, void* stream);
 
 #ifdef __cplusplus
 }

@@ -23,6 +23,29 @@ import numpy as np
 from . import admit, box_width, compact, cost, pack, step
 
 
+def advance(adv, rid, b, K, ids, cs, gen, mask_id):
+    """BlockServe Algorithm 1, lines "update r_i's outputs with Y[i] and set
+    b_i <- b_i + 1" and "remove any request with b_i >= K_i": for every row
+    whose block is committed this iteration, append the block to the
+    request's output, move to the next block and flag the row for eviction
+    once all K_i blocks are done; a continuing row starts its new block fully
+    masked (BlockServe section II-E).  Arrays are updated in place (numpy);
+    ``gen[r]`` is a list of committed tokens.  Returns the eviction flags."""
+    evict = np.zeros(len(adv), dtype=bool)
+    for i in range(len(adv)):
+        if not adv[i]:
+            continue
+        r = int(rid[i])
+        gen[r] = np.concatenate([gen[r], ids[i]])
+        b[i] += 1
+        if b[i] >= K[i]:
+            evict[i] = True
+        else:
+            ids[i] = mask_id
+            cs[i] = np.nan
+    return evict
+
+
 class OracleLoop:
     def __init__(self, p, K, prompts, thr, L, V, mask_id, pad_id, budget, mode="fdfo"):
         assert mode in ("fdfo", "sync")
@@ -101,21 +124,16 @@ class OracleLoop:
     # -- Algorithm 1: update outputs, b_i += 1, evict b_i >= K_i ---------------
     def finish_phase(self, done):
         done = np.asarray(done, dtype=bool)
-        advance = done if self.mode == "fdfo" else (np.full(done.shape, done.all()) if done.size else done)
-        evict = np.zeros(len(self.rid), dtype=bool)
+        adv = done if self.mode == "fdfo" else (np.full(done.shape, done.all()) if done.size else done)
+        b = np.array(self.b, dtype=np.int64)
+        K = np.array([self.K_all[r] for r in self.rid], dtype=np.int64)
+        evict = advance(adv, self.rid, b, K, self.ids, self.cs, self.gen, self.mask_id)
+        self.b = b.tolist()
         for i in range(len(self.rid)):
-            if not advance[i]:
-                continue
-            r = self.rid[i]
-            self.gen[r] = np.concatenate([self.gen[r], self.ids[i]])
-            self.b[i] += 1
-            self.s[i] = 0
-            if self.b[i] >= self.K_all[r]:
-                evict[i] = True
-                self.finish_iter[r] = self.iteration
-            else:
-                self.ids[i] = self.mask_id
-                self.cs[i] = np.nan
+            if adv[i]:
+                self.s[i] = 0
+                if evict[i]:
+                    self.finish_iter[self.rid[i]] = self.iteration
         new_index, src_row, A2 = compact(evict)
         self.rid = [self.rid[i] for i in src_row]
         self.b = [self.b[i] for i in src_row]
