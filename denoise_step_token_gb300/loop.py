@@ -1,0 +1,153 @@
+"""Mixed-state serving loop on the GPU: BlockServe Algorithm 1 with the FDFO
+execution mode.
+
+BlockServe page, section II-C (Algorithm 1): admit from the pending queue
+under the token budget of eq. (1), run the active set one step, commit
+finished blocks (b_i <- b_i + 1) and evict requests with b_i >= K_i.
+FDFO page, sections "FDFO 的核心思想" and "工程设计一": in FDFO mode a
+request whose block is done commits and leaves (or starts its next block)
+at once; in sync mode (``_run_sync``) nothing commits until every active
+block is done.
+
+The host keeps only what admission needs (prompt lengths and block indices
+of the active rows) and reads back one byte per row per step, the done
+flags -- the pages' ``accept_length_per_req_cpu``.  Refill, packing, the
+step, block commit and compaction run in libdllm's kernels.  The model
+forward is outside this loop: the caller supplies each step's logits.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import admit, advance, compact, pack, pack_plan, refill, step
+
+
+class DeviceLoop:
+    """One pending queue served to completion on one device."""
+
+    def __init__(self, p, K, prompt_off, prompt_tokens, thr, *, L, V, mask_id, pad_id, budget, device,
+                 mode="fdfo", capacity=None, features=True):
+        import torch
+        assert mode in ("fdfo", "sync")
+        self.torch = torch
+        self.L, self.V, self.mask_id, self.pad_id = int(L), int(V), int(mask_id), int(pad_id)
+        self.budget, self.mode, self.device, self.features = int(budget), mode, device, features
+        self.p_all = np.asarray(p, dtype=np.int32)
+        self.K_all = np.asarray(K, dtype=np.int32)
+        self.thr_all = np.asarray(thr, dtype=np.float32)
+        R = len(self.p_all)
+        self.R = R
+        # pending queue: sorted by prompt length, ties by request id
+        self.pending = sorted(range(R), key=lambda r: (int(self.p_all[r]), r))
+        cap = R if capacity is None else int(capacity)
+        self.cap = cap
+        i32, f32 = torch.int32, torch.float32
+        z = lambda *shape, dtype=i32: torch.zeros(shape, dtype=dtype, device=device)
+        self.rid, self.p, self.b, self.K = z(cap), z(cap), z(cap), z(cap)
+        self.thr = z(cap, dtype=f32)
+        self.ids = torch.full((cap, L), self.mask_id, dtype=i32, device=device)
+        self.cs = torch.full((cap, L), float("nan"), dtype=f32, device=device)
+        self.gen = z(R, int(self.K_all.max()) * L if R else L)
+        self.prompt_off = torch.as_tensor(np.asarray(prompt_off, dtype=np.int64)).to(device)
+        self.prompt_tokens = torch.as_tensor(np.asarray(prompt_tokens, dtype=np.int32)).to(device)
+        # host mirrors of the active rows
+        self.A = 0
+        self.rid_h = np.zeros(0, dtype=np.int32)
+        self.b_h = np.zeros(0, dtype=np.int32)
+        self.s_h = np.zeros(0, dtype=np.int32)      # steps taken in the current block
+        self.wait_h = np.zeros(0, dtype=bool)       # block done, waiting (sync mode)
+        self.iteration = 0
+        self.box = None
+        self.W = 0
+        self.cost = 0
+        self.last = None
+
+    # -- admission and refill (Algorithm 1, "admit") -------------------------
+    def admit_phase(self):
+        torch = self.torch
+        if not self.pending:
+            return []
+        pend_p = self.p_all[self.pending]
+        picked = admit(pend_p, self.p_all[self.rid_h], self.b_h, self.L, self.budget)
+        if not picked:
+            return []
+        new = [self.pending[k] for k in picked]
+        for k in sorted(picked, reverse=True):
+            del self.pending[k]
+        n = len(new)
+        if self.A + n > self.cap:
+            raise RuntimeError("active set exceeds the loop's row capacity")
+        d = lambda x, dt: torch.as_tensor(np.asarray(x, dtype=dt)).to(self.device)
+        refill(self.A, d(new, np.int32), d(self.p_all[new], np.int32), d(self.K_all[new], np.int32),
+               d(self.thr_all[new], np.float32), self.rid, self.p, self.b, self.K, self.thr, self.ids, self.cs,
+               mask_id=self.mask_id)
+        self.A += n
+        self.rid_h = np.concatenate([self.rid_h, np.asarray(new, dtype=np.int32)])
+        self.b_h = np.concatenate([self.b_h, np.zeros(n, dtype=np.int32)])
+        self.s_h = np.concatenate([self.s_h, np.zeros(n, dtype=np.int32)])
+        self.wait_h = np.concatenate([self.wait_h, np.zeros(n, dtype=bool)])
+        return new
+
+    # -- the box of eq. (1) (BlockServe section II-E) -------------------------
+    def pack_phase(self):
+        A = self.A
+        self.W, self.cost = pack_plan(self.p_all[self.rid_h], self.b_h, self.L)
+        if A == 0:
+            self.box = None
+            return None
+        self.box = pack(self.p[:A], self.b[:A], self.rid[:A], self.prompt_off, self.prompt_tokens, self.gen,
+                        self.ids[:A], L=self.L, W=self.W, pad_id=self.pad_id)
+        return self.box
+
+    # -- one denoise step -------------------------------------------------------
+    def step_phase(self, logits):
+        A = self.A
+        out = step(logits, self.ids[:A], self.thr[:A], self.cs[:A], V=self.V, mask_id=self.mask_id,
+                   feats=self.features)
+        done = out["done"].cpu().numpy().astype(bool)     # the per-step readback
+        self.last = out
+        return done, out
+
+    # -- commit finished blocks, evict, compact ----------------------------------
+    def finish_phase(self, done):
+        torch = self.torch
+        A = self.A
+        if self.mode == "fdfo":
+            adv = done
+        else:
+            adv = done if done.all() else np.zeros_like(done)
+        # a row stepped unless its block was already done and waiting
+        stepped = ~self.wait_h
+        adv_d = torch.as_tensor(adv.astype(np.uint8)).to(self.device)
+        evict_d = advance(adv_d, self.rid[:A], self.K[:A], self.b[:A], self.ids[:A], self.cs[:A], self.gen,
+                          mask_id=self.mask_id)
+        b = self.b_h.copy()
+        s = self.s_h + stepped.astype(np.int32)
+        b[adv] += 1
+        s[adv] = 0
+        evict = adv & (b >= self.K_all[self.rid_h])
+        _, _, A_out = compact(evict_d, [self.rid[:A], self.p[:A], self.b[:A], self.K[:A], self.thr[:A],
+                                        self.ids[:A], self.cs[:A]])
+        keep = ~evict
+        wait = done & ~adv
+        self.rid_h, self.b_h, self.s_h, self.wait_h = self.rid_h[keep], b[keep], s[keep], wait[keep]
+        self.A = int(keep.sum())
+        self.iteration += 1
+        return evict, A_out
+
+    def finished(self):
+        return not self.pending and self.A == 0
+
+    def masked_rows(self):
+        """(row * L + j, rid, b, s, j) of every masked position (reads the
+        block tokens back; a driver that generates logits needs this)."""
+        A = self.A
+        if A == 0:
+            return []
+        ids = self.ids[:A].cpu().numpy()
+        rows, js = np.nonzero(ids == self.mask_id)
+        return [(int(i) * self.L + int(j), int(self.rid_h[i]), int(self.b_h[i]), int(self.s_h[i]), int(j))
+                for i, j in zip(rows, js)]
+
+    def generated(self):
+        return self.gen.cpu().numpy()

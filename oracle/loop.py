@@ -150,11 +150,12 @@ class OracleLoop:
         """Drive the loop to completion; ``logits_fn(rows)`` returns uint16
         [len(rid) * L, ldv] logits for ``masked_rows()`` tuples."""
         while not self.finished() and self.iteration < max_iters:
-            self.admit_phase()
+            new = self.admit_phase()
             rows = self.masked_rows()
             logits = logits_fn(self, rows)
             res = self.step_phase(logits)
             waiting = int(((~res["masked"].any(axis=1)) & (res["done"] == 1)).sum())
-            self.trace.append(dict(A=len(self.rid), W=self.width(), M=len(rows), waiting=waiting))
+            self.trace.append(dict(A=len(self.rid), W=self.width(), M=len(rows), waiting=waiting,
+                                   admitted=len(new), cost=self.cost()))
             self.finish_phase(res["done"])
         return self

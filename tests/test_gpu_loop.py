@@ -1,0 +1,134 @@
+"""The mixed-state serving loop on the GPU, in lockstep with the oracle loop.
+
+Every iteration compares admission, the packed box, the masked rows, the
+step's outputs, block commits, evictions and the compacted batch; at the
+end every request's generated tokens.  Each step's logits are a pure
+function of (request, block, step in block, position) and carry the 1e-4
+decision margins (redrawn through the oracle when needed).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import MARGIN
+from oracle.loop import OracleLoop
+
+pytestmark = pytest.mark.gpu
+
+
+def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv):
+    """Logits [A*L, ldv] for the masked rows, with decision margins."""
+    out = np.full((max(A * L, 1), ldv), synth.POISON_BITS, dtype=np.uint16)
+    if not rows:
+        return out
+    flat = np.array([r[0] for r in rows])
+    key_of = lambda r: (r[1], r[2], r[3], r[4])
+    for _ in range(50):
+        keys = synth.logits_row_keys(seed, [r[1] for r in rows], [r[2] for r in rows], [r[3] for r in rows],
+                                     [r[4] for r in rows], [salts.get(key_of(r), 0) for r in rows])
+        synth.fill_logits_rows(out, V, flat, keys, offset, mask_id)
+        conf, _, _ = oracle.rows_stats(out, flat, V)
+        bad = set()
+        by_row = {}
+        for k, r in enumerate(rows):
+            t = float(np.float32(thr_of_row[r[0] // L]))
+            if abs(conf[k] - t) < MARGIN:
+                bad.add(k)
+            by_row.setdefault(r[0] // L, []).append(k)
+        for i, ks in by_row.items():
+            t = float(np.float32(thr_of_row[i]))
+            c = conf[ks]
+            if not (c > t).any() and len(ks) > 1:
+                order = np.argsort(-c, kind="stable")
+                if c[order[0]] - c[order[1]] < MARGIN:
+                    bad.add(ks[order[0]])
+        if not bad:
+            return out
+        for k in bad:
+            salts[key_of(rows[k])] = salts.get(key_of(rows[k]), 0) + 1
+    raise AssertionError("no margin after 50 redraws")
+
+
+def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000):
+    import torch
+    from denoise_step_token_gb300.loop import DeviceLoop
+    reqs = synth.make_loop_requests(cfg, seed)
+    R, L, V = cfg.R, cfg.L, cfg.V
+    prompts = [reqs.prompt_tokens[reqs.prompt_off[r]:reqs.prompt_off[r + 1]] for r in range(R)]
+    ol = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode)
+    gl = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V, mask_id=cfg.mask_id,
+                    pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode)
+    salts = {}
+    trace = []
+    while not ol.finished() and ol.iteration < max_iters:
+        assert not gl.finished()
+        new_o = ol.admit_phase()
+        new_g = gl.admit_phase()
+        assert new_o == new_g, ol.iteration
+        box_o = ol.box()
+        box_g = gl.pack_phase()
+        assert gl.W == box_o["W"] and gl.cost == ol.cost()
+        if new_o:
+            # Algorithm 1 admits only while eq. (1) stays within the budget;
+            # active rows widen afterwards as their blocks commit
+            assert gl.cost <= cfg.budget
+        for k in ("ids", "attn", "pos", "pad", "blk_start"):
+            np.testing.assert_array_equal(box_g[k].cpu().numpy(), box_o[k], err_msg=k)
+        rows_o = ol.masked_rows()
+        assert rows_o == gl.masked_rows()
+        thr_of_row = np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32)
+        logits = _loop_logits(seed, rows_o, len(ol.rid), L, V, cfg.offset_max, cfg.mask_id, thr_of_row, salts,
+                              cfg.row_stride)
+        ref = ol.step_phase(logits[: len(ol.rid) * L])
+        done_g, out = gl.step_phase(torch.from_numpy(logits[: len(ol.rid) * L].view(np.int16)).to(device))
+        np.testing.assert_array_equal(done_g.astype(np.uint8), ref["done"])
+        np.testing.assert_array_equal(out["n_new"].cpu().numpy(), ref["n_new"])
+        np.testing.assert_array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
+        np.testing.assert_array_equal(gl.ids[: gl.A].cpu().numpy(), ref["input_ids"])
+        np.testing.assert_allclose(out["feats"].cpu().numpy(), ref["feats"], rtol=0, atol=1e-5, equal_nan=True)
+        ev_o, _, _, A_o = ol.finish_phase(ref["done"])
+        ev_g, A_out = gl.finish_phase(done_g)
+        np.testing.assert_array_equal(ev_g, ev_o)
+        assert int(A_out.cpu().numpy()[0]) == A_o == gl.A
+        assert list(gl.rid_h) == ol.rid and list(gl.b_h) == ol.b
+        np.testing.assert_array_equal(gl.rid[: gl.A].cpu().numpy(), ol.rid)
+        np.testing.assert_array_equal(gl.b[: gl.A].cpu().numpy(), ol.b)
+        trace.append((len(rows_o), int(ref["done"].sum())))
+    assert ol.finished() and gl.finished()
+    gen = gl.generated()
+    for r in range(R):
+        np.testing.assert_array_equal(gen[r][: reqs.K[r] * L], ol.gen[r])
+    assert dllm.get_device_error(device) == 0
+    return ol, trace
+
+
+@pytest.fixture(scope="module")
+def device(dllm):
+    import torch
+    return torch.device("cuda", 0)
+
+
+SMALL = synth.LoopConfig("small_loop", 24, 3, 60, 24, 8, 4099, 600, 0.9, 10.0)
+
+
+@pytest.mark.parametrize("mode", ["fdfo", "sync"])
+def test_loop_lockstep_small(dllm, device, mode):
+    ol, trace = _lockstep(dllm, device, SMALL, mode, seed=3)
+    assert ol.iteration == len(trace) > 0
+
+
+def test_loop_lockstep_blockserve_shape_reduced_vocab(dllm, device):
+    # the BlockServe loop's geometry (256 requests, prompts U[64, 1024], 8
+    # blocks of 32, budget 2^20) with a small vocabulary so the oracle keeps up
+    cfg = synth.LoopConfig("bs_small_v", 256, 64, 1024, 256, 32, 1031, 1 << 20, 0.9, 8.0)
+    ol, trace = _lockstep(dllm, device, cfg, "fdfo", seed=5)
+    assert sum(t[0] for t in trace) > 0
+
+
+def test_fdfo_and_sync_agree_and_fdfo_wastes_nothing(dllm, device):
+    f, tf = _lockstep(dllm, device, SMALL, "fdfo", seed=4)
+    s, ts = _lockstep(dllm, device, SMALL, "sync", seed=4)
+    for r in range(SMALL.R):
+        np.testing.assert_array_equal(f.gen[r], s.gen[r])
+    assert f.iteration <= s.iteration

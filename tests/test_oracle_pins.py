@@ -497,7 +497,9 @@ def test_loop_completes_and_fdfo_matches_sync_tokens():
     assert sum(t["waiting"] for t in f.trace) == 0
     assert sum(t["waiting"] for t in s.trace) > 0
     for t in f.trace:
-        assert t["A"] * t["W"] <= cfg.budget
+        if t["admitted"]:
+            # eq. (1) within the budget right after an admission
+            assert t["cost"] <= cfg.budget
 
 
 def test_loop_bs1_fdfo_equals_sync():
