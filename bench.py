@@ -43,8 +43,13 @@ import synth  # noqa: E402
 
 METRIC = "masked positions/sec and logits GB/s per denoise step (% of GB300 HBM peak), 1 GPU"
 UNIT = "masked positions/s"
-WORKLOAD = "dream7b_shaped_mixed_state_step"
-CONFIG_NAME = "dream"
+WORKLOADS = {
+    "dream": "dream7b_shaped_mixed_state_step",
+    "llada": "llada8b_shaped_mixed_state_step",
+    "stress": "large_batch_stress_step",
+    "tiny": "tiny_step",
+    "blockserve": "blockserve_mixed_state_loop",
+}
 LOOP_K = 8                     # blocks per request (gen 256 / L 32)
 BUDGET = 1 << 20               # token budget of eq. (1)
 FALLBACK_HBM_GBS = 6800.0
@@ -75,8 +80,8 @@ def aggregate(units_local, seconds_local, dist=None):
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def make_workload(seed):
-    cfg = synth.STEP_CONFIGS[CONFIG_NAME]
+def make_workload(seed, name="dream"):
+    cfg = synth.STEP_CONFIGS[name]
     inp = synth.make_step_state(cfg, seed)
     lcfg = synth.LoopConfig("mixed", cfg.B, 64, 1024, LOOP_K * cfg.L, cfg.L, cfg.V, BUDGET, 0.9, cfg.offset_max)
     reqs = synth.make_loop_requests(lcfg, seed)
@@ -341,7 +346,7 @@ def run_gpu(args, rank, world, local_rank, dist):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     dllm.load()
-    cfg, inp, reqs, b, gen, pending_p = make_workload(seed=1000 + rank)
+    cfg, inp, reqs, b, gen, pending_p = make_workload(1000 + rank, args.workload)
     pipe = Pipeline(cfg, inp, reqs, b, gen, pending_p, device)
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -477,7 +482,7 @@ def cpu_baseline(inp):
 
 def run_reference(args, rank, world):
     """The oracle, as it stands, timed on the host cores (reference arm)."""
-    cfg, inp, *_ = make_workload(seed=1000)
+    cfg, inp, *_ = make_workload(1000, "dream" if args.workload == "blockserve" else args.workload)
     threads = os.cpu_count() or 1
     # probe: one request, to size each step's sample so the run ends in ~2 min
     probe_rows, probe_s = oracle_over_requests(inp, [int(np.argmax(inp.masked.sum(axis=1)))], 1)
@@ -511,7 +516,7 @@ def run_reference(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD, "B": cfg.B, "L": cfg.L, "V": cfg.V,
+        "config": {"workload": WORKLOADS[args.workload], "B": cfg.B, "L": cfg.L, "V": cfg.V,
                    "sample_rows_per_step": target_rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"each step: about {target_rows} masked rows of the Dream-shaped batch, "
@@ -521,6 +526,86 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# BlockServe mixed-state loop: 256 requests served to completion
+# ---------------------------------------------------------------------------
+def run_loop_bench(args, rank, world, local_rank):
+    """FDFO serving loop over the full BlockServe-shaped queue.  The timed
+    part of each iteration is the hot path (admission, refill, pack, step,
+    done readback, advance, compaction); producing the step's logits (the
+    model forward's job) is not timed: each masked position's row is
+    gathered on the device from a pool of generated rows, chosen by a hash
+    of (request, block, step, position)."""
+    import torch
+    import denoise_step_token_gb300 as dllm
+    from denoise_step_token_gb300.loop import DeviceLoop
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dllm.load()
+    lcfg = synth.LOOP_CONFIGS["blockserve"]
+    seed = 2000 + rank
+    reqs = synth.make_loop_requests(lcfg, seed)
+    L, V, ldv = lcfg.L, lcfg.V, lcfg.row_stride
+    pool_rows = 4096
+    pool_h = np.empty((pool_rows, ldv), dtype=np.uint16)
+    keys = synth.logits_row_keys(seed, np.arange(pool_rows), 0, 0, 0, 0)
+    synth.fill_logits_rows(pool_h, V, np.arange(pool_rows), keys, lcfg.offset_max, lcfg.mask_id)
+    pool = torch.from_numpy(pool_h.view(np.int16)).to(device)
+    loop = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V,
+                      mask_id=lcfg.mask_id, pad_id=lcfg.pad_id, budget=lcfg.budget, device=device, mode="fdfo")
+    logits = torch.empty((lcfg.R * L, ldv), dtype=torch.int16, device=device)
+    ev = []
+    step_ms = []
+    masked_total = 0
+    iters = 0
+    pack_plan_s = 0.0
+    while not loop.finished():
+        # timed: admission (host) and refill
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        loop.admit_phase()
+        torch.cuda.synchronize()
+        t_admit = time.perf_counter() - t0
+        # untimed: the model forward's stand-in -- pool rows for the masked positions
+        rows = loop.masked_rows()
+        if rows:
+            flat = torch.as_tensor([r[0] for r in rows], device=device)
+            h = synth.out(np.uint64(seed), np.asarray([((r[1] * 64 + r[2]) * 4096 + r[3]) * 64 + r[4]
+                                                       for r in rows], dtype=np.uint64))
+            pick = torch.as_tensor((h % np.uint64(pool_rows)).astype(np.int64), device=device)
+            logits[flat] = pool[pick]
+        # timed: pack, step, done readback, advance, compaction
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        loop.pack_phase()
+        e0.record()
+        done, _ = loop.step_phase(logits[: loop.A * L])
+        e1.record()
+        loop.finish_phase(done)
+        torch.cuda.synchronize()
+        t_rest = time.perf_counter() - t1
+        ev.append(t_admit + t_rest)
+        step_ms.append(e0.elapsed_time(e1))
+        iters += 1
+        masked_total += len(rows)
+    secs = sum(ev)
+    out = {
+        "metric": METRIC, "value": masked_total / secs, "unit": UNIT, "n_gpus": world, "steps": iters,
+        "warmup": 0, "ms_per_step": secs * 1e3 / iters, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS["blockserve"], "requests": lcfg.R, "prompt_len": [lcfg.p_lo, lcfg.p_hi],
+                   "gen": lcfg.gen, "L": L, "V": V, "token_budget": lcfg.budget, "threshold": lcfg.threshold,
+                   "mode": "fdfo", "timed": "admit+refill+pack+step+done readback+advance+compact per iteration"},
+        "loop": {"iterations": iters, "timed_s": secs, "masked_positions": masked_total,
+                 "logits_gbs": masked_total * V * 2 / secs / 1e9,
+                 "step_call_ms_total": sum(step_ms), "step_call_share": sum(step_ms) / 1e3 / secs},
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -529,6 +614,8 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dream",
+                    help="dream (default, the headline), llada, stress, tiny, or the blockserve loop")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -539,6 +626,9 @@ def main():
             return 0
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return 0
+
+    if args.workload == "blockserve":
+        return run_loop_bench(args, rank, world, local_rank)
 
     dist = None
     if world > 1:
@@ -566,7 +656,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": res["seconds"] * 1e3 / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": cfg.B, "L": cfg.L, "V": cfg.V, "masked_rows": pipe.M,
+            "config": {"workload": WORKLOADS[args.workload], "B": cfg.B, "L": cfg.L, "V": cfg.V, "masked_rows": pipe.M,
                        "thresholds": "per request from {0.5,0.6,0.7,0.8,0.9}", "mask_fraction": "U[0,1] per request",
                        "box_W": pipe.W, "box_cost": pipe.cost, "token_budget": BUDGET,
                        "step": "admit(host)+pack+step+advance+compact",

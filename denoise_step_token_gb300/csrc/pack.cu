@@ -155,37 +155,49 @@ struct CompactParams {
     long long row_bytes[DLLM_COMPACT_MAX_ARRAYS];
 };
 
-// Copy `rows` rows of one array, all rows in flight at once: thread t of
-// nt handles 32-bit words (or bytes, when a row is not word-sized or the
-// pointers are not word-aligned) t, t + nt, ... of the flattened rows.
-// dst_row(r) < 0 skips row r.
-template <typename DstRow>
-__device__ __forceinline__ void copy_rows(unsigned char* dst, const unsigned char* src, long long rb, int rows,
-                                          DstRow dst_row, long long src_row0, int t, int nt) {
-    const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src);
-    if ((rb & 3) == 0 && (al & 3) == 0) {
-        const long long wpr = rb >> 2;
-        const long long total = wpr * rows;
-        for (long long k = t; k < total; k += nt) {
-            const int r = (int)(k / wpr);
-            const long long w = k - (long long)r * wpr;
-            const int d = dst_row(r);
-            if (d < 0) continue;
-            reinterpret_cast<uint32_t*>(dst)[(long long)d * wpr + w] =
-                reinterpret_cast<const uint32_t*>(src)[(src_row0 + r) * wpr + w];
+// Copy `rows` rows of one array.  Thread t of nt handles 32-bit words (or
+// bytes, when a row is not word-sized or the pointers are not word-aligned)
+// t, t + nt, ... of the flattened rows, four loads in flight before their
+// stores.  dst_row(r) < 0 skips row r.
+template <typename T, typename DstRow>
+__device__ __forceinline__ void copy_rows_t(T* __restrict__ dst, const T* __restrict__ src, int per_row, int rows,
+                                            DstRow dst_row, int src_row0, int t, int nt) {
+    const int total = per_row * rows;
+    for (int k0 = t; k0 < total; k0 += 4 * nt) {
+        T v[4];
+        int d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u * nt;
+            d[u] = -1;
+            if (k < total) {
+                const int r = k / per_row;
+                const int w = k - r * per_row;
+                const int dr = dst_row(r);
+                if (dr >= 0) {
+                    d[u] = dr * per_row + w;
+                    v[u] = src[(src_row0 + r) * per_row + w];
+                }
+            }
         }
-    } else {
-        const long long total = rb * rows;
-        for (long long k = t; k < total; k += nt) {
-            const int r = (int)(k / rb);
-            const long long w = k - (long long)r * rb;
-            const int d = dst_row(r);
-            if (d < 0) continue;
-            dst[(long long)d * rb + w] = src[(src_row0 + r) * rb + w];
-        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (d[u] >= 0) dst[d[u]] = v[u];
     }
 }
 
+template <typename DstRow>
+__device__ __forceinline__ void copy_rows(unsigned char* dst, const unsigned char* src, long long rb, int rows,
+                                          DstRow dst_row, int src_row0, int t, int nt) {
+    const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src);
+    if ((rb & 3) == 0 && (al & 3) == 0)
+        copy_rows_t(reinterpret_cast<uint32_t*>(dst), reinterpret_cast<const uint32_t*>(src), (int)(rb >> 2), rows,
+                    dst_row, src_row0, t, nt);
+    else
+        copy_rows_t(dst, src, (int)rb, rows, dst_row, src_row0, t, nt);
+}
+
+// grid: (row tiles of kCompactRows, arrays); CTA (x, 0) also writes the maps
 __global__ void __launch_bounds__(kCompactRows) compact_scatter_kernel(const __grid_constant__ CompactParams P) {
     __shared__ int s_warp[kCompactRows / 32];
     __shared__ int s_before;
@@ -216,26 +228,31 @@ __global__ void __launch_bounds__(kCompactRows) compact_scatter_kernel(const __g
         total += s_warp[w];
     }
     const int ni = keep ? s_before + wbefore + __popc(bal & ((1u << lane) - 1u)) : -1;
-    if (i < P.A) {
-        if (P.new_index) P.new_index[i] = ni;
-        if (keep && P.src_row) P.src_row[ni] = i;
+    if (blockIdx.y == 0) {
+        if (i < P.A) {
+            if (P.new_index) P.new_index[i] = ni;
+            if (keep && P.src_row) P.src_row[ni] = i;
+        }
+        if (i0 + kCompactRows >= P.A && t == 0) *P.A_out = s_before + total;   // last row tile
     }
     s_new[t] = ni;
-    if (i0 + kCompactRows >= P.A && t == 0) *P.A_out = s_before + total;   // last CTA
     __syncthreads();
-    // scatter every kept row of every array into its staging copy
-    const int rows = min(kCompactRows, P.A - i0);
-    for (int a = 0; a < P.n_arrays; ++a)
+    // scatter the kept rows of array blockIdx.y into its staging copy
+    const int a = blockIdx.y;
+    if (a < P.n_arrays) {
+        const int rows = min(kCompactRows, P.A - i0);
         copy_rows(P.stage[a], P.arrays[a], P.row_bytes[a], rows, [&](int r) { return s_new[r]; }, i0, t,
                   kCompactRows);
+    }
 }
 
+// grid: (row-word blocks, arrays)
 __global__ void __launch_bounds__(256) compact_copyback_kernel(const __grid_constant__ CompactParams P) {
     const int n = *P.A_out;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const int nt = gridDim.x * blockDim.x;
-    for (int a = 0; a < P.n_arrays; ++a)
-        copy_rows(P.arrays[a], P.stage[a], P.row_bytes[a], n, [](int r) { return r; }, 0, t, nt);
+    const int a = blockIdx.y;
+    copy_rows(P.arrays[a], P.stage[a], P.row_bytes[a], n, [](int r) { return r; }, 0, t, nt);
 }
 
 // ---------------------------------------------------------------------------
@@ -444,15 +461,18 @@ extern "C" int dllm_compact(const dllm_compact_args* a, void* stream) {
             off += (size_t(a->A) * size_t(a->row_bytes[k]) + 255) & ~size_t(255);
         }
     }
-    const int blocks = (a->A + kCompactRows - 1) / kCompactRows;
-    compact_scatter_kernel<<<blocks, kCompactRows, 0, s>>>(P);
+    for (int k = 0; k < a->n_arrays; ++k)
+        if ((long long)a->A * a->row_bytes[k] > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
+    const dim3 grid((a->A + kCompactRows - 1) / kCompactRows, std::max(a->n_arrays, 1));
+    compact_scatter_kernel<<<grid, kCompactRows, 0, s>>>(P);
     DLLM_CUDA_TRY(cudaGetLastError());
     if (a->n_arrays > 0) {
         long long words = 0;
-        for (int k = 0; k < a->n_arrays; ++k) words += (long long)a->A * ((a->row_bytes[k] + 3) / 4);
+        for (int k = 0; k < a->n_arrays; ++k)
+            words = std::max(words, (long long)a->A * ((a->row_bytes[k] + 3) / 4));
         const int sms = std::max(sm_count(), 1);
-        const int cb = (int)std::max(1LL, std::min((words + 255) / 256, (long long)sms * 4));
-        compact_copyback_kernel<<<cb, 256, 0, s>>>(P);
+        const int cbx = (int)std::max(1LL, std::min((words + 1023) / 1024, (long long)sms));
+        compact_copyback_kernel<<<dim3(cbx, a->n_arrays), 256, 0, s>>>(P);
         DLLM_CUDA_TRY(cudaGetLastError());
     }
     return DLLM_OK;

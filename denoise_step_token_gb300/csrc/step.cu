@@ -797,10 +797,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             ++issued;
             ++p_q;
         };
-        // lane 1's last row-counter add, tested one group later so that its
-        // round trip overlaps the next group's work
-        int pend_old = -1, pend_k = 0, pend_row = 0;
-        auto flush_pending = [&]() {
+        // Publishing a group: lane 1 stores its partials at once, but adds
+        // to the row counter (a release, which waits for those stores) only
+        // at the end of the next group, before that group's stores; the add's
+        // result is tested one group later still.  Neither wait stalls the
+        // warp on fresh stores.
+        int add_row = -1, add_k = 0;         // partials stored, add not yet issued
+        int pend_old = -1, pend_k = 0, pend_row = 0;   // add issued, result not yet tested
+        auto test_pending = [&]() {
             if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC) {
                 // that group completed the row: acquire the other groups'
                 // partials, then hand the row to the finishers
@@ -808,6 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], pend_row + 1);
             }
             pend_old = -1;
+        };
+        auto issue_add = [&]() {
+            if (lane == 1 && add_row >= 0) {
+                pend_old = atom_add_release_gpu(P.cnt + add_row, add_k);
+                pend_k = add_k;
+                pend_row = add_row;
+            }
+            add_row = -1;
         };
 
 #pragma unroll 1
@@ -886,7 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             for (int j = 0; j < kGroup; ++j)
                 first[j] = __reduce_min_sync(0xffffffffu, (lm[j] == gm[j]) ? (unsigned)gi[j] : (unsigned)kBatchesPerChunk);
             // publish the group's partials (lane 1: lane 0 owns the bulk copies)
-            flush_pending();
+            test_pending();
+            issue_add();
             if (lane == 1) {
 #pragma unroll
                 for (int j = 0; j < kGroup; ++j) {
@@ -899,12 +912,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                         *reinterpret_cast<float4*>(P.part + (long long)row * NC + c0 + j) = rec;
                     }
                 }
-                pend_old = atom_add_release_gpu(P.cnt + row, k);
-                pend_k = k;
-                pend_row = row;
+                add_row = row;
+                add_k = k;
             }
         }
-        flush_pending();
+        test_pending();
+        issue_add();
+        test_pending();
         if (failed) {
             if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
             // let this warp's copies in flight land before shared memory goes away
