@@ -509,3 +509,24 @@ def test_loop_bs1_fdfo_equals_sync():
     s, _ = _small_loop("sync", R=1)
     assert np.array_equal(f.gen[0], s.gen[0])
     assert f.iteration == s.iteration
+
+
+def test_advance_hand_case():
+    # BlockServe Algorithm 1: a committed block is appended to the request's
+    # output, b_i grows by one, and the request is evicted once b_i >= K_i;
+    # a continuing request starts its next block fully masked.
+    from oracle.loop import advance
+    mask = 9
+    adv = np.array([1, 0, 1], dtype=bool)
+    rid = [5, 6, 7]
+    b = np.array([0, 1, 1])
+    K = np.array([2, 3, 2])
+    ids = np.array([[1, 2], [mask, 3], [4, 5]])
+    cs = np.array([[0.9, 0.8], [np.nan, 0.7], [0.6, 0.95]])
+    gen = {5: np.zeros(0, dtype=np.int64), 6: np.array([7, 7]), 7: np.array([8, 8])}
+    evict = advance(adv, rid, b, K, ids, cs, gen, mask)
+    assert evict.tolist() == [False, False, True]
+    assert b.tolist() == [1, 1, 2]
+    assert gen[5].tolist() == [1, 2] and gen[6].tolist() == [7, 7] and gen[7].tolist() == [8, 8, 4, 5]
+    assert ids[0].tolist() == [mask, mask] and np.isnan(cs[0]).all()      # next block starts masked
+    assert ids[1].tolist() == [mask, 3] and ids[2].tolist() == [4, 5]     # untouched / evicted as is
