@@ -10,24 +10,29 @@
 //
 // Kernel design (GB300: 152 SMs, one CTA per SM, warp-specialised):
 //   S1  every CTA scans input_ids once into shared bitmasks, ranks the masked
-//       rows and takes an equal share of the masked-row element stream.
-//   S2  work unit = one fixed 4096-element chunk of one masked row.  Each
-//       streaming warp takes chunks from the CTA's pool (a shared counter)
-//       and runs its own ring of bulk copies (cp.async.bulk, the TMA engine,
-//       L2 evict-first) into shared memory; being the only reader of its
-//       ring, it sees every barrier phase in order.  Each lane folds its
-//       elements into an online (max, sum of exp, first argmax) with a packed
+//       rows and takes an equal share of the element stream of all but the
+//       last min(M/4, 1024) masked rows; those (the tail) are shared by all
+//       CTAs.
+//   S2  work unit = one fixed 8192-element chunk of one masked row.  Each
+//       streaming warp takes chunks from the CTA's pool (a shared counter),
+//       then from the shared tail (tickets on a global counter), and runs
+//       its own ring of bulk copies (cp.async.bulk, the TMA engine, L2
+//       evict-first) into shared memory; being the only reader of its ring,
+//       it sees every barrier phase in order.  Each lane folds its elements
+//       into an online (max, sum of exp, first argmax batch) with a packed
 //       bf16x2 max and one FFMA + MUFU.EX2 + FADD per element; the warp then
-//       publishes the chunk partial with an acquire-release add on the row's
-//       counter.
-//   Rows: the chunk that completes a row queues it for the CTA's finisher
-//       warps, which fold the row's partials in a fixed order, write
-//       conf = 1/s, lse = m + ln s and the argmax token, and count the row
-//       towards its request; the request's last row runs S3-S6 for it
-//       (selection, fallback, update, done, quantile features by rank).
+//       writes each chunk partial as one 64-bit word and counts the chunks
+//       on the row's counter, both relaxed (no fence on the streaming path).
+//   Rows: the add that completes a row queues it for the CTA's finisher
+//       warps, which read the row's partial words (polling any still in
+//       flight), fold them in a fixed order, write conf = 1/s,
+//       lse = m + ln s and the argmax token, and count the row towards its
+//       request; the request's last row runs S3-S6 for it (selection,
+//       fallback, update, done, quantile features by rank).
 // The chunk split, lane mapping and fold order depend only on V, so a
 // request's results are bit-identical whatever else is in the batch.  No
-// CTA waits for another: counters only elect the last arriver.  input_ids is
+// CTA waits for another to make progress: counters elect the last arriver,
+// and a finisher waits only for stores already issued to land.  input_ids is
 // written only after every CTA has finished scanning it (otherwise the
 // grid's last CTA to exit writes it), so a CTA that starts late still sees
 // the entry state.  Every wait inside a CTA is bounded in time.
@@ -44,13 +49,13 @@ namespace {
 
 // Pipeline shape (tunable at build time; the defaults are the measured best).
 #ifndef DLLM_STEP_WARPS
-#define DLLM_STEP_WARPS 20
+#define DLLM_STEP_WARPS 16
 #endif
 #ifndef DLLM_STEP_FINISHERS
 #define DLLM_STEP_FINISHERS 2
 #endif
 #ifndef DLLM_STEP_STAGES
-#define DLLM_STEP_STAGES 2
+#define DLLM_STEP_STAGES 3
 #endif
 #ifndef DLLM_STEP_COPY_ELEMS
 #define DLLM_STEP_COPY_ELEMS 2048
@@ -60,6 +65,9 @@ namespace {
 #endif
 #ifndef DLLM_STEP_GROUP
 #define DLLM_STEP_GROUP 2
+#endif
+#ifndef DLLM_STEP_TAIL_DEN
+#define DLLM_STEP_TAIL_DEN 4
 #endif
 
 constexpr int kStreamWarps = DLLM_STEP_WARPS;         // warps streaming logits
@@ -72,6 +80,8 @@ constexpr int kCopyElems = DLLM_STEP_COPY_ELEMS;      // one bulk copy
 constexpr int kCopyBytes = kCopyElems * 2;
 constexpr int kChunkElems = DLLM_STEP_CHUNK_ELEMS;    // fixed reduction chunk of a row
 constexpr int kGroup = DLLM_STEP_GROUP;               // chunks of one row taken at once
+constexpr int kTailDen = DLLM_STEP_TAIL_DEN;          // up to 1/kTailDen of the masked rows ...
+constexpr int kTailRowsMax = 1024;                    // ... and at most this many are shared by all CTAs
 constexpr int kBatchVecs = 8;                         // 16-byte vectors per lane per batch
 constexpr int kBatchElems = kBatchVecs * 8 * 32;      // 2048 contiguous elements
 constexpr int kBatchesPerCopy = kCopyElems / kBatchElems;
@@ -82,16 +92,54 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s for any single wait
 static_assert(kCopyElems % kBatchElems == 0, "a copy holds whole batches");
 static_assert(kChunkElems % kCopyElems == 0, "a chunk holds whole copies");
 static_assert(kStages >= 1 && kStages <= 8, "pipeline depth");
+static_assert(kTailDen >= 1 && kTailDen <= 64, "tail share");
 
-struct Partial {
-    float m;    // chunk max
-    float s;    // sum of exp(x - m) over the chunk
-    int kb;     // first batch of the chunk holding m
-    int pad;
-};
+// A chunk partial in one 64-bit word, written with a single relaxed store:
+// low half = the chunk max m (a bf16 value, so the low 16 bits of its fp32
+// pattern are zero) with (first batch holding m) + 1 in those 16 bits; high
+// half = sum of exp(x - m) over the chunk.  A zero word is "not yet written":
+// partial words are zero at rest and the row finisher clears them.
+__device__ __forceinline__ unsigned long long pack_partial(float m, float s, int kb) {
+    const uint32_t lo = (__float_as_uint(m) & 0xffff0000u) | (uint32_t)(kb + 1);
+    return ((unsigned long long)__float_as_uint(s) << 32) | lo;
+}
+__device__ __forceinline__ void unpack_partial(unsigned long long w, float& m, float& s, int& kb) {
+    const uint32_t lo = (uint32_t)w;
+    m = __uint_as_float(lo & 0xffff0000u);
+    kb = (int)(lo & 0xffffu) - 1;
+    s = __uint_as_float((uint32_t)(w >> 32));
+}
+
+// A finished row in one 64-bit word: low half = conf, high half = the
+// argmax token with the top bit set (so the word is never zero); token
+// 0x7fffffff stands for "none found" (-1).
+__device__ __forceinline__ unsigned long long pack_row(float conf, int tok) {
+    const uint32_t hi = 0x80000000u | ((uint32_t)tok & 0x7fffffffu);
+    return ((unsigned long long)hi << 32) | __float_as_uint(conf);
+}
+__device__ __forceinline__ void unpack_row(unsigned long long w, float& conf, int& tok) {
+    conf = __uint_as_float((uint32_t)w);
+    const int t = (int)((uint32_t)(w >> 32) & 0x7fffffffu);
+    tok = (t == 0x7fffffff) ? -1 : t;
+}
+
+// Poll a zero-at-rest word until its (already issued) store lands; bounded.
+__device__ __noinline__ unsigned long long poll_word(const unsigned long long* p, int* err) {
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    unsigned long long w;
+    while ((w = ld_relaxed_gpu_u64(p)) == 0ull) {
+        __nanosleep(32);
+        if ((++spins & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_error(err, DLLM_DEVERR_TIMEOUT);
+            break;
+        }
+    }
+    return w;
+}
 
 struct StepParams {
-    int B, L, V, NC, BL, mask_id, list_cap, zero_cap;
+    int B, L, V, NC, BL, mask_id, list_cap, static_cap, zero_cap;
     long long ldv;
     const uint16_t* logits;
     int* ids;
@@ -104,22 +152,24 @@ struct StepParams {
     float* conf_out;
     float* lse_out;
     int* tok_out;
-    int* ctl;        // [0] CTAs done scanning, [1] CTAs exited
-    int* cnt;        // [BL] row counters, [B] request counters, [B] committed flags
-    Partial* part;   // [BL * NC]
-    float* row_conf;
-    float* row_lse;
+    int* ctl;        // [0] CTAs done scanning, [1] CTAs exited (low 16 bits) and deferred
+                     // commits (high bits), [2] tail tickets drawn
+    int* cnt;        // [BL] row counters, [B] request counters, [B] deferred-commit list
+    unsigned long long* part;   // [BL * NC] packed chunk partials, zero at rest
+    unsigned long long* row_word;   // [BL] a finished row's conf and token, zero at rest
     int* row_tok;
     uint8_t* sel;
     int* err;
 };
 
 // Workspace layout.  The first quarter holds everything that must be zero
-// between calls (control words and counters); per-call data sits at the end,
-// so calls of different shapes never put data on each other's counters.
+// between calls (control words, counters, chunk partials); per-call data
+// sits at the end, so calls of different shapes never put data on each
+// other's zero-at-rest words.
 struct WsLayout {
     size_t front, counters_bytes, data_bytes;
-    size_t off_part, off_conf, off_lse, off_tok, off_sel;
+    size_t off_part, off_row;   // from the workspace start, inside the front quarter
+    size_t off_tok, off_sel;    // from the data start
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -127,11 +177,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool ws_layout(long long B, long long L, long long V, size_t bytes, WsLayout* w) {
     const long long BL = B * L;
     const long long NC = (V + kChunkElems - 1) / kChunkElems;
-    w->counters_bytes = 64 + 4 * size_t(BL + 2 * B);
+    w->off_part = align256(64 + 4 * size_t(BL + 2 * B));
+    w->off_row = align256(w->off_part + size_t(BL * NC) * 8);
+    w->counters_bytes = w->off_row + size_t(BL) * 8;
     size_t d = 0;
-    w->off_part = d; d = align256(d + size_t(BL * NC) * sizeof(Partial));
-    w->off_conf = d; d = align256(d + size_t(BL) * 4);
-    w->off_lse = d;  d = align256(d + size_t(BL) * 4);
     w->off_tok = d;  d = align256(d + size_t(BL) * 4);
     w->off_sel = d;  d = align256(d + size_t(BL));
     w->data_bytes = d;
@@ -333,8 +382,8 @@ __device__ __forceinline__ void warp_features(const float (&val)[NK], const bool
 // ---------------------------------------------------------------------------
 template <int NK>
 __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool has_masked, int lane) {
-    // The caller's acquire (the request counter, or the launch itself for
-    // requests without masked rows) makes every row result of b visible.
+    // Row results arrive as zero-at-rest words (polled until they land);
+    // requests without masked rows read only the launch's inputs.
     const int L = P.L;
     const long long base = (long long)b * L;
     const float t = P.thr[b];
@@ -342,6 +391,7 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
 
     int id[NK], tk[NK];
     float c[NK], cs_old[NK];
+    unsigned long long rw[NK];
     bool msk[NK];
     bool any_masked = false, any_pass = false;
     float best_c = -INFINITY;
@@ -353,14 +403,18 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
         const bool valid = j < L;
         id[k] = valid ? P.ids[base + j] : 0;
         cs_old[k] = valid ? P.cs[base + j] : 0.f;
-        c[k] = (valid && has_masked) ? __ldcg(P.row_conf + base + j) : 0.f;
-        tk[k] = (valid && has_masked) ? __ldcg(P.row_tok + base + j) : -1;
+        rw[k] = (valid && has_masked) ? ld_relaxed_gpu_u64(P.row_word + base + j) : 0ull;
     }
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
         msk[k] = j < L && id[k] == P.mask_id;
+        c[k] = 0.f;
+        tk[k] = -1;
         if (msk[k]) {
+            if (rw[k] == 0ull) rw[k] = poll_word(P.row_word + base + j, P.err);
+            P.row_word[base + j] = 0ull;
+            unpack_row(rw[k], c[k], tk[k]);
             any_masked = true;
             if (c[k] > t) any_pass = true;
             // j grows with k, so a strict > keeps the lowest position on ties
@@ -431,19 +485,19 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     }
     if (P.feats) warp_features<NK>(val, inU, L, lane, P.feats + (long long)b * DLLM_NUM_FEATURES);
 
-    // S4 commit of input_ids: only once every CTA has finished its scan.
-    int* committed = P.cnt + P.BL + P.B;
-    if (!has_masked) {
-        if (lane == 0) committed[b] = 1;
-        return;
-    }
+    // S4 commit of input_ids: only once every CTA has finished its scan;
+    // before that the request goes on the deferred list, which the grid's
+    // last CTA commits (the add's high half counts the list's entries).
+    if (!has_masked) return;
     __syncwarp();   // lane 0's acquire of the scan count orders the warp's writes
     if (__shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
 #pragma unroll
         for (int k = 0; k < NK; ++k) {
             if (selk[k]) P.ids[base + lane + 32 * k] = id[k];
         }
-        if (lane == 0) committed[b] = 1;
+    } else if (lane == 0) {
+        const int slot = (int)((unsigned)atomicAdd(P.ctl + 1, 1 << 16) >> 16);
+        P.cnt[P.BL + P.B + slot] = b;
     }
     if (lane == 0) P.cnt[P.BL + b] = 0;   // request counter back to rest
 }
@@ -461,10 +515,10 @@ __device__ __forceinline__ void finalize_request(const StepParams& P, int b, boo
 // row results, then count the row towards its request.
 // ---------------------------------------------------------------------------
 __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_gmask, int row, int lane) {
-    // Visibility of every chunk partial of the row comes from the acquire
-    // chain: each chunk group's release-add on the row counter, the
-    // completing lane's fence after its add, its release store into the CTA
-    // queue and the finisher's acquire load of that entry.
+    // Every chunk of the row has been counted, but the words holding the
+    // partials are written with relaxed stores: a word still reading zero
+    // is polled (bounded in time) until its store lands.  Each word is
+    // cleared once read, ready for the next call.
     const int NC = P.NC;
     const int b = row / P.L;
     // masked rows of this request at entry, from this CTA's scan bitmask
@@ -485,10 +539,16 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     float M = -INFINITY, S = 0.f;
     long long key = 0x7fffffffffffffffLL;   // chunk * batches + batch of the first maximum
     for (int c = lane; c < NC; c += 32) {
-        const float4 raw = __ldcg(reinterpret_cast<const float4*>(P.part + (long long)row * NC + c));
-        const long long kc = (long long)c * kBatchesPerChunk + min(__float_as_int(raw.z), kBatchesPerChunk - 1);
-        if (raw.x > M) key = kc;
-        combine(M, S, raw.x, raw.y);
+        unsigned long long* wp = P.part + (long long)row * NC + c;
+        unsigned long long w = ld_relaxed_gpu_u64(wp);
+        if (w == 0ull) w = poll_word(wp, P.err);
+        *wp = 0ull;
+        float pm, ps;
+        int pk;
+        unpack_partial(w, pm, ps, pk);
+        const long long kc = (long long)c * kBatchesPerChunk + min(max(pk, 0), kBatchesPerChunk - 1);
+        if (pm > M) key = kc;
+        combine(M, S, pm, ps);
     }
 #pragma unroll
     for (int off = 16; off; off >>= 1) {
@@ -523,20 +583,20 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     best = __reduce_min_sync(0xffffffffu, best);
     const float conf = __fdiv_rn(1.0f, S);
     const float lse = M + logf(S);
+    // the row's word and its count on the request are both relaxed: the
+    // request's finalizer polls for words still in flight
     int old = 0;
     if (lane == 0) {
-        P.row_conf[row] = conf;
-        P.row_lse[row] = lse;
         P.row_tok[row] = (int)best;
         if (P.conf_out) P.conf_out[row] = conf;
         if (P.lse_out) P.lse_out[row] = lse;
         if (P.tok_out) P.tok_out[row] = (int)best;
         P.cnt[row] = 0;
-        old = atom_add_acqrel_gpu(P.cnt + P.BL + b, 1);
+        st_relaxed_gpu_u64(P.row_word + row, pack_row(conf, (int)best));
+        old = atom_add_relaxed_gpu(P.cnt + P.BL + b, 1);
     }
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old == mb - 1) {
-        __syncwarp();   // lane 0's acquire-release add orders the whole warp's reads
         finalize_request(P, b, true, lane);
     }
 }
@@ -651,37 +711,47 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     const int before = wbase + incl - cnt;
     const int NC = P.NC;
-    const long long V = P.V;
-    const long long U = (long long)M * NC;
-    // CTA k's share of the masked-row element stream starts at element
-    // floor(M * V * k / G) = V * a + e with a = floor(M k / G) and
-    // e = floor(V * (M k mod G) / G) < V: row a, element e of that row.  Its
-    // first unit is the first chunk starting there or later.  Only 32-bit
-    // divisions (M * G and V * G fit in 32 bits, checked on the host).
-    auto first_unit = [&](int k) -> long long {
-        if (k >= G) return U;
-        const int mk = M * k;
-        int r = mk / G;
-        const int e = (int)(((long long)V * (mk - r * G)) / G);
+    const int V = P.V;
+    const int U = M * NC;   // units fit in 32 bits (checked on the host)
+    // The last T = min(ceil(M / kTailDen), kTailRowsMax) masked rows (the
+    // tail) are taken one chunk at a time by any warp whose CTA has run out,
+    // so that CTAs the memory system serves more slowly do not hold up the
+    // end of the step; the rows before them are split evenly over the CTAs.
+    // With Ms = M - T, CTA k's share starts at element floor(Ms V k / G) =
+    // V a + e with a = floor(Ms k / G) and e = floor(V (Ms k mod G) / G) < V:
+    // row a, element e of that row.  Its first unit is the first chunk
+    // starting there or later; k = G gives the tail's first unit Ms * NC.
+    // Only 32-bit divisions (M G and V G fit in 32 bits, checked on the host).
+    const int T = min((M + kTailDen - 1) / kTailDen, kTailRowsMax);
+    const int Ms = M - T;
+    auto first_unit = [&](int k) -> int {
+        const unsigned mk = (unsigned)Ms * k;
+        int r = (int)(mk / (unsigned)G);
+        const int e = (int)(((unsigned)V * (mk - (unsigned)r * G)) / (unsigned)G);
         int cc = (e + kChunkElems - 1) / kChunkElems;
         if (cc >= NC) {
             r += 1;
             cc = 0;
         }
-        return (long long)r * NC + cc;
+        return r * NC + cc;
     };
-    const long long u0 = first_unit(cta);
-    const long long u1 = first_unit(cta + 1);
-    const int r_lo32i = (int)u0 / NC;   // units fit in 32 bits (checked on the host)
-    const long long r_lo = r_lo32i;
-    const long long r_hi = (u1 > u0) ? (long long)((int)(u1 - 1) / NC) : r_lo - 1;
+    const int u0 = first_unit(cta);
+    const int u1 = first_unit(cta + 1);
+    const int u_tail = Ms * NC;
+    const int n_tail = U - u_tail;
+    const int r_lo = u0 / NC;
+    const int r_hi = (u1 > u0) ? (u1 - 1) / NC : r_lo - 1;
+    const int r_tail = Ms;   // first row of the tail
+    const int r_last = (n_tail > 0) ? M - 1 : r_hi;
+    const int static_cap = P.static_cap;
     int rank = before;
-    for (int g = g0; g < g1 && rank <= r_hi; ++g) {
+    for (int g = g0; g < g1 && rank <= r_last; ++g) {
         unsigned bits = s_gmask[g];
         while (bits) {
             const int i = __ffs(bits) - 1;
             bits &= bits - 1;
             if (rank >= r_lo && rank <= r_hi) s_list[rank - r_lo] = (g << 4) + i;
+            if (rank >= r_tail) s_list[static_cap + rank - r_tail] = (g << 4) + i;
             ++rank;
         }
     }
@@ -700,10 +770,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     __syncthreads();
 
-    const int n_units = (int)(u1 - u0);   // this CTA's chunks: unit k is chunk u0 + k
-    const int u_first = (int)u0;          // M * NC < 2^31 (checked on the host)
-    const int r_lo32 = (int)r_lo;
+    const int n_units = u1 - u0;   // this CTA's chunks: unit k is chunk u0 + k
+    const int u_first = u0;
     const int V32 = P.V;
+    // masked position of unit gu's row (units of the tail have their own slots)
+    auto row_of = [&](int gu) -> int {
+        const int rr = gu / NC;
+        return (gu >= u_tail) ? s_list[static_cap + rr - r_tail] : s_list[rr - r_lo];
+    };
 
     if (warp < kStreamWarps) {
         // ---- S2: stream groups of chunks through this warp's ring ----------
@@ -719,6 +793,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const int tail_units = 2 * kStreamWarps;   // single-chunk grabs below this many left
 
         // Take the next group: returns its first unit (or -1) and its size.
+        // Once the CTA's pool is spent, units come one at a time from the
+        // shared tail through tickets on ctl[2]; lane 0 draws each ticket
+        // one grab ahead of its use, so the atomic's latency stays hidden.
+        int t_ahead = -1;   // lane 0: ticket drawn ahead of use
+        const int ahead_margin = G * kStreamWarps;
         auto grab = [&](int& k) -> int {
             int got = -1, kk = 0;
             if (lane == 0) {
@@ -731,11 +810,25 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     want = min(want, min(row_end - cur, left));
                     const int old = atomicCAS(&s_next, cur, cur + want);
                     if (old == cur) {
-                        got = cur;
+                        got = gu;
                         kk = want;
+                        if (n_tail > 0 && t_ahead < 0 && left - want <= tail_units)
+                            t_ahead = atomicAdd(P.ctl + 2, 1);
                         break;
                     }
                     cur = old;
+                }
+                if (got < 0 && n_tail > 0) {
+                    const int t = (t_ahead >= 0) ? t_ahead : atomicAdd(P.ctl + 2, 1);
+                    t_ahead = -1;
+                    if (t < n_tail) {
+                        got = u_tail + t;
+                        kk = 1;
+                        // draw ahead only while every warp can still get a
+                        // ticket: near the end a ticket held ahead would be
+                        // extra work for one warp while others idle
+                        if (t + ahead_margin < n_tail) t_ahead = atomicAdd(P.ctl + 2, 1);
+                    }
                 }
             }
             k = __shfl_sync(0xffffffffu, kk, 0);
@@ -752,12 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         uint32_t issued = 0, consumed = 0;
         bool failed = false;
 
-        auto start_chunk = [&](int u) {
-            const int gu = u_first + u;
-            const int rr = gu / NC;
-            const int c = gu - rr * NC;
-            const int row = s_list[rr - r_lo32];
-            p_unit = u;
+        auto start_chunk = [&](int gu) {
+            const int c = gu - (gu / NC) * NC;
+            const int row = row_of(gu);
+            p_unit = gu;
             p_q = 0;
             p_len = min(kChunkElems, V32 - c * kChunkElems);
             p_src = (long long)row * P.ldv + (long long)c * kChunkElems;
@@ -797,29 +888,17 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             ++issued;
             ++p_q;
         };
-        // Publishing a group: lane 1 stores its partials at once, but adds
-        // to the row counter (a release, which waits for those stores) only
-        // at the end of the next group, before that group's stores; the add's
-        // result is tested one group later still.  Neither wait stalls the
-        // warp on fresh stores.
-        int add_row = -1, add_k = 0;         // partials stored, add not yet issued
+        // Publishing a group: lane 1 writes each chunk's partial word with a
+        // relaxed store and adds the group's chunk count to the row counter
+        // with a relaxed add (no fence: a release here would wait for this
+        // warp's memory traffic).  The add's result is tested one group
+        // later; the add that brings the counter to NC queues the row for
+        // the finishers, who poll for the words still in flight.
         int pend_old = -1, pend_k = 0, pend_row = 0;   // add issued, result not yet tested
         auto test_pending = [&]() {
-            if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC) {
-                // that group completed the row: acquire the other groups'
-                // partials, then hand the row to the finishers
-                fence_acq_rel_gpu();
+            if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC)
                 st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], pend_row + 1);
-            }
             pend_old = -1;
-        };
-        auto issue_add = [&]() {
-            if (lane == 1 && add_row >= 0) {
-                pend_old = atom_add_release_gpu(P.cnt + add_row, add_k);
-                pend_k = add_k;
-                pend_row = add_row;
-            }
-            add_row = -1;
         };
 
 #pragma unroll 1
@@ -827,17 +906,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
 #pragma unroll 1
         while (consumed < issued && !failed) {
-            const int u = fifo_u[0], k = fifo_k[0];
+            const int gu = fifo_u[0], k = fifo_k[0];
 #pragma unroll
             for (int i = 0; i < kStages; ++i) {
                 fifo_u[i] = fifo_u[i + 1];
                 fifo_k[i] = fifo_k[i + 1];
             }
             --nfifo;
-            const int gu = u_first + u;
-            const int rr = gu / NC;
-            const int c0 = gu - rr * NC;
-            const int row = s_list[rr - r_lo32];
+            const int c0 = gu - (gu / NC) * NC;
+            const int row = row_of(gu);
             float gm[kGroup], gs[kGroup];
             int gi[kGroup];
 #pragma unroll
@@ -899,25 +976,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 first[j] = __reduce_min_sync(0xffffffffu, (lm[j] == gm[j]) ? (unsigned)gi[j] : (unsigned)kBatchesPerChunk);
             // publish the group's partials (lane 1: lane 0 owns the bulk copies)
             test_pending();
-            issue_add();
             if (lane == 1) {
 #pragma unroll
                 for (int j = 0; j < kGroup; ++j) {
-                    if (j < k) {
-                        float4 rec;
-                        rec.x = gm[j];
-                        rec.y = gs[j];
-                        rec.z = __int_as_float((int)first[j]);
-                        rec.w = 0.f;
-                        *reinterpret_cast<float4*>(P.part + (long long)row * NC + c0 + j) = rec;
-                    }
+                    if (j < k)
+                        st_relaxed_gpu_u64(P.part + (long long)row * NC + c0 + j,
+                                           pack_partial(gm[j], gs[j], (int)first[j]));
                 }
-                add_row = row;
-                add_k = k;
+                pend_old = atom_add_relaxed_gpu(P.cnt + row, k);
+                pend_k = k;
+                pend_row = row;
             }
         }
-        test_pending();
-        issue_add();
         test_pending();
         if (failed) {
             if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
@@ -947,25 +1017,24 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // ---- exit: the last CTA commits deferred requests and resets ----------
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
-        s_last = (atomicAdd(P.ctl + 1, 1) == G - 1);
+        const unsigned old = (unsigned)atom_add_acqrel_gpu(P.ctl + 1, 1);
+        s_last = ((int)(old & 0xffffu) == G - 1) ? 1 + (int)(old >> 16) : 0;   // 1 + deferred commits
     }
     __syncthreads();
     if (s_last) {
-        __threadfence();
-        int* committed = P.cnt + P.BL + P.B;
-        for (int b = tid; b < P.B; b += kThreads) {
-            if (__ldcg(committed + b) == 0) {   // its finisher ran before every CTA had scanned
-                for (int j = 0; j < P.L; ++j) {
-                    const long long idx = (long long)b * P.L + j;
-                    if (P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
-                }
+        const int n_def = s_last - 1;
+        const int* list = P.cnt + P.BL + P.B;
+        for (int i = tid; i < n_def; i += kThreads) {   // finalized before every CTA had scanned
+            const int b = __ldcg(list + i);
+            for (int j = 0; j < P.L; ++j) {
+                const long long idx = (long long)b * P.L + j;
+                if (P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
             }
-            committed[b] = 0;
         }
         if (tid == 0) {
             P.ctl[0] = 0;
             P.ctl[1] = 0;
+            P.ctl[2] = 0;
         }
     }
 }
@@ -1001,6 +1070,13 @@ __global__ void __launch_bounds__(256) features_kernel(int B, int L, int mask_id
 
 int g_smem_configured[64];
 
+struct LaunchFacts {
+    volatile bool ready;
+    long long max_dynamic;   // dynamic shared memory available to step_kernel
+};
+LaunchFacts g_launch_facts[64];
+std::mutex g_launch_mu;
+
 }  // namespace
 }  // namespace dllm
 
@@ -1022,7 +1098,7 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     if (!a) return DLLM_ERR_INVAL;
     if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
     if (a->B == 0) return DLLM_OK;
-    if ((long long)a->B * a->L > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
+    if ((long long)a->B * a->L > 0x7fffffffLL || a->B >= (1 << 16)) return DLLM_ERR_UNSUPPORTED;
     if (!a->logits || !a->input_ids || !a->thr || !a->conf_state || !a->done || !a->accept_len || !a->n_new)
         return DLLM_ERR_INVAL;
     if ((a->ldv % 8) != 0 || (reinterpret_cast<uintptr_t>(a->logits) & 15u) != 0) return DLLM_ERR_ALIGN;
@@ -1034,38 +1110,53 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     DLLM_CUDA_TRY(cudaGetDevice(&dev));
     const int G = sm_count();
     if (G <= 0) return DLLM_ERR_CUDA;
+    if (G >= (1 << 15)) return DLLM_ERR_UNSUPPORTED;   // the exit counter's low half counts CTAs
     const int BL = a->B * a->L;
     const int NC = (a->V + kChunkElems - 1) / kChunkElems;
-    if ((long long)BL * NC > 0x7fffffffLL || (long long)BL * G > 0x7fffffffLL ||
-        (long long)a->V * G > 0x7fffffffLL)
+    if ((long long)BL * NC > 0x7fffffffLL || (long long)BL * G > 0x7fffffffLL || (long long)a->V * G > 0x7fffffffLL)
         return DLLM_ERR_UNSUPPORTED;
-    const int list_cap = BL / G + 3;
+    // rows one CTA touches: its static share (< BL / G + 3 rows) plus the
+    // tail (at most min(ceil(BL / kTailDen), kTailRowsMax) rows)
+    const int static_cap = BL / G + 3;
+    const int list_cap = static_cap + min((BL + kTailDen - 1) / kTailDen, kTailRowsMax);
     const int zero_cap = a->B / G + 1;
     const size_t smem = size_t(kStreamWarps) * kStages * kCopyBytes + size_t(kStreamWarps) * kStages * 8 +
                         size_t(2 * list_cap + zero_cap) * 4 + size_t((BL + 15) / 16) * 2;
-    int max_optin = 0;
-    DLLM_CUDA_TRY(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-    cudaFuncAttributes fa;
-    DLLM_CUDA_TRY(cudaFuncGetAttributes(&fa, step_kernel));
-    if (smem + fa.sharedSizeBytes > size_t(max_optin)) return DLLM_ERR_UNSUPPORTED;
-    if (dev < 0 || dev >= 64 || g_smem_configured[dev] < (int)smem) {
-        DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (dev >= 0 && dev < 64) g_smem_configured[dev] = (int)smem;
+    // per-device launch facts, queried once
+    if (dev < 0 || dev >= 64) return DLLM_ERR_UNSUPPORTED;
+    LaunchFacts& lf = g_launch_facts[dev];
+    if (!lf.ready) {
+        std::lock_guard<std::mutex> lock(g_launch_mu);
+        if (!lf.ready) {
+            int max_optin = 0;
+            DLLM_CUDA_TRY(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+            cudaFuncAttributes fa;
+            DLLM_CUDA_TRY(cudaFuncGetAttributes(&fa, step_kernel));
+            lf.max_dynamic = max_optin - (long long)fa.sharedSizeBytes;
+            lf.ready = true;
+        }
+    }
+    if ((long long)smem > lf.max_dynamic) return DLLM_ERR_UNSUPPORTED;
+    if (g_smem_configured[dev] < (int)smem) {
+        std::lock_guard<std::mutex> lock(g_launch_mu);
+        if (g_smem_configured[dev] < (int)smem) {
+            DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            g_smem_configured[dev] = (int)smem;
+        }
     }
 
     unsigned char* ws = static_cast<unsigned char*>(a->workspace);
     unsigned char* data = ws + ((a->workspace_bytes - w.data_bytes) & ~size_t(255));
     StepParams P;
     P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
-    P.list_cap = list_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
+    P.list_cap = list_cap; P.static_cap = static_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
     P.logits = a->logits; P.ids = a->input_ids; P.thr = a->thr; P.cs = a->conf_state;
     P.done = a->done; P.accept = a->accept_len; P.n_new = a->n_new; P.feats = a->feats;
     P.conf_out = a->conf_out; P.lse_out = a->lse_out; P.tok_out = a->tok_out;
     P.ctl = reinterpret_cast<int*>(ws);
     P.cnt = reinterpret_cast<int*>(ws + 64);
-    P.part = reinterpret_cast<Partial*>(data + w.off_part);
-    P.row_conf = reinterpret_cast<float*>(data + w.off_conf);
-    P.row_lse = reinterpret_cast<float*>(data + w.off_lse);
+    P.part = reinterpret_cast<unsigned long long*>(ws + w.off_part);
+    P.row_word = reinterpret_cast<unsigned long long*>(ws + w.off_row);
     P.row_tok = reinterpret_cast<int*>(data + w.off_tok);
     P.sel = data + w.off_sel;
     P.err = error_word_ptr();

@@ -49,7 +49,7 @@ extern "C" {
 
 /* Device error word values (read with dllm_get_device_error). */
 #define DLLM_DEVERR_NONE 0
-#define DLLM_DEVERR_TIMEOUT 1     /* a bounded wait on a bulk copy expired */
+#define DLLM_DEVERR_TIMEOUT 1     /* a bounded wait (bulk copy, partial word) expired */
 #define DLLM_DEVERR_ROW_WIDTH 2   /* dllm_pack: p + (b + 1) * L > W for a row */
 #define DLLM_DEVERR_BLOCK_INDEX 3 /* dllm_advance: block index outside [0, K) or output row too short */
 
@@ -142,11 +142,12 @@ typedef struct dllm_step_args {
 
 /* Workspace bytes dllm_step needs for this shape (0 if the shape is invalid).
  * A workspace sized for (B, L, V) also serves every call with B' <= B,
- * B'*L' <= B*L and B'*L'*ceil(V'/16384) <= B*L*ceil(V/16384): its first
- * quarter holds the counters that must be zero between calls and the
- * rest the per-call data, so no call's data lands on another's counters.
- * Calls sharing a workspace must be ordered on one stream.  After a device
- * error (DLLM_DEVERR_TIMEOUT) re-initialise it. */
+ * B'*L' <= B*L and B'*L'*ceil(V'/8192) <= B*L*ceil(V/8192): its first
+ * quarter holds the words that must be zero between calls (counters and
+ * the packed chunk partials, which each call clears as it reads them) and
+ * the rest the per-call data, so no call's data lands on another's
+ * zero-at-rest words.  Calls sharing a workspace must be ordered on one
+ * stream.  After a device error (DLLM_DEVERR_TIMEOUT) re-initialise it. */
 size_t dllm_step_workspace_size(int32_t B, int32_t L, int32_t V);
 
 /* cudaMemsetAsync(workspace, 0, bytes) on `stream`. */
@@ -154,8 +155,11 @@ int dllm_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* Run S1-S6.  Errors: DLLM_ERR_INVAL (shape, NULL required pointer),
  * DLLM_ERR_ALIGN (logits not 16-byte aligned, ldv % 8 != 0),
- * DLLM_ERR_WORKSPACE, DLLM_ERR_UNSUPPORTED, DLLM_ERR_CUDA.  A NaN threshold
- * never passes.  input_ids and conf_state may not alias any output. */
+ * DLLM_ERR_WORKSPACE, DLLM_ERR_CUDA, DLLM_ERR_UNSUPPORTED (B >= 65536,
+ * B * L * number of SMs * 8 or V * number of SMs * 8 at or above 2^31, or
+ * the shared memory the shape needs above the device's limit).  A NaN
+ * threshold never passes.  input_ids and conf_state may not alias any
+ * output. */
 int dllm_step(const dllm_step_args* args, void* stream);
 
 /* dllm_step without a caller workspace (the pages have no counterpart; this
