@@ -45,6 +45,7 @@ METRIC = "masked positions/sec and logits GB/s per denoise step (% of GB300 HBM 
 UNIT = "masked positions/s"
 WORKLOADS = {
     "dream": "dream7b_shaped_mixed_state_step",
+    "dream_fixed_steps": "dream7b_shaped_mixed_state_step_fixed_steps_S32",
     "llada": "llada8b_shaped_mixed_state_step",
     "stress": "large_batch_stress_step",
     "tiny": "tiny_step",
@@ -80,8 +81,17 @@ def aggregate(units_local, seconds_local, dist=None):
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
+FIXED_STEPS_S = 32   # the pages' S = 32 denoising steps per block of L = 32
+
+
+def step_config_name(name):
+    """Step configuration behind a workload name (the fixed-steps workload
+    runs the Dream-shaped batch under the fixed-steps rule)."""
+    return "dream" if name in ("blockserve", "dream_fixed_steps") else name
+
+
 def make_workload(seed, name="dream"):
-    cfg = synth.STEP_CONFIGS[name]
+    cfg = synth.STEP_CONFIGS[step_config_name(name)]
     inp = synth.make_step_state(cfg, seed)
     lcfg = synth.LoopConfig("mixed", cfg.B, 64, 1024, LOOP_K * cfg.L, cfg.L, cfg.V, BUDGET, 0.9, cfg.offset_max)
     reqs = synth.make_loop_requests(lcfg, seed)
@@ -202,7 +212,7 @@ class ClockSampler:
 class Pipeline:
     """Device buffers and prebuilt C-ABI argument structs for one batch."""
 
-    def __init__(self, cfg, inp, reqs, b, gen, pending_p, device, ring=RING):
+    def __init__(self, cfg, inp, reqs, b, gen, pending_p, device, ring=RING, fixed_steps=None):
         import torch
         import denoise_step_token_gb300 as dllm
         self.torch, self.dllm, self.lib = torch, dllm, dllm.load()
@@ -275,6 +285,15 @@ class Pipeline:
         self.admit_idx = np.zeros(max(len(pending_p), 1), dtype=np.int32)
         self.n_admit = ctypes.c_int32(0)
         self.args = [self._build_args(s) for s in range(ring)]
+        # fixed-steps rule: request b has taken L - (its masked count) steps
+        # of its block (one token per step at S = L), so its quota is
+        # transfer_quota(L, S, that step)
+        self.quota = None
+        if fixed_steps is not None:
+            steps = L - inp.masked.sum(axis=1)
+            q = np.array([dllm.transfer_quota(L, fixed_steps, int(t)) for t in steps], dtype=np.int32)
+            self.quota = torch.from_numpy(q).to(device)
+            self.quota_ptr = ctypes.c_void_p(self.quota.data_ptr())
 
     def view(self, slot, name, dtype=None, shape=None):
         t = self.state[slot, self.off[name]:self.off[name] + self.words[name]]
@@ -325,7 +344,10 @@ class Pipeline:
         rc = lib.dllm_pack(ctypes.byref(pa), stream)
         if ev_before is not None:
             ev_before.record()
-        rc |= lib.dllm_step(ctypes.byref(sa), stream)
+        if self.quota is None:
+            rc |= lib.dllm_step(ctypes.byref(sa), stream)
+        else:
+            rc |= lib.dllm_step_quota(ctypes.byref(sa), self.quota_ptr, stream)
         if ev_after is not None:
             ev_after.record()
         rc |= lib.dllm_advance(ctypes.byref(aa), stream)
@@ -347,7 +369,8 @@ def run_gpu(args, rank, world, local_rank, dist):
     torch.cuda.set_device(device)
     dllm.load()
     cfg, inp, reqs, b, gen, pending_p = make_workload(1000 + rank, args.workload)
-    pipe = Pipeline(cfg, inp, reqs, b, gen, pending_p, device)
+    pipe = Pipeline(cfg, inp, reqs, b, gen, pending_p, device,
+                    fixed_steps=FIXED_STEPS_S if args.workload == "dream_fixed_steps" else None)
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     K, W = args.steps, args.warmup
@@ -452,10 +475,19 @@ def oracle_request_logits(inp, b):
     return out
 
 
-def oracle_over_requests(inp, reqs, threads):
+def fixed_steps_quota(inp, S):
+    """Per-request counts of the fixed-steps rule for a mixed-state batch:
+    request b has taken L - (its masked count) steps of its block."""
+    import oracle
+    L = inp.cfg.L
+    return np.array([oracle.transfer_quota(L, S, int(L - m)) for m in inp.masked.sum(axis=1)], dtype=np.int64)
+
+
+def oracle_over_requests(inp, reqs, threads, quota=None):
     """Run the oracle's step on each listed request (one sub-batch each) on a
     thread pool; returns (masked rows processed, wall seconds of the oracle
-    calls alone)."""
+    calls alone).  ``quota``: per-request counts of the fixed-steps rule, or
+    None for the threshold rule."""
     import oracle
     cfg = inp.cfg
     logits = {b: oracle_request_logits(inp, b) for b in reqs}
@@ -463,7 +495,7 @@ def oracle_over_requests(inp, reqs, threads):
 
     def one(b):
         oracle.step(logits[b], cfg.V, inp.input_ids[b:b + 1], inp.thr[b:b + 1], inp.conf_state[b:b + 1],
-                    cfg.mask_id)
+                    cfg.mask_id, quota=None if quota is None else quota[b:b + 1])
 
     t = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
@@ -471,10 +503,10 @@ def oracle_over_requests(inp, reqs, threads):
     return rows, time.perf_counter() - t
 
 
-def cpu_baseline(inp):
+def cpu_baseline(inp, quota=None):
     threads = os.cpu_count() or 1
     reqs = list(range(inp.cfg.B))
-    rows, secs = oracle_over_requests(inp, reqs, threads)
+    rows, secs = oracle_over_requests(inp, reqs, threads, quota)
     return {"value": rows / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"one full pass of the oracle over the {inp.cfg.B}-request Dream-shaped batch "
                       f"({rows} masked rows, {secs:.2f} s wall on {threads} threads, one request per task)"}
@@ -482,7 +514,8 @@ def cpu_baseline(inp):
 
 def run_reference(args, rank, world):
     """The oracle, as it stands, timed on the host cores (reference arm)."""
-    cfg, inp, *_ = make_workload(1000, "dream" if args.workload == "blockserve" else args.workload)
+    cfg, inp, *_ = make_workload(1000, args.workload)
+    quota = fixed_steps_quota(inp, FIXED_STEPS_S) if args.workload == "dream_fixed_steps" else None
     threads = os.cpu_count() or 1
     # probe: one request, to size each step's sample so the run ends in ~2 min
     probe_rows, probe_s = oracle_over_requests(inp, [int(np.argmax(inp.masked.sum(axis=1)))], 1)
@@ -504,11 +537,11 @@ def run_reference(args, rank, world):
         return picked
 
     for _ in range(args.warmup):
-        oracle_over_requests(inp, sample(), threads)
+        oracle_over_requests(inp, sample(), threads, quota)
     units = 0
     secs = 0.0
     for _ in range(args.steps):
-        r, s = oracle_over_requests(inp, sample(), threads)
+        r, s = oracle_over_requests(inp, sample(), threads, quota)
         units += r
         secs += s
     value = units / secs
@@ -615,7 +648,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dream",
-                    help="dream (default, the headline), llada, stress, tiny, or the blockserve loop")
+                    help="dream (default, the headline), dream_fixed_steps, llada, stress, tiny, or the blockserve loop")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -647,8 +680,9 @@ def main():
     value = res["units"] / res["seconds"]
     e2e = run_e2e(pipe, args.e2e_steps)
     cpu = None
+    fixed = args.workload == "dream_fixed_steps"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(res["inp"])
+        cpu = cpu_baseline(res["inp"], fixed_steps_quota(res["inp"], FIXED_STEPS_S) if fixed else None)
     if dist is not None:
         dist.barrier()
     if rank == 0:
@@ -657,7 +691,9 @@ def main():
             "ms_per_step": res["seconds"] * 1e3 / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOADS[args.workload], "B": cfg.B, "L": cfg.L, "V": cfg.V, "masked_rows": pipe.M,
-                       "thresholds": "per request from {0.5,0.6,0.7,0.8,0.9}", "mask_fraction": "U[0,1] per request",
+                       "rule": (f"fixed steps, S = {FIXED_STEPS_S} per block" if fixed else
+                                "threshold per request from {0.5,0.6,0.7,0.8,0.9}"),
+                       "mask_fraction": "U[0,1] per request",
                        "box_W": pipe.W, "box_cost": pipe.cost, "token_budget": BUDGET,
                        "step": "admit(host)+pack+step+advance+compact",
                        "l2": "inputs larger than L2: 0.62 GB of masked logits rows per step, no flush",
@@ -666,7 +702,8 @@ def main():
             "step_kernel_ms": step_ms,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                         "kernel": "step_kernel (dllm_step)", "algorithmic_bytes_per_launch": alg},
+                         "kernel": "step_kernel (dllm_step_quota)" if fixed else "step_kernel (dllm_step)",
+                         "algorithmic_bytes_per_launch": alg},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": LAUNCHES_PER_STEP * K,

@@ -94,6 +94,8 @@ _SIGNATURES = {
     "dllm_step_workspace_size": (_sz, [_i32, _i32, _i32]),
     "dllm_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
     "dllm_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
+    "dllm_step_quota": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p, _p]),
+    "dllm_transfer_quota": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "dllm_step_noalloc": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
     "dllm_step_noalloc_capacity": (_sz, []),
     "dllm_features": (ctypes.c_int, [_i32, _i32, _i32, _p, _p, _p, _p]),
@@ -220,22 +222,33 @@ def step_workspace_size(B, L, V):
     return int(load().dllm_step_workspace_size(B, L, V))
 
 
-def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=False, out=None, workspace=None):
-    """One denoise step (dllm_step) on the current stream.
+def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=False, out=None, workspace=None,
+         quota=None):
+    """One denoise step (dllm_step, or dllm_step_quota when ``quota`` is
+    given) on the current stream.
 
     logits:     bf16 (or 16-bit) CUDA tensor of B*L rows with V <= row stride
                 (shape [B, L, ldv] or [B*L, ldv]); ldv % 8 == 0
     input_ids:  int32 [B, L] (updated in place)
-    thr:        float32 [B]
+    thr:        float32 [B] (threshold rule; may be None with ``quota``)
     conf_state: float32 [B, L] (updated in place)
+    quota:      int32 [B] CUDA tensor or None: positions to unmask per
+                request under the fixed-steps rule
     Returns a dict of output tensors: done (uint8 [B]), accept_len, n_new
     (int32 [B]), feats (float32 [B, 6]) and, with debug, conf / lse / tok [B, L].
     """
     torch = _torch()
-    dev = _require_cuda(logits, input_ids, thr, conf_state)
+    if quota is None:
+        dev = _require_cuda(logits, input_ids, thr, conf_state)
+        if thr.dtype != torch.float32:
+            raise TypeError("thr float32 expected")
+    else:
+        dev = _require_cuda(logits, input_ids, conf_state, quota, *(() if thr is None else (thr,)))
+        if quota.dtype != torch.int32 or quota.numel() != input_ids.shape[0]:
+            raise TypeError("quota must be int32 [B]")
     B, L = input_ids.shape
-    if input_ids.dtype != torch.int32 or conf_state.dtype != torch.float32 or thr.dtype != torch.float32:
-        raise TypeError("input_ids int32, thr / conf_state float32 expected")
+    if input_ids.dtype != torch.int32 or conf_state.dtype != torch.float32:
+        raise TypeError("input_ids int32, conf_state float32 expected")
     if logits.element_size() != 2:
         raise TypeError("logits must be a 16-bit (bf16) tensor")
     ldv = logits.shape[-1]
@@ -261,8 +274,21 @@ def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=Fa
                  done=_ptr(out["done"]), accept_len=_ptr(out["accept_len"]), n_new=_ptr(out["n_new"]),
                  feats=_ptr(out.get("feats")), conf_out=_ptr(out.get("conf")), lse_out=_ptr(out.get("lse")),
                  tok_out=_ptr(out.get("tok")), workspace=_ptr(ws), workspace_bytes=ws.numel())
-    _check("dllm_step", lib.dllm_step(ctypes.byref(a), _stream(dev)))
+    if quota is None:
+        _check("dllm_step", lib.dllm_step(ctypes.byref(a), _stream(dev)))
+    else:
+        _check("dllm_step_quota", lib.dllm_step_quota(ctypes.byref(a), _ptr(quota), _stream(dev)))
     return out
+
+
+def transfer_quota(L, S, s):
+    """dllm_transfer_quota: positions to unmask at step s of a block under
+    the fixed-steps rule (L over S steps, the remainder to the first steps;
+    L once s >= S)."""
+    q = int(load().dllm_transfer_quota(int(L), int(S), int(s)))
+    if q < 0:
+        raise ValueError("transfer_quota needs L >= 1, S >= 1, s >= 0")
+    return q
 
 
 def step_host(logits_host, input_ids, thr, conf_state, *, V, mask_id, device=None):

@@ -148,6 +148,27 @@ __device__ __forceinline__ int atom_add_release_gpu(int* p, int v) {
     return old;
 }
 
+// Unsigned division by a divisor fixed at launch (Granlund and Montgomery,
+// "Division by Invariant Integers using Multiplication", PLDI 1994, section
+// 4): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(m, n) + n) >> l for every 0 <= n < 2^31 (the sum stays
+// below 2^32 because umulhi(m, n) < n).
+struct FastDiv {
+    uint32_t m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const unsigned long long num = (1ull << 32) * ((1ull << l) - d);   // < 2^63: 2^l - d < d <= 2^31
+    return FastDiv{static_cast<uint32_t>(num / d + 1), l};
+}
+
+__device__ __forceinline__ int fast_div(int n, const FastDiv& f) {
+    const uint32_t u = static_cast<uint32_t>(n);
+    return static_cast<int>((__umulhi(u, f.m) + u) >> f.l);
+}
+
 // Relaxed (but strong, single-copy atomic) accesses at GPU scope: no
 // ordering with this thread's other accesses, no fence.
 __device__ __forceinline__ int atom_add_relaxed_gpu(int* p, int v) {

@@ -140,10 +140,12 @@ __device__ __noinline__ unsigned long long poll_word(const unsigned long long* p
 
 struct StepParams {
     int B, L, V, NC, BL, mask_id, list_cap, static_cap, zero_cap;
+    FastDiv div_nc, div_g;   // division by NC and by the grid size
     long long ldv;
     const uint16_t* logits;
     int* ids;
     const float* thr;
+    const int* quota;   // [B] positions to unmask (fixed-steps rule), or null (threshold rule)
     float* cs;
     uint8_t* done;
     int* accept;
@@ -386,8 +388,8 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     // requests without masked rows read only the launch's inputs.
     const int L = P.L;
     const long long base = (long long)b * L;
-    const float t = P.thr[b];
-    const int scanned = (lane == 0 && has_masked) ? ld_acquire_gpu(P.ctl) : 0;
+    const float t = P.quota ? 0.f : P.thr[b];
+    const int q = P.quota ? P.quota[b] : 0;
 
     int id[NK], tk[NK];
     float c[NK], cs_old[NK];
@@ -405,6 +407,9 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
         cs_old[k] = valid ? P.cs[base + j] : 0.f;
         rw[k] = (valid && has_masked) ? ld_relaxed_gpu_u64(P.row_word + base + j) : 0ull;
     }
+    // the scan count guards only the commit at the end: loaded after the
+    // block's loads so that its acquire does not hold them back
+    const int scanned = (lane == 0 && has_masked) ? ld_acquire_gpu(P.ctl) : 0;
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
@@ -430,7 +435,7 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     any_masked = __any_sync(0xffffffffu, any_masked);
     any_pass = __any_sync(0xffffffffu, any_pass);
     int fb_j = -1;
-    if (any_masked && !any_pass) {
+    if (!P.quota && any_masked && !any_pass) {
         // most confident masked position, lowest position on ties
         float bc = best_c;
         int bj = best_j;
@@ -446,6 +451,29 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
         fb_j = bj;
     }
 
+    // fixed-steps rule: a masked position is taken when fewer than q masked
+    // positions beat it (higher confidence, or equal and lower position)
+    int qrank[NK];
+#pragma unroll
+    for (int k = 0; k < NK; ++k) qrank[k] = 0;
+    if (P.quota) {
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+#pragma unroll 4
+            for (int src = 0; src < 32; ++src) {
+                const int jj = src + 32 * kk;
+                const float co = __shfl_sync(0xffffffffu, c[kk], src);
+                const bool mo = __shfl_sync(0xffffffffu, msk[kk] ? 1 : 0, src) != 0;
+                if (!mo) continue;
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    const int j = lane + 32 * k;
+                    if (msk[k] && (co > c[k] || (co == c[k] && jj < j))) ++qrank[k];
+                }
+            }
+        }
+    }
+
     float val[NK];
     bool inU[NK];
     bool selk[NK];
@@ -455,7 +483,7 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
         const bool valid = j < L;
-        const bool s = msk[k] && (c[k] > t || j == fb_j);
+        const bool s = msk[k] && (P.quota ? qrank[k] < q : (c[k] > t || j == fb_j));
         selk[k] = s;
         const int new_id = s ? tk[k] : id[k];
         float new_cs = 0.f;
@@ -725,9 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const int T = min((M + kTailDen - 1) / kTailDen, kTailRowsMax);
     const int Ms = M - T;
     auto first_unit = [&](int k) -> int {
-        const unsigned mk = (unsigned)Ms * k;
-        int r = (int)(mk / (unsigned)G);
-        const int e = (int)(((unsigned)V * (mk - (unsigned)r * G)) / (unsigned)G);
+        const int mk = Ms * k;
+        int r = fast_div(mk, P.div_g);
+        const int e = fast_div(V * (mk - r * G), P.div_g);
         int cc = (e + kChunkElems - 1) / kChunkElems;
         if (cc >= NC) {
             r += 1;
@@ -739,21 +767,28 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const int u1 = first_unit(cta + 1);
     const int u_tail = Ms * NC;
     const int n_tail = U - u_tail;
-    const int r_lo = u0 / NC;
-    const int r_hi = (u1 > u0) ? (u1 - 1) / NC : r_lo - 1;
+    const int r_lo = fast_div(u0, P.div_nc);
+    const int r_hi = (u1 > u0) ? fast_div(u1 - 1, P.div_nc) : r_lo - 1;
     const int r_tail = Ms;   // first row of the tail
     const int r_last = (n_tail > 0) ? M - 1 : r_hi;
     const int static_cap = P.static_cap;
-    int rank = before;
-    for (int g = g0; g < g1 && rank <= r_last; ++g) {
-        unsigned bits = s_gmask[g];
-        while (bits) {
-            const int i = __ffs(bits) - 1;
-            bits &= bits - 1;
-            if (rank >= r_lo && rank <= r_hi) s_list[rank - r_lo] = (g << 4) + i;
-            if (rank >= r_tail) s_list[static_cap + rank - r_tail] = (g << 4) + i;
-            ++rank;
+    // each set bit's rank is independent of the others: before the group's
+    // first rank plus the set bits below it in the group
+    int rank0 = before;
+    for (int g = g0; g < g1 && rank0 <= r_last; ++g) {
+        const unsigned bits = s_gmask[g];
+        const int c = __popc(bits);
+        if ((rank0 <= r_hi && rank0 + c > r_lo) || rank0 + c > r_tail) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if ((bits >> i) & 1u) {
+                    const int rank = rank0 + __popc(bits & ((1u << i) - 1u));
+                    if (rank >= r_lo && rank <= r_hi) s_list[rank - r_lo] = (g << 4) + i;
+                    if (rank >= r_tail) s_list[static_cap + rank - r_tail] = (g << 4) + i;
+                }
+            }
         }
+        rank0 += c;
     }
     // this CTA's requests (b = cta + G*k) without a masked position
     for (long long k = tid; cta + (long long)G * k < P.B; k += kThreads) {
@@ -775,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const int V32 = P.V;
     // masked position of unit gu's row (units of the tail have their own slots)
     auto row_of = [&](int gu) -> int {
-        const int rr = gu / NC;
+        const int rr = fast_div(gu, P.div_nc);
         return (gu >= u_tail) ? s_list[static_cap + rr - r_tail] : s_list[rr - r_lo];
     };
 
@@ -794,17 +829,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
         // Take the next group: returns its first unit (or -1) and its size.
         // Once the CTA's pool is spent, units come one at a time from the
-        // shared tail through tickets on ctl[2]; lane 0 draws each ticket
-        // one grab ahead of its use, so the atomic's latency stays hidden.
+        // shared tail through tickets on ctl[2].  Lane 0 draws its first
+        // ticket while the CTA's pool is nearly spent, hiding that atomic's
+        // latency; later tickets are drawn when needed (a ticket held ahead
+        // is a chunk of work one warp still owes while others idle).
         int t_ahead = -1;   // lane 0: ticket drawn ahead of use
-        const int ahead_margin = G * kStreamWarps;
         auto grab = [&](int& k) -> int {
             int got = -1, kk = 0;
             if (lane == 0) {
                 int cur = *reinterpret_cast<volatile int*>(&s_next);
                 while (cur < n_units) {
                     const int gu = u_first + cur;
-                    const int row_end = (gu / NC + 1) * NC - u_first;   // first unit of the next row
+                    const int row_end = (fast_div(gu, P.div_nc) + 1) * NC - u_first;   // first unit of the next row
                     const int left = n_units - cur;
                     int want = left > tail_units ? kGroup : 1;
                     want = min(want, min(row_end - cur, left));
@@ -824,10 +860,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     if (t < n_tail) {
                         got = u_tail + t;
                         kk = 1;
-                        // draw ahead only while every warp can still get a
-                        // ticket: near the end a ticket held ahead would be
-                        // extra work for one warp while others idle
-                        if (t + ahead_margin < n_tail) t_ahead = atomicAdd(P.ctl + 2, 1);
                     }
                 }
             }
@@ -846,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         bool failed = false;
 
         auto start_chunk = [&](int gu) {
-            const int c = gu - (gu / NC) * NC;
+            const int c = gu - fast_div(gu, P.div_nc) * NC;
             const int row = row_of(gu);
             p_unit = gu;
             p_q = 0;
@@ -913,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 fifo_k[i] = fifo_k[i + 1];
             }
             --nfifo;
-            const int c0 = gu - (gu / NC) * NC;
+            const int c0 = gu - fast_div(gu, P.div_nc) * NC;
             const int row = row_of(gu);
             float gm[kGroup], gs[kGroup];
             int gi[kGroup];
@@ -1094,12 +1126,17 @@ extern "C" int dllm_workspace_init(void* workspace, size_t bytes, void* stream) 
     return DLLM_OK;
 }
 
-extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
+namespace dllm {
+namespace {
+
+// dllm_step and dllm_step_quota: quota null selects the threshold rule.
+int launch_step(const dllm_step_args* a, const int32_t* quota, void* stream) {
     if (!a) return DLLM_ERR_INVAL;
     if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
     if (a->B == 0) return DLLM_OK;
     if ((long long)a->B * a->L > 0x7fffffffLL || a->B >= (1 << 16)) return DLLM_ERR_UNSUPPORTED;
-    if (!a->logits || !a->input_ids || !a->thr || !a->conf_state || !a->done || !a->accept_len || !a->n_new)
+    if (!a->logits || !a->input_ids || (!quota && !a->thr) || !a->conf_state || !a->done || !a->accept_len ||
+        !a->n_new)
         return DLLM_ERR_INVAL;
     if ((a->ldv % 8) != 0 || (reinterpret_cast<uintptr_t>(a->logits) & 15u) != 0) return DLLM_ERR_ALIGN;
     if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return DLLM_ERR_WORKSPACE;
@@ -1150,7 +1187,9 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     StepParams P;
     P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
     P.list_cap = list_cap; P.static_cap = static_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
-    P.logits = a->logits; P.ids = a->input_ids; P.thr = a->thr; P.cs = a->conf_state;
+    P.div_nc = make_fastdiv((uint32_t)NC);
+    P.div_g = make_fastdiv((uint32_t)G);
+    P.logits = a->logits; P.ids = a->input_ids; P.thr = a->thr; P.quota = quota; P.cs = a->conf_state;
     P.done = a->done; P.accept = a->accept_len; P.n_new = a->n_new; P.feats = a->feats;
     P.conf_out = a->conf_out; P.lse_out = a->lse_out; P.tok_out = a->tok_out;
     P.ctl = reinterpret_cast<int*>(ws);
@@ -1164,6 +1203,22 @@ extern "C" int dllm_step(const dllm_step_args* a, void* stream) {
     step_kernel<<<G, kThreads, smem, as_stream(stream)>>>(P);
     DLLM_CUDA_TRY(cudaGetLastError());
     return DLLM_OK;
+}
+
+}  // namespace
+}  // namespace dllm
+
+extern "C" int dllm_step(const dllm_step_args* a, void* stream) { return launch_step(a, nullptr, stream); }
+
+extern "C" int dllm_step_quota(const dllm_step_args* a, const int32_t* quota, void* stream) {
+    if (!quota) return DLLM_ERR_INVAL;
+    return launch_step(a, quota, stream);
+}
+
+extern "C" int32_t dllm_transfer_quota(int32_t L, int32_t S, int32_t s) {
+    if (L < 1 || S < 1 || s < 0) return -1;
+    if (s >= S) return L;
+    return L / S + (s < L % S ? 1 : 0);
 }
 
 extern "C" int dllm_features(int32_t B, int32_t L, int32_t mask_id, const int32_t* input_ids,

@@ -19,16 +19,19 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import admit, advance, compact, pack, pack_plan, refill, step
+from . import admit, advance, compact, pack, pack_plan, refill, step, transfer_quota
 
 
 class DeviceLoop:
-    """One pending queue served to completion on one device."""
+    """One pending queue served to completion on one device.  ``S``: None
+    for the threshold rule, else the fixed-steps rule with S steps per block
+    (BlockServe page, section II-E)."""
 
     def __init__(self, p, K, prompt_off, prompt_tokens, thr, *, L, V, mask_id, pad_id, budget, device,
-                 mode="fdfo", capacity=None, features=True):
+                 mode="fdfo", capacity=None, features=True, S=None):
         import torch
         assert mode in ("fdfo", "sync")
+        self.S = None if S is None else int(S)
         self.torch = torch
         self.L, self.V, self.mask_id, self.pad_id = int(L), int(V), int(mask_id), int(pad_id)
         self.budget, self.mode, self.device, self.features = int(budget), mode, device, features
@@ -102,8 +105,12 @@ class DeviceLoop:
     # -- one denoise step -------------------------------------------------------
     def step_phase(self, logits):
         A = self.A
+        quota = None
+        if self.S is not None:
+            q = np.array([transfer_quota(self.L, self.S, int(s)) for s in self.s_h], dtype=np.int32)
+            quota = self.torch.from_numpy(q).to(self.device)
         out = step(logits, self.ids[:A], self.thr[:A], self.cs[:A], V=self.V, mask_id=self.mask_id,
-                   feats=self.features)
+                   feats=self.features, quota=quota)
         done = out["done"].cpu().numpy().astype(bool)     # the per-step readback
         self.last = out
         return done, out

@@ -162,6 +162,23 @@ int dllm_workspace_init(void* workspace, size_t bytes, void* stream);
  * output. */
 int dllm_step(const dllm_step_args* args, void* stream);
 
+/* S1-S6 with the fixed-steps rule in place of the threshold rule (BlockServe
+ * page, section II-E: each block's masked tokens are transferred over S
+ * denoising steps by a per-step quota).  Request b unmasks exactly quota[b]
+ * of its masked positions -- the most confident ones, ties to the lower
+ * position -- or all of them when fewer are masked; quota[b] <= 0 unmasks
+ * nothing.  quota: device int32 [B].  Everything else is dllm_step's (S1, S2,
+ * S4-S6, outputs, workspace rules); args->thr is not read and may be NULL.
+ * Errors as dllm_step, plus DLLM_ERR_INVAL for a NULL quota. */
+int dllm_step_quota(const dllm_step_args* args, const int32_t* quota, void* stream);
+
+/* Host.  The fixed-steps quota of step s (0-based) of a block (BlockServe
+ * page, section II-E): L spread evenly over S steps, floor(L / S) per step
+ * plus one for each of the first L mod S steps; a step past the schedule
+ * (s >= S) returns L (transfer everything left).  -1 if L < 1, S < 1 or
+ * s < 0. */
+int32_t dllm_transfer_quota(int32_t L, int32_t S, int32_t s);
+
 /* dllm_step without a caller workspace (the pages have no counterpart; this
  * is a deployment convenience).  It runs exactly dllm_step, but its scratch
  * is a fixed buffer of dllm_step_noalloc_capacity() bytes (16 MiB) that the

@@ -112,6 +112,40 @@ def select_positions(masked, conf, thr):
     return sel
 
 
+def transfer_quota(L, S, s):
+    """Tokens to unmask at step s (0-based) of a block under the fixed-steps
+    rule (BlockServe page, section II-E, "向量化混合调度执行"): at the start
+    of each block cycle the block's L masked tokens are spread evenly over S
+    denoising steps, the same for every block since each starts fully masked.
+    Reading: q(s) = floor(L / S), plus one for the first L mod S steps; a step
+    past the schedule (s >= S) transfers everything still masked (returned
+    as L).
+    """
+    if L < 1 or S < 1 or s < 0:
+        raise ValueError("L, S >= 1 and s >= 0")
+    if s >= S:
+        return L
+    return L // S + (1 if s < L % S else 0)
+
+
+def select_quota(masked, conf, q):
+    """The q most confident masked positions of one block (all of them when
+    fewer than q are masked); ties go to the lower position.  The fixed-steps
+    counterpart of ``select_positions`` (BlockServe page, section II-E).
+    Plain repeated selection of the best remaining position."""
+    masked = np.asarray(masked, dtype=bool)
+    sel = np.zeros(masked.shape, dtype=bool)
+    for _ in range(max(int(q), 0)):
+        best = -1
+        for j in range(masked.size):
+            if masked[j] and not sel[j] and (best < 0 or conf[j] > conf[best]):
+                best = j
+        if best < 0:
+            break
+        sel[best] = True
+    return sel
+
+
 # ---------------------------------------------------------------------------
 # S6: confidence features for a step predictor.
 # ---------------------------------------------------------------------------
@@ -157,7 +191,7 @@ def features(input_ids, conf_state, mask_id):
 # ---------------------------------------------------------------------------
 # S1-S6: one denoise step.
 # ---------------------------------------------------------------------------
-def step(logits_bits, V, input_ids, thr, conf_state, mask_id):
+def step(logits_bits, V, input_ids, thr, conf_state, mask_id, quota=None):
     """``step(forward_batch, full_logits, states) -> done_flags`` for one
     batch (FDFO page, section "工程设计一"): read the logits, update
     input_ids by the LowConfidence rule, report per-block completion.
@@ -169,6 +203,9 @@ def step(logits_bits, V, input_ids, thr, conf_state, mask_id):
     conf_state:  float [B, L]  -- confidence at unmask time (per-request
                                   algorithm state carried between rounds,
                                   FDFO page, section "工程设计二")
+    quota:       int [B] or None -- when given, the fixed-steps rule
+                                  (``select_quota``) replaces the threshold
+                                  rule and ``thr`` is not read
     Returns a dict with the updated ``input_ids`` / ``conf_state`` and the
     outputs ``done``, ``accept_len``, ``n_new``, ``feats`` and per-position
     ``conf`` / ``lse`` / ``tok`` (NaN, NaN, -1 on positions not masked at
@@ -192,7 +229,10 @@ def step(logits_bits, V, input_ids, thr, conf_state, mask_id):
     done = np.zeros(B, dtype=np.uint8)
     accept = np.zeros(B, dtype=np.int64)
     for b in range(B):
-        sel = select_positions(masked[b], conf[b], thr[b])         # S3
+        if quota is None:
+            sel = select_positions(masked[b], conf[b], thr[b])     # S3
+        else:
+            sel = select_quota(masked[b], conf[b], quota[b])
         new_ids[b, sel] = tok[b, sel]                               # S4
         new_cs[b, sel] = conf[b, sel]
         n_new[b] = int(sel.sum())                                   # S5

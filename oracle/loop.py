@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import admit, box_width, compact, cost, pack, step
+from . import admit, box_width, compact, cost, pack, step, transfer_quota
 
 
 def advance(adv, rid, b, K, ids, cs, gen, mask_id):
@@ -47,8 +47,12 @@ def advance(adv, rid, b, K, ids, cs, gen, mask_id):
 
 
 class OracleLoop:
-    def __init__(self, p, K, prompts, thr, L, V, mask_id, pad_id, budget, mode="fdfo"):
+    """``S``: None for the threshold rule, else the fixed-steps rule with S
+    steps per block (``transfer_quota`` of each row's steps in its block)."""
+
+    def __init__(self, p, K, prompts, thr, L, V, mask_id, pad_id, budget, mode="fdfo", S=None):
         assert mode in ("fdfo", "sync")
+        self.S = S
         self.L, self.V, self.mask_id, self.pad_id = L, V, mask_id, pad_id
         self.budget = budget
         self.mode = mode
@@ -61,6 +65,7 @@ class OracleLoop:
         self.pending = sorted(range(R), key=lambda r: (int(self.p_all[r]), r))
         self.gen = [np.zeros(0, dtype=np.int64) for _ in range(R)]
         self.finish_iter = np.full(R, -1, dtype=np.int64)
+        self.admit_iter = np.full(R, -1, dtype=np.int64)
         # Active set, one entry per row (SoA).
         self.rid = []
         self.b = []
@@ -79,6 +84,7 @@ class OracleLoop:
         for k in sorted(picked, reverse=True):
             del self.pending[k]
         for r in new:
+            self.admit_iter[r] = self.iteration
             self.rid.append(r)
             self.b.append(0)
             self.s.append(0)
@@ -109,10 +115,17 @@ class OracleLoop:
                     out.append((i * self.L + j, self.rid[i], self.b[i], self.s[i], j))
         return out
 
+    def quota(self):
+        """Per-row counts of the fixed-steps rule this step (None under the
+        threshold rule)."""
+        if self.S is None:
+            return None
+        return np.array([transfer_quota(self.L, self.S, s) for s in self.s], dtype=np.int64)
+
     # -- one denoise step (FDFO page, "工程设计一") -----------------------------
     def step_phase(self, logits_bits):
         thr = np.array([self.thr_all[r] for r in self.rid], dtype=np.float32)
-        res = step(logits_bits, self.V, self.ids, thr, self.cs, self.mask_id)
+        res = step(logits_bits, self.V, self.ids, thr, self.cs, self.mask_id, quota=self.quota())
         had_masked = res["masked"].any(axis=1)
         self.ids = res["input_ids"]
         self.cs = res["conf_state"]

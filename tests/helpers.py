@@ -2,11 +2,13 @@
 upload of generated logits, comparison against the oracle.
 
 Decision margins: wherever float arithmetic decides a discrete outcome (a
-confidence against its threshold, the fallback's most confident position),
-the GPU computes in float32 and the oracle in float64.  Cases are drawn so
-that every such decision has a margin of at least 1e-4: a masked row whose
-oracle confidence is within 1e-4 of its threshold, or a fallback whose top
-two confidences are within 1e-4, gets its row redrawn (salt + 1).  Only the
+confidence against its threshold, the fallback's most confident position,
+the last position a fixed-steps quota takes), the GPU computes in float32
+and the oracle in float64.  Cases are drawn so that every such decision has
+a margin of at least 1e-4: a masked row whose oracle confidence is within
+1e-4 of its threshold, a fallback whose top two confidences are within
+1e-4, or a quota boundary whose two confidences (the q-th and (q+1)-th
+most confident) are within 1e-4, gets a row redrawn (salt + 1).  Only the
 oracle is consulted; no expected value comes from the GPU.
 """
 from __future__ import annotations
@@ -20,7 +22,7 @@ MARGIN = 1e-4
 CONF_TOL = 1e-5
 
 
-def _bad_rows(inp, reqs, conf_by_row):
+def _bad_rows(inp, reqs, conf_by_row, quota=None):
     """Rows of the listed requests that sit inside a decision margin."""
     cfg = inp.cfg
     L = cfg.L
@@ -29,8 +31,15 @@ def _bad_rows(inp, reqs, conf_by_row):
         rows = [b * L + j for j in range(L) if inp.input_ids[b, j] == cfg.mask_id]
         if not rows:
             continue
-        t = float(np.float32(inp.thr[b]))
         confs = np.array([conf_by_row[r] for r in rows])
+        if quota is not None:
+            q = int(quota[b])
+            if 0 < q < len(rows):
+                order = np.argsort(-confs, kind="stable")
+                if confs[order[q - 1]] - confs[order[q]] < MARGIN:
+                    bad.append(rows[order[q]])
+            continue
+        t = float(np.float32(inp.thr[b]))
         near = [r for r, c in zip(rows, confs) if abs(c - t) < MARGIN]
         bad.extend(near)
         if not (confs > t).any() and len(rows) > 1:
@@ -51,8 +60,9 @@ def host_rows(inp, rows):
     return out[: len(rows)]
 
 
-def enforce_margins(inp, reqs=None, max_iter=50):
-    """Redraw rows of the listed requests until all decisions have margin."""
+def enforce_margins(inp, reqs=None, max_iter=50, quota=None):
+    """Redraw rows of the listed requests until all decisions have margin
+    (threshold rule, or the fixed-steps rule when ``quota`` [B] is given)."""
     cfg = inp.cfg
     if reqs is None:
         reqs = range(inp.input_ids.shape[0])
@@ -62,7 +72,7 @@ def enforce_margins(inp, reqs=None, max_iter=50):
         rows = [b * L + j for b in reqs for j in range(L) if inp.input_ids[b, j] == cfg.mask_id]
         logits = host_rows(inp, rows)
         conf, _, _ = oracle.rows_stats(logits, range(len(rows)), cfg.V)
-        bad = _bad_rows(inp, reqs, dict(zip(rows, conf)))
+        bad = _bad_rows(inp, reqs, dict(zip(rows, conf)), quota)
         if not bad:
             return
         flat = inp.salt.reshape(-1)
@@ -88,13 +98,14 @@ def sub_batch_logits(inp, reqs):
     return out
 
 
-def oracle_step(inp, reqs=None):
+def oracle_step(inp, reqs=None, quota=None):
     cfg = inp.cfg
     if reqs is None:
         reqs = list(range(inp.input_ids.shape[0]))
     reqs = list(reqs)
     return oracle.step(sub_batch_logits(inp, reqs), cfg.V, inp.input_ids[reqs], inp.thr[reqs],
-                       inp.conf_state[reqs], cfg.mask_id)
+                       inp.conf_state[reqs], cfg.mask_id,
+                       quota=None if quota is None else np.asarray(quota)[reqs])
 
 
 def device_logits(inp, device, chunk_rows=2048):

@@ -116,3 +116,22 @@ def test_admit_rejects_unsorted_queue():
     n = ctypes.c_int32(0)
     rc = lib.dllm_admit(2, pend.ctypes.data, 0, None, None, 4, 100, idx.ctypes.data, ctypes.byref(n))
     assert rc == -1
+
+
+def test_transfer_quota_matches_oracle():
+    lib = dllm.load()
+    for L in (1, 2, 7, 32, 33, 64, 1024):
+        for S in (1, 3, 5, 8, 32, 100):
+            for s in range(0, S + 2):
+                assert lib.dllm_transfer_quota(L, S, s) == oracle.transfer_quota(L, S, s), (L, S, s)
+    assert lib.dllm_transfer_quota(0, 4, 0) == -1
+    assert lib.dllm_transfer_quota(4, 0, 0) == -1
+    assert lib.dllm_transfer_quota(4, 4, -1) == -1
+
+
+def test_step_quota_validation():
+    lib = dllm.load()
+    assert lib.dllm_step_quota(ctypes.byref(_args()), None, None) == -1
+    assert lib.dllm_step_quota(ctypes.byref(_args(L=0)), ctypes.c_void_p(0x20000), None) == -1
+    assert lib.dllm_step_quota(ctypes.byref(_args(ldv=20)), ctypes.c_void_p(0x20000), None) == -2
+    assert lib.dllm_step_quota(ctypes.byref(_args(B=0)), ctypes.c_void_p(0x20000), None) == 0

@@ -17,8 +17,9 @@ from oracle.loop import OracleLoop
 pytestmark = pytest.mark.gpu
 
 
-def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv):
-    """Logits [A*L, ldv] for the masked rows, with decision margins."""
+def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv, quota_of_row=None):
+    """Logits [A*L, ldv] for the masked rows, with decision margins (at the
+    threshold and fallback, or at the quota boundary)."""
     out = np.full((max(A * L, 1), ldv), synth.POISON_BITS, dtype=np.uint16)
     if not rows:
         return out
@@ -33,10 +34,18 @@ def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv):
         by_row = {}
         for k, r in enumerate(rows):
             t = float(np.float32(thr_of_row[r[0] // L]))
-            if abs(conf[k] - t) < MARGIN:
+            if quota_of_row is None and abs(conf[k] - t) < MARGIN:
                 bad.add(k)
             by_row.setdefault(r[0] // L, []).append(k)
         for i, ks in by_row.items():
+            if quota_of_row is not None:
+                q = int(quota_of_row[i])
+                c = conf[ks]
+                if 0 < q < len(ks):
+                    order = np.argsort(-c, kind="stable")
+                    if c[order[q - 1]] - c[order[q]] < MARGIN:
+                        bad.add(ks[order[q]])
+                continue
             t = float(np.float32(thr_of_row[i]))
             c = conf[ks]
             if not (c > t).any() and len(ks) > 1:
@@ -50,15 +59,15 @@ def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv):
     raise AssertionError("no margin after 50 redraws")
 
 
-def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000):
+def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None):
     import torch
     from denoise_step_token_gb300.loop import DeviceLoop
     reqs = synth.make_loop_requests(cfg, seed)
     R, L, V = cfg.R, cfg.L, cfg.V
     prompts = [reqs.prompt_tokens[reqs.prompt_off[r]:reqs.prompt_off[r + 1]] for r in range(R)]
-    ol = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode)
+    ol = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode, S=S)
     gl = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V, mask_id=cfg.mask_id,
-                    pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode)
+                    pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode, S=S)
     salts = {}
     trace = []
     while not ol.finished() and ol.iteration < max_iters:
@@ -79,7 +88,7 @@ def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000):
         assert rows_o == gl.masked_rows()
         thr_of_row = np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32)
         logits = _loop_logits(seed, rows_o, len(ol.rid), L, V, cfg.offset_max, cfg.mask_id, thr_of_row, salts,
-                              cfg.row_stride)
+                              cfg.row_stride, ol.quota())
         ref = ol.step_phase(logits[: len(ol.rid) * L])
         done_g, out = gl.step_phase(torch.from_numpy(logits[: len(ol.rid) * L].view(np.int16)).to(device))
         np.testing.assert_array_equal(done_g.astype(np.uint8), ref["done"])
@@ -132,3 +141,11 @@ def test_fdfo_and_sync_agree_and_fdfo_wastes_nothing(dllm, device):
     for r in range(SMALL.R):
         np.testing.assert_array_equal(f.gen[r], s.gen[r])
     assert f.iteration <= s.iteration
+
+
+@pytest.mark.parametrize("S", [8, 32])
+def test_loop_lockstep_fixed_steps(dllm, device, S):
+    """The fixed-steps rule (BlockServe page, section II-E) in the serving
+    loop: every block takes exactly S steps when L >= S."""
+    ol, trace = _lockstep(dllm, device, SMALL, "fdfo", seed=6, S=S)
+    assert ol.iteration == len(trace) > 0

@@ -475,11 +475,11 @@ def _loop_logits(seed, V):
     return fn
 
 
-def _small_loop(mode, R=6, budget=400, thr=0.9, seed=1):
+def _small_loop(mode, R=6, budget=400, thr=0.9, seed=1, S=None):
     cfg = synth.LoopConfig("small", R, 3, 40, 24, 8, 97, budget, thr, 8.0)
     reqs = synth.make_loop_requests(cfg, seed)
     prompts = [reqs.prompt_tokens[reqs.prompt_off[r]:reqs.prompt_off[r + 1]] for r in range(R)]
-    lp = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, cfg.L, cfg.V, cfg.mask_id, cfg.pad_id, budget, mode)
+    lp = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, cfg.L, cfg.V, cfg.mask_id, cfg.pad_id, budget, mode, S=S)
     return lp.run(_loop_logits(seed, cfg.V)), cfg
 
 
@@ -530,3 +530,86 @@ def test_advance_hand_case():
     assert gen[5].tolist() == [1, 2] and gen[6].tolist() == [7, 7] and gen[7].tolist() == [8, 8, 4, 5]
     assert ids[0].tolist() == [mask, mask] and np.isnan(cs[0]).all()      # next block starts masked
     assert ids[1].tolist() == [mask, 3] and ids[2].tolist() == [4, 5]     # untouched / evicted as is
+
+
+# --------------------------------------------------------------------------
+# Fixed-steps transfer rule (BlockServe page, section II-E)
+# --------------------------------------------------------------------------
+def test_transfer_quota_schedule_closed_form():
+    # spreading L over S steps: the S quotas sum to L, take the two values
+    # floor(L/S) and ceil(L/S), never increase, and the larger one occurs
+    # L mod S times
+    for L in range(1, 70):
+        for S in range(1, 70):
+            qs = [oracle.transfer_quota(L, S, s) for s in range(S)]
+            assert sum(qs) == L
+            assert set(qs) <= {L // S, -(-L // S)}
+            assert all(a >= b for a, b in zip(qs, qs[1:]))
+            assert sum(1 for q in qs if q == L // S + 1) == (L % S if L % S else 0)
+    # the pages' setting L = S = 32: one token per step
+    assert [oracle.transfer_quota(32, 32, s) for s in range(32)] == [1] * 32
+    assert [oracle.transfer_quota(32, 5, s) for s in range(5)] == [7, 7, 6, 6, 6]
+    assert [oracle.transfer_quota(4, 8, s) for s in range(8)] == [1, 1, 1, 1, 0, 0, 0, 0]
+    assert oracle.transfer_quota(32, 32, 40) == 32
+    with pytest.raises(ValueError):
+        oracle.transfer_quota(0, 4, 0)
+
+
+def test_select_quota_against_lexsort():
+    # the q most confident masked positions, ties to the lower position, is
+    # the first q of a lexicographic sort on (-conf, position)
+    rng = np.random.default_rng(8)
+    for _ in range(400):
+        L = int(rng.integers(1, 13))
+        masked = rng.random(L) < 0.7
+        conf = np.round(rng.random(L), 1)          # many ties
+        q = int(rng.integers(-1, L + 3))
+        order = [j for j in np.lexsort((np.arange(L), -conf)) if masked[j]]
+        want = np.zeros(L, dtype=bool)
+        want[order[: max(q, 0)]] = True
+        assert np.array_equal(oracle.select_quota(masked, conf, q), want)
+
+
+def test_select_quota_one_is_the_threshold_fallback():
+    # with every confidence in (0, 1], a threshold of 1 passes nothing, so the
+    # threshold rule reduces to its fallback: the single most confident
+    # masked position -- the fixed-steps rule with q = 1
+    rng = np.random.default_rng(9)
+    for _ in range(300):
+        L = int(rng.integers(1, 10))
+        masked = rng.random(L) < 0.6
+        conf = np.round(rng.uniform(0.01, 1.0, L), 2)
+        assert np.array_equal(oracle.select_quota(masked, conf, 1), oracle.select_positions(masked, conf, 1.0))
+
+
+def test_step_quota_extremes():
+    cfg = synth.StepConfig("q", 3, 8, 50, 6.0, "fraction", (0.5,))
+    inp = synth.make_step_state(cfg, 4)
+    rows = np.flatnonzero(inp.masked.reshape(-1))
+    logits = np.full((cfg.B * cfg.L, cfg.row_stride), synth.POISON_BITS, dtype=np.uint16)
+    synth.fill_logits_rows(logits, cfg.V, rows, synth.step_row_keys(inp, rows), cfg.offset_max, cfg.mask_id)
+    allq = oracle.step(logits, cfg.V, inp.input_ids, inp.thr, inp.conf_state, cfg.mask_id,
+                       quota=np.full(cfg.B, cfg.L))
+    assert (allq["done"] == 1).all() and np.array_equal(allq["n_new"], inp.masked.sum(axis=1))
+    none = oracle.step(logits, cfg.V, inp.input_ids, inp.thr, inp.conf_state, cfg.mask_id,
+                       quota=np.zeros(cfg.B, dtype=int))
+    assert np.array_equal(none["input_ids"], inp.input_ids) and (none["n_new"] == 0).all()
+    # tokens written are the argmax tokens, confidences recorded at unmask time
+    one = oracle.step(logits, cfg.V, inp.input_ids, inp.thr, inp.conf_state, cfg.mask_id,
+                      quota=np.ones(cfg.B, dtype=int))
+    chg = one["input_ids"] != inp.input_ids
+    assert np.array_equal(one["input_ids"][chg], one["tok"][chg])
+    assert np.array_equal(one["conf_state"][chg], one["conf"][chg])
+    assert np.array_equal(one["n_new"], inp.masked.any(axis=1).astype(int))
+
+
+@pytest.mark.parametrize("S", [1, 3, 4, 8])
+def test_loop_fixed_steps_blocks_take_S_steps(S):
+    # BlockServe page, section II-E: with the per-step quota spreading L over
+    # S steps, every block of every request is done after exactly S steps
+    # (L = 8 >= S), so a request admitted at iteration a leaves at a + K S - 1
+    f, cfg = _small_loop("fdfo", S=S)
+    assert f.finished()
+    for r in range(cfg.R):
+        assert f.finish_iter[r] - f.admit_iter[r] + 1 == cfg.K * S
+        assert not (f.gen[r] == cfg.mask_id).any()
