@@ -50,6 +50,7 @@ WORKLOADS = {
     "stress": "large_batch_stress_step",
     "tiny": "tiny_step",
     "blockserve": "blockserve_mixed_state_loop",
+    "blockserve_small": "blockserve_mixed_state_loop_small_batch",
 }
 LOOP_K = 8                     # blocks per request (gen 256 / L 32)
 BUDGET = 1 << 20               # token budget of eq. (1)
@@ -87,7 +88,7 @@ FIXED_STEPS_S = 32   # the pages' S = 32 denoising steps per block of L = 32
 def step_config_name(name):
     """Step configuration behind a workload name (the fixed-steps workload
     runs the Dream-shaped batch under the fixed-steps rule)."""
-    return "dream" if name in ("blockserve", "dream_fixed_steps") else name
+    return "dream" if name in synth.LOOP_CONFIGS or name == "dream_fixed_steps" else name
 
 
 def make_workload(seed, name="dream"):
@@ -562,7 +563,8 @@ def run_reference(args, rank, world):
 # BlockServe mixed-state loop: 256 requests served to completion
 # ---------------------------------------------------------------------------
 def run_loop_bench(args, rank, world, local_rank):
-    """FDFO serving loop over the full BlockServe-shaped queue.  The timed
+    """FDFO serving loop over a BlockServe-shaped queue, with the in-place
+    re-loop, and the same queue again without it for comparison.  The timed
     part of each iteration is the hot path (admission, refill, pack, step,
     done readback, advance, compaction); producing the step's logits (the
     model forward's job) is not timed: each masked position's row is
@@ -570,12 +572,40 @@ def run_loop_bench(args, rank, world, local_rank):
     of (request, block, step, position)."""
     import torch
     import denoise_step_token_gb300 as dllm
-    from denoise_step_token_gb300.loop import DeviceLoop
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     dllm.load()
-    lcfg = synth.LOOP_CONFIGS["blockserve"]
-    seed = 2000 + rank
+    lcfg = synth.LOOP_CONFIGS[args.workload]
+    on = serve_queue(lcfg, 2000 + rank, device, reloop=True)
+    off = serve_queue(lcfg, 2000 + rank, device, reloop=False)
+    secs = on["secs"]
+    out = {
+        "metric": METRIC, "value": on["masked"] / secs, "unit": UNIT, "n_gpus": world, "steps": on["iters"],
+        "warmup": 0, "ms_per_step": secs * 1e3 / on["iters"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload], "requests": lcfg.R, "prompt_len": [lcfg.p_lo, lcfg.p_hi],
+                   "gen": lcfg.gen, "L": lcfg.L, "V": lcfg.V, "token_budget": lcfg.budget,
+                   "threshold": lcfg.threshold, "mode": "fdfo", "in_place_reloop": True,
+                   "timed": "admit+refill+pack+step+done readback+advance+compact per iteration"},
+        "loop": {"iterations": on["iters"], "timed_s": secs, "masked_positions": on["masked"],
+                 "mean_active_rows": on["mean_A"],
+                 "logits_gbs": on["masked"] * lcfg.V * 2 / secs / 1e9,
+                 "step_call_ms_total": on["step_ms"], "step_call_share": on["step_ms"] / 1e3 / secs,
+                 "reloop_iterations": on["reloops"]},
+        "without_reloop": {"value": off["masked"] / off["secs"], "timed_s": off["secs"],
+                           "iterations": off["iters"], "ms_per_step": off["secs"] * 1e3 / off["iters"]},
+    }
+    assert on["iters"] == off["iters"] and on["masked"] == off["masked"]
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+def serve_queue(lcfg, seed, device, reloop):
+    """Serve one generated queue to completion; returns the timed seconds,
+    iterations, masked positions, step-call milliseconds and re-loops."""
+    import torch
+    from denoise_step_token_gb300.loop import DeviceLoop
     reqs = synth.make_loop_requests(lcfg, seed)
     L, V, ldv = lcfg.L, lcfg.V, lcfg.row_stride
     pool_rows = 4096
@@ -584,13 +614,14 @@ def run_loop_bench(args, rank, world, local_rank):
     synth.fill_logits_rows(pool_h, V, np.arange(pool_rows), keys, lcfg.offset_max, lcfg.mask_id)
     pool = torch.from_numpy(pool_h.view(np.int16)).to(device)
     loop = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V,
-                      mask_id=lcfg.mask_id, pad_id=lcfg.pad_id, budget=lcfg.budget, device=device, mode="fdfo")
+                      mask_id=lcfg.mask_id, pad_id=lcfg.pad_id, budget=lcfg.budget, device=device, mode="fdfo",
+                      reloop=reloop)
     logits = torch.empty((lcfg.R * L, ldv), dtype=torch.int16, device=device)
     ev = []
     step_ms = []
+    active = []
     masked_total = 0
     iters = 0
-    pack_plan_s = 0.0
     while not loop.finished():
         # timed: admission (host) and refill
         torch.cuda.synchronize()
@@ -612,6 +643,7 @@ def run_loop_bench(args, rank, world, local_rank):
         torch.cuda.synchronize()
         t1 = time.perf_counter()
         loop.pack_phase()
+        active.append(loop.A)
         e0.record()
         done, _ = loop.step_phase(logits[: loop.A * L])
         e1.record()
@@ -622,21 +654,8 @@ def run_loop_bench(args, rank, world, local_rank):
         step_ms.append(e0.elapsed_time(e1))
         iters += 1
         masked_total += len(rows)
-    secs = sum(ev)
-    out = {
-        "metric": METRIC, "value": masked_total / secs, "unit": UNIT, "n_gpus": world, "steps": iters,
-        "warmup": 0, "ms_per_step": secs * 1e3 / iters, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOADS["blockserve"], "requests": lcfg.R, "prompt_len": [lcfg.p_lo, lcfg.p_hi],
-                   "gen": lcfg.gen, "L": L, "V": V, "token_budget": lcfg.budget, "threshold": lcfg.threshold,
-                   "mode": "fdfo", "timed": "admit+refill+pack+step+done readback+advance+compact per iteration"},
-        "loop": {"iterations": iters, "timed_s": secs, "masked_positions": masked_total,
-                 "logits_gbs": masked_total * V * 2 / secs / 1e9,
-                 "step_call_ms_total": sum(step_ms), "step_call_share": sum(step_ms) / 1e3 / secs},
-    }
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    return 0
+    return {"secs": sum(ev), "iters": iters, "masked": masked_total, "step_ms": sum(step_ms),
+            "reloops": loop.reloops, "mean_A": float(np.mean(active)) if active else 0.0}
 
 
 def main():
@@ -660,7 +679,7 @@ def main():
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return 0
 
-    if args.workload == "blockserve":
+    if args.workload in synth.LOOP_CONFIGS:
         return run_loop_bench(args, rank, world, local_rank)
 
     dist = None

@@ -102,6 +102,7 @@ _SIGNATURES = {
     "dllm_pack_plan": (ctypes.c_int, [_i32, _p, _p, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "dllm_admit": (ctypes.c_int, [_i32, _p, _i32, _p, _p, _i32, _i64, _p, ctypes.POINTER(_i32)]),
     "dllm_pack": (ctypes.c_int, [ctypes.POINTER(PackArgs), _p]),
+    "dllm_pack_block": (ctypes.c_int, [ctypes.POINTER(PackArgs), _p]),
     "dllm_advance": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), _p]),
     "dllm_compact_workspace_size": (_sz, [_i32, _i32, _p]),
     "dllm_compact": (ctypes.c_int, [ctypes.POINTER(CompactArgs), _p]),
@@ -383,6 +384,17 @@ def pack(p, b, rid, prompt_off, prompt_tokens, gen_tokens, block_ids, *, L, W, p
                  pos=_ptr(out.get("pos")), pad=_ptr(out.get("pad")), blk_start=_ptr(out.get("blk_start")))
     _check("dllm_pack", load().dllm_pack(ctypes.byref(a), _stream(dev)))
     return out
+
+
+def pack_block(block_ids, box_ids, *, L, W):
+    """dllm_pack_block: rewrite the active-block columns [W - L, W) of a
+    packed box ``box_ids`` [A, W] from ``block_ids`` [A, L] (the in-place
+    re-loop's update: nothing else in the box changed)."""
+    dev = _require_cuda(block_ids, box_ids)
+    A = block_ids.shape[0]
+    a = PackArgs(A=A, L=L, W=W, block_ids=_ptr(block_ids), ids=_ptr(box_ids))
+    _check("dllm_pack_block", load().dllm_pack_block(ctypes.byref(a), _stream(dev)))
+    return box_ids
 
 
 def advance(adv, rid, K, b, input_ids, conf_state, gen_tokens, *, mask_id, evict=None):

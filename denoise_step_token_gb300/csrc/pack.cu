@@ -407,6 +407,39 @@ extern "C" int dllm_pack(const dllm_pack_args* a, void* stream) {
     return DLLM_OK;
 }
 
+// ---------------------------------------------------------------------------
+// dllm_pack_block: rewrite the active-block columns [W - L, W) of a packed
+// box from the rows' current blocks (FDFO page, "工程设计四": with no block
+// completed, the next step runs on the same batch).  One thread per token.
+// ---------------------------------------------------------------------------
+namespace dllm {
+namespace {
+
+__global__ void __launch_bounds__(256) pack_block_kernel(int A, int L, int W, const int* __restrict__ block_ids,
+                                                         int* __restrict__ ids) {
+    const long long n = (long long)A * L;
+    for (long long t = blockIdx.x * 256ll + threadIdx.x; t < n; t += (long long)gridDim.x * 256) {
+        const int i = (int)(t / L), j = (int)(t - (long long)i * L);
+        ids[(long long)i * W + (W - L) + j] = block_ids[t];
+    }
+}
+
+}  // namespace
+}  // namespace dllm
+
+extern "C" int dllm_pack_block(const dllm_pack_args* a, void* stream) {
+    if (!a || a->A < 0 || a->L < 1) return DLLM_ERR_INVAL;
+    if (a->A == 0) return DLLM_OK;
+    if (a->W < a->L || !a->block_ids || !a->ids) return DLLM_ERR_INVAL;
+    const long long total = (long long)a->A * a->L;
+    const int sms = sm_count();
+    long long blocks = (total + 255) / 256;
+    blocks = std::min<long long>(blocks, (long long)std::max(sms, 1) * 8);
+    pack_block_kernel<<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(a->A, a->L, a->W, a->block_ids, a->ids);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    return DLLM_OK;
+}
+
 extern "C" int dllm_advance(const dllm_advance_args* a, void* stream) {
     if (!a || a->A < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->ld_gen < 0) return DLLM_ERR_INVAL;
     if (a->A == 0) return DLLM_OK;

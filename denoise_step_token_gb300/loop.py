@@ -19,19 +19,31 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import admit, advance, compact, pack, pack_plan, refill, step, transfer_quota
+from . import admit, advance, compact, pack, pack_block, pack_plan, refill, step, transfer_quota
 
 
 class DeviceLoop:
     """One pending queue served to completion on one device.  ``S``: None
     for the threshold rule, else the fixed-steps rule with S steps per block
-    (BlockServe page, section II-E)."""
+    (BlockServe page, section II-E).
+
+    ``reloop``: the in-place re-loop of the FDFO page, section "工程设计四"
+    (#27877): after a step in which no row advanced, the next step runs on
+    the same batch.  Nothing was committed or evicted, so admission would
+    admit nothing (it stopped at the first candidate the budget rejects and
+    neither the active set nor its widths changed), advance and compaction
+    are no-ops, and the box differs only in its active-block columns: those
+    phases are skipped and ``dllm_pack_block`` refreshes the block columns.
+    The trace is identical to the loop without re-loop."""
 
     def __init__(self, p, K, prompt_off, prompt_tokens, thr, *, L, V, mask_id, pad_id, budget, device,
-                 mode="fdfo", capacity=None, features=True, S=None):
+                 mode="fdfo", capacity=None, features=True, S=None, reloop=False):
         import torch
         assert mode in ("fdfo", "sync")
         self.S = None if S is None else int(S)
+        self.reloop = bool(reloop)
+        self.in_place = False        # the last step advanced no row: re-loop on the same batch
+        self.reloops = 0             # iterations that ran in place
         self.torch = torch
         self.L, self.V, self.mask_id, self.pad_id = int(L), int(V), int(mask_id), int(pad_id)
         self.budget, self.mode, self.device, self.features = int(budget), mode, device, features
@@ -68,7 +80,7 @@ class DeviceLoop:
     # -- admission and refill (Algorithm 1, "admit") -------------------------
     def admit_phase(self):
         torch = self.torch
-        if not self.pending:
+        if not self.pending or self.in_place:
             return []
         pend_p = self.p_all[self.pending]
         picked = admit(pend_p, self.p_all[self.rid_h], self.b_h, self.L, self.budget)
@@ -94,6 +106,10 @@ class DeviceLoop:
     # -- the box of eq. (1) (BlockServe section II-E) -------------------------
     def pack_phase(self):
         A = self.A
+        if self.in_place and self.box is not None:
+            self.reloops += 1
+            pack_block(self.ids[:A], self.box["ids"], L=self.L, W=self.W)
+            return self.box
         self.W, self.cost = pack_plan(self.p_all[self.rid_h], self.b_h, self.L)
         if A == 0:
             self.box = None
@@ -125,6 +141,14 @@ class DeviceLoop:
             adv = done if done.all() else np.zeros_like(done)
         # a row stepped unless its block was already done and waiting
         stepped = ~self.wait_h
+        if self.reloop and not adv.any():
+            # nothing commits: no advance, no compaction, same batch next step
+            self.s_h = self.s_h + stepped.astype(np.int32)
+            self.wait_h = done & ~adv
+            self.in_place = True
+            self.iteration += 1
+            return np.zeros(A, dtype=bool), None
+        self.in_place = False
         adv_d = torch.as_tensor(adv.astype(np.uint8)).to(self.device)
         evict_d = advance(adv_d, self.rid[:A], self.K[:A], self.b[:A], self.ids[:A], self.cs[:A], self.gen,
                           mask_id=self.mask_id)

@@ -277,6 +277,17 @@ typedef struct dllm_pack_args {
 
 int dllm_pack(const dllm_pack_args* args, void* stream);
 
+/* The in-place re-loop's box update (FDFO page, section "工程设计四",
+ * #27877: when no block completed in a round, the next forward and step run
+ * on the same batch without a return to the scheduler).  With no block
+ * committed, no row was admitted or evicted and every width is unchanged, so
+ * the box differs from the last dllm_pack only in the active blocks: this
+ * rewrites ids[i][W - L + j] = block_ids[i][j] for i < A, j < L and leaves
+ * every other column and attn / pos / pad / blk_start as they are.  Reads
+ * args->A, L, W, block_ids and ids only.  Errors: DLLM_ERR_INVAL (A < 0,
+ * L < 1, W < L with A > 0, NULL block_ids or ids). */
+int dllm_pack_block(const dllm_pack_args* args, void* stream);
+
 /* ======================================================================
  * dllm_advance -- commit finished blocks (BlockServe Algorithm 1: update
  * r_i's outputs with its block, b_i <- b_i + 1, evict when b_i >= K_i;

@@ -270,6 +270,9 @@ STEP_CONFIGS = {
 
 LOOP_CONFIGS = {
     "blockserve": LoopConfig("blockserve", 256, 64, 1024, 256, 32, 126464, 1 << 20, 0.9, 12.0),
+    # the same queue shape served at a small batch: the budget of eq. (1)
+    # holds about four widest rows
+    "blockserve_small": LoopConfig("blockserve_small", 64, 64, 1024, 256, 32, 126464, 5120, 0.9, 12.0),
 }
 
 

@@ -59,7 +59,7 @@ def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv, q
     raise AssertionError("no margin after 50 redraws")
 
 
-def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None):
+def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None, reloop=False):
     import torch
     from denoise_step_token_gb300.loop import DeviceLoop
     reqs = synth.make_loop_requests(cfg, seed)
@@ -67,7 +67,7 @@ def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None):
     prompts = [reqs.prompt_tokens[reqs.prompt_off[r]:reqs.prompt_off[r + 1]] for r in range(R)]
     ol = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode, S=S)
     gl = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V, mask_id=cfg.mask_id,
-                    pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode, S=S)
+                    pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode, S=S, reloop=reloop)
     salts = {}
     trace = []
     while not ol.finished() and ol.iteration < max_iters:
@@ -99,7 +99,10 @@ def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None):
         ev_o, _, _, A_o = ol.finish_phase(ref["done"])
         ev_g, A_out = gl.finish_phase(done_g)
         np.testing.assert_array_equal(ev_g, ev_o)
-        assert int(A_out.cpu().numpy()[0]) == A_o == gl.A
+        if A_out is None:        # re-loop: nothing advanced, nothing ran
+            assert reloop and A_o == gl.A and not ev_o.any()
+        else:
+            assert int(A_out.cpu().numpy()[0]) == A_o == gl.A
         assert list(gl.rid_h) == ol.rid and list(gl.b_h) == ol.b
         np.testing.assert_array_equal(gl.rid[: gl.A].cpu().numpy(), ol.rid)
         np.testing.assert_array_equal(gl.b[: gl.A].cpu().numpy(), ol.b)
@@ -109,6 +112,8 @@ def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None):
     for r in range(R):
         np.testing.assert_array_equal(gen[r][: reqs.K[r] * L], ol.gen[r])
     assert dllm.get_device_error(device) == 0
+    if reloop:
+        trace.append(("reloops", gl.reloops))
     return ol, trace
 
 
@@ -149,3 +154,17 @@ def test_loop_lockstep_fixed_steps(dllm, device, S):
     loop: every block takes exactly S steps when L >= S."""
     ol, trace = _lockstep(dllm, device, SMALL, "fdfo", seed=6, S=S)
     assert ol.iteration == len(trace) > 0
+
+
+@pytest.mark.parametrize("mode", ["fdfo", "sync"])
+def test_loop_in_place_reloop_matches_oracle(dllm, device, mode):
+    """FDFO page, section "工程设计四" (#27877): after a step in which no
+    block completed, the loop steps the same batch again (no admission,
+    pack, advance or compaction; the box's block columns refreshed in
+    place).  The whole trace -- admissions, boxes, steps, evictions, tokens
+    -- still equals the oracle loop's, and some iterations did re-loop."""
+    small_batch = synth.LoopConfig("small_batch", 16, 3, 60, 24, 8, 4099, 220, 0.9, 10.0)
+    ol, trace = _lockstep(dllm, device, small_batch, mode, seed=9, reloop=True)
+    reloops = trace.pop()[1]
+    assert ol.iteration == len(trace) > 0
+    assert 0 < reloops < ol.iteration
