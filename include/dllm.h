@@ -199,7 +199,7 @@ int32_t dllm_transfer_quota(int32_t L, int32_t S, int32_t s);
  *     streams, other host threads without ordering) race and corrupt each
  *     other.  Order them on one stream.
  *   - Shapes whose workspace exceeds the buffer (dllm_step_workspace_size
- *     layout, e.g. B * L * ceil(V / 8192) above roughly 700k) return
+ *     layout; for V near 150k, B * L * ceil(V / 8192) above about 480k) return
  *     DLLM_ERR_SCRATCH_LIMIT and launch nothing. */
 int dllm_step_noalloc(const dllm_step_args* args, void* stream);
 
