@@ -596,9 +596,35 @@ def run_loop_bench(args, rank, world, local_rank):
                            "iterations": off["iters"], "ms_per_step": off["secs"] * 1e3 / off["iters"]},
     }
     assert on["iters"] == off["iters"] and on["masked"] == off["masked"]
+    out["threshold_control"] = time_threshold_control(lcfg, seed=3000 + rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
+
+
+def time_threshold_control(lcfg, seed, A=256, reps=200):
+    """Host cost of one DiLaServe threshold decision (stub step prediction,
+    Algorithm 2, Algorithm 1) for a batch of A active requests over the five
+    candidate thresholds, on this machine's host CPU."""
+    from denoise_step_token_gb300.control import ThresholdController
+    rng = np.random.default_rng(seed)
+    L, K = lcfg.L, lcfg.K
+    q = np.sort(rng.uniform(0.3, 1.0, size=(A, 4)).astype(np.float32), axis=1)
+    feats = np.stack([q[:, 0], q[:, 1], q[:, 2], q.mean(axis=1), q[:, 3], rng.random(A)], axis=1).astype(np.float32)
+    feats[rng.random(A) < 0.1, :5] = np.nan
+    masked = rng.integers(0, L + 1, size=A)
+    left = rng.integers(0, K, size=A)
+    total = rng.integers(lcfg.p_lo, lcfg.p_hi + 1, size=A) + lcfg.gen
+    elapsed = rng.uniform(0.0, 1.0, size=A)
+    ctl = ThresholdController([0.5, 0.6, 0.7, 0.8, 0.9], L=L, slo_s=2.0, tokens_per_s=1.0e7,
+                              step_latency_s=lambda n: 0.0006)
+    ctl.choose(feats, masked, left, total, elapsed)
+    t = time.perf_counter()
+    for _ in range(reps):
+        thr, choice, cap = ctl.choose(feats, masked, left, total, elapsed)
+    us = (time.perf_counter() - t) / reps * 1e6
+    return {"requests": A, "candidates": 5, "us_per_decision": us,
+            "mean_threshold": float(thr.mean()), "capped_requests": int((cap < 4).sum())}
 
 
 def serve_queue(lcfg, seed, device, reloop):

@@ -34,14 +34,26 @@ class DeviceLoop:
     neither the active set nor its widths changed), advance and compaction
     are no-ops, and the box differs only in its active-block columns: those
     phases are skipped and ``dllm_pack_block`` refreshes the block columns.
-    The trace is identical to the loop without re-loop."""
+    The trace is identical to the loop without re-loop.
+
+    ``controller``: a ``control.ThresholdController`` (DiLaServe review,
+    section 3.2).  Before every step it picks each active request's
+    threshold from the block features of the request's last step (NaN for a
+    fresh block), the positions still masked, the blocks left, the request's
+    total tokens and its time since admission on a modelled clock that
+    advances by the controller's step latency at the current batch size."""
 
     def __init__(self, p, K, prompt_off, prompt_tokens, thr, *, L, V, mask_id, pad_id, budget, device,
-                 mode="fdfo", capacity=None, features=True, S=None, reloop=False):
+                 mode="fdfo", capacity=None, features=True, S=None, reloop=False, controller=None):
         import torch
         assert mode in ("fdfo", "sync")
         self.S = None if S is None else int(S)
         self.reloop = bool(reloop)
+        self.controller = controller
+        self.now = 0.0                                  # modelled clock (controller)
+        self.admit_s = np.zeros(0)                      # admission time per active row
+        self.feat_h = np.zeros((0, 6), dtype=np.float32)   # last block features per active row
+        self.thr_log = []                               # thresholds the controller chose, per step
         self.in_place = False        # the last step advanced no row: re-loop on the same batch
         self.reloops = 0             # iterations that ran in place
         self.torch = torch
@@ -101,6 +113,8 @@ class DeviceLoop:
         self.b_h = np.concatenate([self.b_h, np.zeros(n, dtype=np.int32)])
         self.s_h = np.concatenate([self.s_h, np.zeros(n, dtype=np.int32)])
         self.wait_h = np.concatenate([self.wait_h, np.zeros(n, dtype=bool)])
+        self.admit_s = np.concatenate([self.admit_s, np.full(n, self.now)])
+        self.feat_h = np.concatenate([self.feat_h, np.full((n, 6), np.nan, dtype=np.float32)])
         return new
 
     # -- the box of eq. (1) (BlockServe section II-E) -------------------------
@@ -119,8 +133,27 @@ class DeviceLoop:
         return self.box
 
     # -- one denoise step -------------------------------------------------------
-    def step_phase(self, logits):
+    def control_inputs(self):
+        """The controller's inputs for the active rows: features, masked
+        positions, blocks left, total tokens, time since admission."""
+        L = self.L
+        f = self.feat_h
+        frac = np.where(np.isnan(f[:, 0]), 0.0, f[:, 5])
+        masked = (L - np.rint(frac * L)).astype(np.int32)
+        K = self.K_all[self.rid_h]
+        left = (K - self.b_h - 1).astype(np.int32)
+        total = (self.p_all[self.rid_h] + K * L).astype(np.float64)
+        return f, masked, left, total, self.now - self.admit_s
+
+    def step_phase(self, logits, thr=None):
+        """One step on the active rows.  ``thr``: float32 [A] thresholds for
+        this step (else the controller's, else the requests' own)."""
         A = self.A
+        if thr is None and self.controller is not None and A:
+            thr, _, _ = self.controller.choose(*self.control_inputs())
+            self.thr_log.append(thr.copy())
+        if thr is not None and A:
+            self.thr[:A].copy_(self.torch.from_numpy(np.ascontiguousarray(thr, dtype=np.float32)))
         quota = None
         if self.S is not None:
             q = np.array([transfer_quota(self.L, self.S, int(s)) for s in self.s_h], dtype=np.int32)
@@ -129,6 +162,9 @@ class DeviceLoop:
                    feats=self.features, quota=quota)
         done = out["done"].cpu().numpy().astype(bool)     # the per-step readback
         self.last = out
+        if self.controller is not None:
+            self.feat_h = out["feats"].cpu().numpy().copy()
+            self.now += float(self.controller.step_latency_s(A))
         return done, out
 
     # -- commit finished blocks, evict, compact ----------------------------------
@@ -162,6 +198,10 @@ class DeviceLoop:
         keep = ~evict
         wait = done & ~adv
         self.rid_h, self.b_h, self.s_h, self.wait_h = self.rid_h[keep], b[keep], s[keep], wait[keep]
+        if self.feat_h.shape[0] == A:
+            self.feat_h[adv] = np.nan                     # a fresh block: nothing unmasked yet
+            self.feat_h = self.feat_h[keep]
+        self.admit_s = self.admit_s[keep]
         self.A = int(keep.sum())
         self.iteration += 1
         return evict, A_out

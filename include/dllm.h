@@ -212,6 +212,46 @@ int dllm_features(int32_t B, int32_t L, int32_t mask_id, const int32_t* input_id
                   const float* conf_state, float* feats, void* stream);
 
 /* ======================================================================
+ * Confidence-threshold control (host functions; DiLaServe review, section
+ * 3.2, "Confidence Threshold Controller").  Thresholds are indexed by their
+ * position in an ascending candidate list (e.g. {0.5, 0.6, 0.7, 0.8, 0.9},
+ * section 4.1).  All arrays are host memory, row-major [R][T].
+ * ====================================================================== */
+
+/* A stand-in for the review's step predictor (item ③: a gradient-boosted
+ * model over 11 features, trained offline -- not built here).  For request
+ * i at candidate threshold cand[k]: P = P(confidence > cand[k]) read off
+ * the block features feats[i][0..5] (dllm_step's output: min, q25, median,
+ * avg, q75, unmasked fraction) as the piecewise-linear distribution through
+ * (min, 0), (q25, .25), (median, .5), (q75, .75), (1, 1), or 1 - cand[k]
+ * when no position is unmasked yet (NaN features); a step then unmasks
+ * max(1, floor(P m)) of the m positions still masked.  steps_out[i][k] =
+ * steps to clear masked[i] positions + blocks_left[i] * steps to clear L.
+ * Double precision, no contraction.  DLLM_ERR_INVAL for R < 0, T < 1,
+ * L < 1, masked[i] outside [0, L], blocks_left[i] < 0 or a NULL array. */
+int dllm_predict_steps_stub(int32_t R, int32_t T, const double* cand, int32_t L, const float* feats,
+                            const int32_t* masked, const int32_t* blocks_left, double* steps_out);
+
+/* Algorithm 2 (item ②, adaptive load control).  load[i][k]: request i's
+ * load at threshold k (total tokens x predicted remaining steps); requests
+ * in arrival order; capacity = tokens per second x SLO.  For each request in
+ * turn, thresholds are tried from the highest down; threshold k is dropped
+ * while committed + load[i][k] + rest[i] > capacity (rest[i] = the later
+ * requests at their lowest threshold, summed from the back: rest[R-1] = 0,
+ * rest[i] = load[i+1][0] + rest[i+1]), and the
+ * first that fits becomes max_allowed[i] (the lowest is kept if none fits);
+ * committed then adds load[i][max_allowed[i]].  Every threshold at or below
+ * max_allowed[i] stays allowed. */
+int dllm_load_control(int32_t R, int32_t T, const double* load, double capacity, int32_t* max_allowed);
+
+/* Algorithm 1 (item ①, SLO-aware threshold choice).  choice[i] = the
+ * highest k <= max_allowed[i] (T - 1 when max_allowed is NULL) with
+ * rem_steps[i][k] * step_latency[i] <= slo_left[i], else 0 (the fastest).
+ * DLLM_ERR_INVAL for a max_allowed entry outside [0, T). */
+int dllm_slo_thresholds(int32_t R, int32_t T, const double* rem_steps, const double* step_latency,
+                        const double* slo_left, const int32_t* max_allowed, int32_t* choice);
+
+/* ======================================================================
  * Bounding-box planning and admission (host functions).
  *
  * BlockServe page, section II-D, eq. (1):

@@ -123,8 +123,11 @@ class OracleLoop:
         return np.array([transfer_quota(self.L, self.S, s) for s in self.s], dtype=np.int64)
 
     # -- one denoise step (FDFO page, "工程设计一") -----------------------------
-    def step_phase(self, logits_bits):
-        thr = np.array([self.thr_all[r] for r in self.rid], dtype=np.float32)
+    def step_phase(self, logits_bits, thr=None):
+        """``thr``: float32 thresholds of the active rows for this step (else
+        each request's own)."""
+        if thr is None:
+            thr = np.array([self.thr_all[r] for r in self.rid], dtype=np.float32)
         res = step(logits_bits, self.V, self.ids, thr, self.cs, self.mask_id, quota=self.quota())
         had_masked = res["masked"].any(axis=1)
         self.ids = res["input_ids"]

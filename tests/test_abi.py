@@ -135,3 +135,45 @@ def test_step_quota_validation():
     assert lib.dllm_step_quota(ctypes.byref(_args(L=0)), ctypes.c_void_p(0x20000), None) == -1
     assert lib.dllm_step_quota(ctypes.byref(_args(ldv=20)), ctypes.c_void_p(0x20000), None) == -2
     assert lib.dllm_step_quota(ctypes.byref(_args(B=0)), ctypes.c_void_p(0x20000), None) == 0
+
+
+def _dptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def test_threshold_control_matches_oracle():
+    """dllm_predict_steps_stub, dllm_load_control and dllm_slo_thresholds
+    (host functions) equal the oracle exactly on random inputs."""
+    from oracle import control as oc
+    lib = dllm.load()
+    rng = np.random.default_rng(15)
+    cand = np.array([0.5, 0.6, 0.7, 0.8, 0.9])
+    T, L = len(cand), 32
+    for trial in range(20):
+        R = int(rng.integers(1, 40))
+        q = np.sort(rng.random((R, 4)).astype(np.float32), axis=1)
+        feats = np.stack([q[:, 0], q[:, 1], q[:, 2], q.mean(axis=1), q[:, 3], rng.random(R)], axis=1).astype(np.float32)
+        feats[rng.random(R) < 0.2, :5] = np.nan
+        masked = rng.integers(0, L + 1, size=R).astype(np.int32)
+        left = rng.integers(0, 8, size=R).astype(np.int32)
+        steps = np.empty((R, T))
+        assert lib.dllm_predict_steps_stub(R, T, _dptr(cand), L, _dptr(feats), _dptr(masked), _dptr(left),
+                                           _dptr(steps)) == 0
+        want = np.array([[oc.predict_steps_stub(t, feats[i], masked[i], left[i], L) for t in cand]
+                         for i in range(R)])
+        np.testing.assert_array_equal(steps, want)
+        load = steps * rng.integers(100, 1300, size=(R, 1))
+        cap = float(rng.uniform(load[:, 0].sum() * 0.8, load[:, -1].sum() * 1.1))
+        keep = np.empty(R, dtype=np.int32)
+        assert lib.dllm_load_control(R, T, _dptr(np.ascontiguousarray(load)), cap, _dptr(keep)) == 0
+        np.testing.assert_array_equal(keep, oc.load_control(load, cap))
+        lat = rng.uniform(0.005, 0.05, size=R)
+        slo = rng.uniform(0.0, 5.0, size=R)
+        choice = np.empty(R, dtype=np.int32)
+        assert lib.dllm_slo_thresholds(R, T, _dptr(steps), _dptr(lat), _dptr(slo), _dptr(keep), _dptr(choice)) == 0
+        np.testing.assert_array_equal(choice, [oc.slo_threshold(steps[i], lat[i], slo[i], keep[i]) for i in range(R)])
+    bad = np.array([7], dtype=np.int32)
+    one = np.ones(T)
+    assert lib.dllm_slo_thresholds(1, T, _dptr(one), _dptr(one[:1]), _dptr(one[:1]), _dptr(bad),
+                                   _dptr(np.empty(1, dtype=np.int32))) == -1
+    assert lib.dllm_load_control(1, 0, None, 1.0, None) == -1

@@ -59,7 +59,7 @@ def _loop_logits(seed, rows, A, L, V, offset, mask_id, thr_of_row, salts, ldv, q
     raise AssertionError("no margin after 50 redraws")
 
 
-def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None, reloop=False):
+def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None, reloop=False, thr_fn=None):
     import torch
     from denoise_step_token_gb300.loop import DeviceLoop
     reqs = synth.make_loop_requests(cfg, seed)
@@ -86,16 +86,23 @@ def _lockstep(dllm, device, cfg, mode, seed, max_iters=10000, S=None, reloop=Fal
             np.testing.assert_array_equal(box_g[k].cpu().numpy(), box_o[k], err_msg=k)
         rows_o = ol.masked_rows()
         assert rows_o == gl.masked_rows()
-        thr_of_row = np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32)
+        thr_step = None if thr_fn is None else thr_fn(ol, new_o)
+        thr_of_row = (np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32) if thr_step is None
+                      else thr_step)
         logits = _loop_logits(seed, rows_o, len(ol.rid), L, V, cfg.offset_max, cfg.mask_id, thr_of_row, salts,
                               cfg.row_stride, ol.quota())
-        ref = ol.step_phase(logits[: len(ol.rid) * L])
-        done_g, out = gl.step_phase(torch.from_numpy(logits[: len(ol.rid) * L].view(np.int16)).to(device))
+        ref = ol.step_phase(logits[: len(ol.rid) * L], thr=thr_step)
+        if thr_fn is not None:
+            thr_fn.after_step(ol, ref)
+        done_g, out = gl.step_phase(torch.from_numpy(logits[: len(ol.rid) * L].view(np.int16)).to(device),
+                                    thr=thr_step)
         np.testing.assert_array_equal(done_g.astype(np.uint8), ref["done"])
         np.testing.assert_array_equal(out["n_new"].cpu().numpy(), ref["n_new"])
         np.testing.assert_array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
         np.testing.assert_array_equal(gl.ids[: gl.A].cpu().numpy(), ref["input_ids"])
         np.testing.assert_allclose(out["feats"].cpu().numpy(), ref["feats"], rtol=0, atol=1e-5, equal_nan=True)
+        if thr_fn is not None:
+            thr_fn.before_finish(ol, ref)
         ev_o, _, _, A_o = ol.finish_phase(ref["done"])
         ev_g, A_out = gl.finish_phase(done_g)
         np.testing.assert_array_equal(ev_g, ev_o)
@@ -168,3 +175,93 @@ def test_loop_in_place_reloop_matches_oracle(dllm, device, mode):
     reloops = trace.pop()[1]
     assert ol.iteration == len(trace) > 0
     assert 0 < reloops < ol.iteration
+
+
+class OracleController:
+    """The threshold controller (DiLaServe review, section 3.2) evaluated on
+    the oracle loop's own features with the oracle's control functions; its
+    thresholds drive both loops, so no oracle input comes from the GPU."""
+
+    def __init__(self, cand, L, slo_s, tokens_per_s, lat_s):
+        self.cand, self.L, self.slo, self.cap, self.lat = np.asarray(cand), L, slo_s, tokens_per_s * slo_s, lat_s
+        self.now, self.admit, self.feats = 0.0, {}, {}
+        self.log = []
+
+    def __call__(self, ol, new):
+        from oracle import control as oc
+        for r in new:
+            self.admit[r] = self.now
+            self.feats[r] = np.full(6, np.nan, dtype=np.float32)
+        L, A = self.L, len(ol.rid)
+        if A == 0:
+            return None
+        steps = np.zeros((A, len(self.cand)))
+        total = np.zeros(A)
+        for i, r in enumerate(ol.rid):
+            f = self.feats[r]
+            m = L if np.isnan(f[0]) else int(L - np.rint(np.float32(f[5]) * L))
+            left = int(ol.K_all[r]) - int(ol.b[i]) - 1
+            steps[i] = [oc.predict_steps_stub(t, f, m, left, L) for t in self.cand]
+            total[i] = float(ol.p_all[r] + ol.K_all[r] * L)
+        caps = oc.load_control(steps * total[:, None], self.cap)
+        thr = np.array([self.cand[oc.slo_threshold(steps[i], self.lat(A), self.slo - (self.now - self.admit[r]),
+                                                     caps[i])] for i, r in enumerate(ol.rid)], dtype=np.float32)
+        self.log.append(thr)
+        return thr
+
+    def after_step(self, ol, ref):
+        for i, r in enumerate(ol.rid):
+            self.feats[r] = ref["feats"][i].astype(np.float32)
+        self.now += self.lat(len(ol.rid))
+
+    def before_finish(self, ol, ref):
+        done = np.asarray(ref["done"], dtype=bool)
+        if ol.mode == "fdfo":
+            for i, r in enumerate(ol.rid):
+                if done[i]:
+                    self.feats[r] = np.full(6, np.nan, dtype=np.float32)
+
+
+def test_loop_lockstep_with_threshold_control(dllm, device):
+    """Per-step thresholds from the DiLaServe controller (Algorithms 1 and
+    2 over the stub predictor) drive the GPU loop and the oracle loop in
+    lockstep; the thresholds change over the run."""
+    ctl = OracleController([0.5, 0.6, 0.7, 0.8, 0.9], SMALL.L, slo_s=0.05, tokens_per_s=2.0e5,
+                           lat_s=lambda A: 0.0005 + 0.00002 * A)
+    ol, trace = _lockstep(dllm, device, SMALL, "fdfo", seed=7, thr_fn=ctl)
+    used = np.concatenate(ctl.log)
+    assert len(np.unique(used)) > 1
+
+
+def test_loop_runs_under_the_library_controller(dllm, device):
+    """DeviceLoop with control.ThresholdController: the queue completes,
+    every threshold is a candidate, and a tight SLO lowers the thresholds."""
+    from denoise_step_token_gb300.control import ThresholdController
+    from denoise_step_token_gb300.loop import DeviceLoop
+    import torch
+    cfg = SMALL
+    reqs = synth.make_loop_requests(cfg, 11)
+    cand = [0.5, 0.6, 0.7, 0.8, 0.9]
+    mean_thr = {}
+    for slo in (10.0, 0.02):
+        ctl = ThresholdController(cand, L=cfg.L, slo_s=slo, tokens_per_s=1e9, step_latency_s=lambda A: 0.001)
+        gl = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=cfg.L, V=cfg.V,
+                        mask_id=cfg.mask_id, pad_id=cfg.pad_id, budget=cfg.budget, device=device, controller=ctl)
+        it = 0
+        while not gl.finished() and it < 5000:
+            gl.admit_phase()
+            gl.pack_phase()
+            rows = gl.masked_rows()
+            logits = _loop_logits(11, rows, gl.A, cfg.L, cfg.V, cfg.offset_max, cfg.mask_id,
+                                  np.full(max(gl.A, 1), 0.5, np.float32), {}, cfg.row_stride)
+            done, _ = gl.step_phase(torch.from_numpy(logits[: gl.A * cfg.L].view(np.int16)).to(device))
+            gl.finish_phase(done)
+            it += 1
+        assert gl.finished()
+        gen = gl.generated()
+        for r in range(cfg.R):
+            assert not (gen[r][: reqs.K[r] * cfg.L] == cfg.mask_id).any()
+        used = np.concatenate(gl.thr_log)
+        assert set(np.unique(used).tolist()) <= set(np.float32(cand).tolist())
+        mean_thr[slo] = float(used.mean())
+    assert mean_thr[0.02] < mean_thr[10.0]

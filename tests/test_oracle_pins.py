@@ -613,3 +613,88 @@ def test_loop_fixed_steps_blocks_take_S_steps(S):
     for r in range(cfg.R):
         assert f.finish_iter[r] - f.admit_iter[r] + 1 == cfg.K * S
         assert not (f.gen[r] == cfg.mask_id).any()
+
+
+# --------------------------------------------------------------------------
+# DiLaServe threshold control (review, section 3.2)
+# --------------------------------------------------------------------------
+def test_rate_above_knots_and_limits():
+    from oracle.control import rate_above
+    f = [0.2, 0.4, 0.6, 0.7, 0.8, 0.5]          # min, q25, median, avg, q75, frac
+    # the distribution passes through its knots
+    assert rate_above(0.2, f) == 1.0
+    assert rate_above(0.4, f) == 0.75
+    assert rate_above(0.6, f) == 0.5
+    assert rate_above(0.8, f) == 0.25
+    assert rate_above(0.1, f) == 1.0 and rate_above(1.0, f) == 0.0
+    # linear between knots: halfway from q25 to the median
+    assert rate_above(0.5, f) == pytest.approx(0.625, abs=1e-15)
+    # no unmasked position yet: uniform
+    nan = [float("nan")] * 5 + [0.0]
+    assert rate_above(0.7, nan) == pytest.approx(0.3, abs=1e-15)
+    # never increases with the threshold
+    ts = np.linspace(0, 1.2, 121)
+    r = [rate_above(t, f) for t in ts]
+    assert all(a >= b for a, b in zip(r, r[1:]))
+
+
+def test_steps_to_clear_closed_forms():
+    from oracle.control import steps_to_clear
+    for m in range(0, 40):
+        assert steps_to_clear(m, 0.0) == m          # the fallback alone: one per step
+        assert steps_to_clear(m, 1.0) == (1 if m else 0)
+    for k in range(0, 11):
+        assert steps_to_clear(2 ** k, 0.5) == k + 1  # halving: 2^k, 2^(k-1), ..., 1, 0
+    # by hand: 10 -3-> 7 -2-> 5 -1-> 4 -1-> 3 -1-> 2 -1-> 1 -1-> 0
+    assert steps_to_clear(10, 0.3) == 7
+
+
+def test_predict_steps_grows_with_the_threshold():
+    from oracle.control import predict_steps_stub
+    rng = np.random.default_rng(13)
+    for _ in range(100):
+        q = np.sort(rng.random(4))
+        f = [q[0], q[1], q[2], float(q.mean()), q[3], 0.5]
+        m, kb = int(rng.integers(0, 33)), int(rng.integers(0, 8))
+        steps = [predict_steps_stub(t, f, m, kb, 32) for t in (0.5, 0.6, 0.7, 0.8, 0.9)]
+        assert all(a <= b for a, b in zip(steps, steps[1:]))
+        assert steps[0] >= (1 if m else 0) + kb
+
+
+def test_load_control_hand_case():
+    from oracle.control import load_control
+    load = [[1, 2, 4], [1, 3, 5], [2, 2, 6]]
+    # request 0: 0 + 4 + (1 + 2) = 7 <= 9 keeps the top; committed 4
+    # request 1: 4 + 5 + 2 = 11 > 9 drops it, 4 + 3 + 2 = 9 keeps index 1; committed 7
+    # request 2: 7 + 6 = 13 > 9, 7 + 2 = 9 keeps index 1
+    assert load_control(load, 9.0).tolist() == [2, 1, 1]
+    assert load_control(load, 1e9).tolist() == [2, 2, 2]
+    assert load_control(load, 0.0).tolist() == [0, 0, 0]
+
+
+def test_load_control_keeps_the_worst_case_within_capacity():
+    from oracle.control import load_control
+    rng = np.random.default_rng(14)
+    for _ in range(200):
+        R, T = int(rng.integers(1, 9)), int(rng.integers(1, 6))
+        load = np.sort(rng.integers(1, 20, size=(R, T)), axis=1).astype(float)
+        cap = float(rng.integers(int(load[:, 0].sum()), int(load[:, -1].sum()) + 2))
+        keep = load_control(load, cap)
+        # the all-lowest plan fits, so the chosen plan fits ...
+        assert sum(load[i, keep[i]] for i in range(R)) <= cap
+        # ... and raising the first request that is not at its top by one
+        # step breaks the worst case at its turn
+        for i in range(R):
+            if keep[i] < T - 1:
+                committed = sum(load[j, keep[j]] for j in range(i))
+                assert committed + load[i, keep[i] + 1] + load[i + 1:, 0].sum() > cap
+                break
+
+
+def test_slo_threshold_hand_cases():
+    from oracle.control import slo_threshold
+    steps = [10, 20, 40]
+    assert slo_threshold(steps, 0.01, 0.25) == 1          # 0.4 s > 0.25 s, 0.2 s fits
+    assert slo_threshold(steps, 0.01, 1.0) == 2
+    assert slo_threshold(steps, 0.01, 1.0, max_allowed=0) == 0
+    assert slo_threshold(steps, 0.01, 0.05) == 0          # nothing fits: the fastest
