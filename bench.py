@@ -227,6 +227,7 @@ class Pipeline:
         self.logits = torch.empty((B * L, ldv), dtype=torch.int16, device=device)
         self.logits.fill_(int(np.uint16(synth.POISON_BITS).view(np.int16)))
         rows = np.flatnonzero(inp.masked.reshape(-1))
+        self.masked_rows = rows
         for s0 in range(0, len(rows), 1024):
             part = rows[s0:s0 + 1024]
             h = np.empty((len(part), ldv), dtype=np.uint16)
@@ -338,21 +339,30 @@ class Pipeline:
         if rc:
             raise RuntimeError(f"dllm_admit failed: {rc}")
 
-    def run(self, slot, stream, ev_before=None, ev_after=None):
+    def run(self, slot, stream, ev_before=None, ev_after=None, compact=None):
+        """One pipeline step on state slot ``slot``.  ``compact``: (device
+        logits of the masked rows only, their count) to read those through
+        dllm_step_compact instead of the full logits array."""
         lib = self.lib
         pa, sa, aa, ca = self.args[slot]
         self.admit_host()
         rc = lib.dllm_pack(ctypes.byref(pa), stream)
         if ev_before is not None:
             ev_before.record()
-        if self.quota is None:
+        if compact is not None:
+            buf, rows = compact
+            saved = sa.logits
+            sa.logits = ctypes.c_void_p(buf.data_ptr())
+            rc |= lib.dllm_step_compact(ctypes.byref(sa), rows, self.quota_ptr if self.quota is not None else None,
+                                        stream)
+            sa.logits = saved
+        elif self.quota is None:
             rc |= lib.dllm_step(ctypes.byref(sa), stream)
         else:
             rc |= lib.dllm_step_quota(ctypes.byref(sa), self.quota_ptr, stream)
         if ev_after is not None:
             ev_after.record()
-        rc |= lib.dllm_advance(ctypes.byref(aa), stream)
-        rc |= lib.dllm_compact(ctypes.byref(ca), stream)
+        rc |= lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream)
         if rc:
             raise RuntimeError("a dllm call failed inside the timed loop")
 
@@ -360,7 +370,7 @@ class Pipeline:
         self.state.copy_(self.pristine)
 
 
-LAUNCHES_PER_STEP = 5   # pack, step, advance, compact (scatter + copy-back)
+LAUNCHES_PER_STEP = 3   # pack, step, advance + compaction (one launch)
 
 
 def run_gpu(args, rank, world, local_rank, dist):
@@ -427,11 +437,15 @@ def run_gpu(args, rank, world, local_rank, dist):
 
 def run_e2e(pipe, steps):
     """Same step through the public API from pinned host buffers: every step
-    copies its inputs host->device and reads its results back."""
+    copies its inputs host->device (the masked positions' logits rows, which
+    are all the step reads, through dllm_step_compact; the batch state) and
+    reads its results back."""
     torch = pipe.torch
     dev = pipe.device
-    logits_h = torch.empty(pipe.logits.shape, dtype=pipe.logits.dtype, pin_memory=True)
-    logits_h.copy_(pipe.logits)
+    rows_d = torch.from_numpy(pipe.masked_rows).to(dev)
+    compact_d = pipe.logits[rows_d].contiguous()
+    logits_h = torch.empty(compact_d.shape, dtype=compact_d.dtype, pin_memory=True)
+    logits_h.copy_(compact_d)
     state_h = torch.from_numpy(pipe.slot_host.copy()).pin_memory()
     out_words = pipe.B * (1 + 1 + 1 + 6) + pipe.words["ids"] + pipe.words["cs"] + 1
     out_h = torch.empty(out_words, dtype=torch.int32, pin_memory=True)
@@ -439,9 +453,9 @@ def run_e2e(pipe, steps):
     sh = ctypes.c_void_p(stream.cuda_stream)
     B = pipe.B
     def one():
-        pipe.logits.copy_(logits_h, non_blocking=True)
+        compact_d.copy_(logits_h, non_blocking=True)
         pipe.state[0].copy_(state_h, non_blocking=True)
-        pipe.run(0, sh)
+        pipe.run(0, sh, compact=(compact_d, compact_d.shape[0]))
         o = 0
         for t in (pipe.done[0].to(torch.int32), pipe.accept[0], pipe.n_new[0], pipe.feats[0].view(torch.int32).reshape(-1),
                   pipe.view(0, "ids"), pipe.view(0, "cs"), pipe.A_out[0]):
@@ -455,7 +469,7 @@ def run_e2e(pipe, steps):
     for _ in range(steps):
         one()
     el = time.perf_counter() - t
-    h2d = pipe.logits.numel() * 2 + pipe.slot_words * 4
+    h2d = compact_d.numel() * 2 + pipe.slot_words * 4
     d2h = out_words * 4
     return {"value": pipe.M * steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps}
@@ -740,7 +754,7 @@ def main():
                                 "threshold per request from {0.5,0.6,0.7,0.8,0.9}"),
                        "mask_fraction": "U[0,1] per request",
                        "box_W": pipe.W, "box_cost": pipe.cost, "token_budget": BUDGET,
-                       "step": "admit(host)+pack+step+advance+compact",
+                       "step": "admit(host)+pack+step+advance/compact (one launch)",
                        "l2": "inputs larger than L2: 0.62 GB of masked logits rows per step, no flush",
                        "state_ring": RING},
             "logits_gbs": pipe.M * cfg.V * 2 * K / res["seconds"] / 1e9 / world,

@@ -95,6 +95,7 @@ _SIGNATURES = {
     "dllm_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
     "dllm_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
     "dllm_step_quota": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p, _p]),
+    "dllm_step_compact": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int64, _p, _p]),
     "dllm_predict_steps_stub": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_int32, _p, _p, _p, _p]),
     "dllm_load_control": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_double, _p]),
     "dllm_slo_thresholds": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p, _p, _p]),
@@ -106,6 +107,7 @@ _SIGNATURES = {
     "dllm_admit": (ctypes.c_int, [_i32, _p, _i32, _p, _p, _i32, _i64, _p, ctypes.POINTER(_i32)]),
     "dllm_pack": (ctypes.c_int, [ctypes.POINTER(PackArgs), _p]),
     "dllm_pack_block": (ctypes.c_int, [ctypes.POINTER(PackArgs), _p]),
+    "dllm_advance_compact": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), ctypes.POINTER(CompactArgs), _p]),
     "dllm_advance": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), _p]),
     "dllm_compact_workspace_size": (_sz, [_i32, _i32, _p]),
     "dllm_compact": (ctypes.c_int, [ctypes.POINTER(CompactArgs), _p]),
@@ -227,7 +229,7 @@ def step_workspace_size(B, L, V):
 
 
 def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=False, out=None, workspace=None,
-         quota=None):
+         quota=None, compact=False):
     """One denoise step (dllm_step, or dllm_step_quota when ``quota`` is
     given) on the current stream.
 
@@ -238,6 +240,9 @@ def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=Fa
     conf_state: float32 [B, L] (updated in place)
     quota:      int32 [B] CUDA tensor or None: positions to unmask per
                 request under the fixed-steps rule
+    compact:    logits hold only the masked positions' rows, in position
+                order (dllm_step_compact); any number of rows >= the masked
+                count
     Returns a dict of output tensors: done (uint8 [B]), accept_len, n_new
     (int32 [B]), feats (float32 [B, 6]) and, with debug, conf / lse / tok [B, L].
     """
@@ -256,7 +261,7 @@ def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=Fa
     if logits.element_size() != 2:
         raise TypeError("logits must be a 16-bit (bf16) tensor")
     ldv = logits.shape[-1]
-    if logits.numel() != B * L * ldv:
+    if not compact and logits.numel() != B * L * ldv:
         raise ValueError("logits must hold B*L rows of the row stride")
     if out is None:
         out = {
@@ -278,7 +283,10 @@ def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=Fa
                  done=_ptr(out["done"]), accept_len=_ptr(out["accept_len"]), n_new=_ptr(out["n_new"]),
                  feats=_ptr(out.get("feats")), conf_out=_ptr(out.get("conf")), lse_out=_ptr(out.get("lse")),
                  tok_out=_ptr(out.get("tok")), workspace=_ptr(ws), workspace_bytes=ws.numel())
-    if quota is None:
+    if compact:
+        rows = logits.numel() // ldv
+        _check("dllm_step_compact", lib.dllm_step_compact(ctypes.byref(a), rows, _ptr(quota), _stream(dev)))
+    elif quota is None:
         _check("dllm_step", lib.dllm_step(ctypes.byref(a), _stream(dev)))
     else:
         _check("dllm_step_quota", lib.dllm_step_quota(ctypes.byref(a), _ptr(quota), _stream(dev)))
@@ -440,6 +448,39 @@ def compact(evict, arrays, *, new_index=None, src_row=None, A_out=None):
                     workspace_bytes=ws.numel())
     _check("dllm_compact", lib.dllm_compact(ctypes.byref(a), _stream(dev)))
     return new_index, src_row, A_out
+
+
+def advance_compact(adv, rid, K, b, input_ids, conf_state, gen_tokens, arrays, *, mask_id, evict=None,
+                    new_index=None, src_row=None, A_out=None):
+    """dllm_advance_compact: commit the advanced rows' blocks, then compact
+    ``arrays`` (which may include b / input_ids / conf_state) by the evict
+    flags, in one launch.  Returns (evict, new_index, src_row, A_out)."""
+    torch = _torch()
+    dev = _require_cuda(adv, rid, K, b, input_ids, conf_state, gen_tokens, *arrays)
+    A, L = input_ids.shape
+    if len(arrays) > COMPACT_MAX_ARRAYS:
+        raise ValueError("too many arrays")
+    for t in arrays:
+        if A and t.shape[0] != A:
+            raise ValueError("every array needs A rows")
+    if evict is None:
+        evict = torch.empty(max(A, 1), dtype=torch.uint8, device=dev)
+    if new_index is None:
+        new_index = torch.empty(max(A, 1), dtype=torch.int32, device=dev)
+    if src_row is None:
+        src_row = torch.empty(max(A, 1), dtype=torch.int32, device=dev)
+    if A_out is None:
+        A_out = torch.empty(1, dtype=torch.int32, device=dev)
+    aa = AdvanceArgs(A=A, L=L, mask_id=mask_id, advance=_ptr(adv), rid=_ptr(rid), K=_ptr(K), b=_ptr(b),
+                     input_ids=_ptr(input_ids), conf_state=_ptr(conf_state), gen_tokens=_ptr(gen_tokens),
+                     ld_gen=gen_tokens.shape[-1], evict=_ptr(evict))
+    rb = [(t.numel() // A) * t.element_size() if A else 1 for t in arrays]
+    rb_arr = (_i64 * COMPACT_MAX_ARRAYS)(*rb)
+    arr_ptrs = (_p * COMPACT_MAX_ARRAYS)(*[t.data_ptr() for t in arrays])
+    ca = CompactArgs(A=A, n_arrays=len(arrays), evict=_ptr(evict), new_index=_ptr(new_index),
+                     src_row=_ptr(src_row), A_out=_ptr(A_out), arrays=arr_ptrs, row_bytes=rb_arr)
+    _check("dllm_advance_compact", load().dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), _stream(dev)))
+    return evict, new_index, src_row, A_out
 
 
 def refill(A0, new_rid, new_p, new_K, new_thr, rid, p, b, K, thr, input_ids, conf_state, *, mask_id):

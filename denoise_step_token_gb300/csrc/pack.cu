@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
@@ -453,6 +454,195 @@ extern "C" int dllm_advance(const dllm_advance_args* a, void* stream) {
     if (!P.err) return DLLM_ERR_CUDA;
     const int wpb = 8;
     advance_kernel<<<(a->A + wpb - 1) / wpb, wpb * 32, 0, as_stream(stream)>>>(P);
+    DLLM_CUDA_TRY(cudaGetLastError());
+    return DLLM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// dllm_advance_compact: dllm_advance then dllm_compact by its evict flags, in
+// one launch of one CTA.  Rows are compacted in place, in chunks of rows in
+// increasing order: a chunk's surviving rows are first staged in shared
+// memory, then written to their new rows.  A destination is never above its
+// source, so it lies in a chunk already staged (this one or an earlier one)
+// and nothing is overwritten before it is read.
+// ---------------------------------------------------------------------------
+namespace dllm {
+namespace {
+
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedStageBytes = 96 * 1024;
+
+struct FusedParams {
+    AdvanceParams adv;
+    int n_arrays, chunk_rows, word;   // word: 4-byte elements (else bytes)
+    unsigned char* arrays[DLLM_COMPACT_MAX_ARRAYS];
+    long long row_bytes[DLLM_COMPACT_MAX_ARRAYS];
+    long long stage_off[DLLM_COMPACT_MAX_ARRAYS];   // per-row offset of each array in a staged row
+    long long row_total;                            // staged bytes per row
+    int* new_index;
+    int* src_row;
+    int* A_out;
+};
+
+// The block commit of dllm_advance for all rows, by one CTA, 1024 rows at a
+// time: one thread per row reads its row's state and writes b and evict,
+// then every thread copies block tokens, one element each.
+__device__ __forceinline__ void advance_rows(const AdvanceParams& P, long long* s_dst, uint8_t* s_ev, int tid) {
+    for (int c0 = 0; c0 < P.A; c0 += kFusedThreads) {
+        const int i = c0 + tid;
+        long long dst = -1;
+        bool ev = false;
+        if (i < P.A) {
+            if (P.advance[i]) {
+                const int r = P.rid[i];
+                const int b = P.b[i];
+                const int K = P.K[i];
+                if (b < 0 || b >= K || (long long)(b + 1) * P.L > P.ld_gen) {
+                    set_error(P.err, DLLM_DEVERR_BLOCK_INDEX);
+                } else {
+                    dst = (long long)r * P.ld_gen + (long long)b * P.L;
+                    ev = b + 1 >= K;
+                    P.b[i] = b + 1;
+                }
+            }
+            P.evict[i] = ev ? 1 : 0;
+        }
+        s_dst[tid] = dst;
+        s_ev[tid] = ev ? 1 : 0;
+        __syncthreads();
+        const int rows = min(kFusedThreads, P.A - c0);
+        const long long n = (long long)rows * P.L;
+        const float qnan = __int_as_float(0x7fc00000);
+        for (long long t = tid; t < n; t += kFusedThreads) {
+            const int row = (int)(t / P.L);
+            const long long d = s_dst[row];
+            if (d < 0) continue;
+            const int j = (int)(t - (long long)row * P.L);
+            const long long src = (long long)(c0 + row) * P.L + j;
+            P.gen[d + j] = P.ids[src];
+            if (!s_ev[row]) {
+                P.ids[src] = P.mask_id;
+                P.cs[src] = qnan;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename E>
+__device__ __forceinline__ void move_chunk(const FusedParams& P, unsigned char* stage, const int* s_src,
+                                           const int* s_dst, int kept, int tid) {
+    // stage: kept row k of array a at stage + k * row_total + stage_off[a]
+    for (int a = 0; a < P.n_arrays; ++a) {
+        const long long n = P.row_bytes[a] / (long long)sizeof(E);
+        const long long total = n * kept;
+        const E* base = reinterpret_cast<const E*>(P.arrays[a]);
+        for (long long t = tid; t < total; t += kFusedThreads) {
+            const int k = (int)(t / n);
+            const long long j = t - (long long)k * n;
+            *reinterpret_cast<E*>(stage + (long long)k * P.row_total + P.stage_off[a] + j * (long long)sizeof(E)) =
+                base[(long long)s_src[k] * n + j];
+        }
+    }
+    __syncthreads();
+    for (int a = 0; a < P.n_arrays; ++a) {
+        const long long n = P.row_bytes[a] / (long long)sizeof(E);
+        const long long total = n * kept;
+        E* base = reinterpret_cast<E*>(P.arrays[a]);
+        for (long long t = tid; t < total; t += kFusedThreads) {
+            const int k = (int)(t / n);
+            const long long j = t - (long long)k * n;
+            base[(long long)s_dst[k] * n + j] = *reinterpret_cast<const E*>(
+                stage + (long long)k * P.row_total + P.stage_off[a] + j * (long long)sizeof(E));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __grid_constant__ FusedParams P) {
+    extern __shared__ __align__(16) unsigned char stage[];
+    __shared__ int s_wsum[kFusedThreads / 32];
+    __shared__ int s_src[kFusedThreads], s_dst[kFusedThreads];
+    __shared__ long long s_gen_dst[kFusedThreads];
+    __shared__ uint8_t s_ev[kFusedThreads];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int A = P.adv.A;
+    advance_rows(P.adv, s_gen_dst, s_ev, tid);   // ends with a barrier: evict, ids, cs, b visible CTA-wide
+    int base = 0;      // survivors before the chunk
+    for (int c0 = 0; c0 < A; c0 += P.chunk_rows) {
+        const int i = c0 + tid;
+        const bool in = tid < P.chunk_rows && i < A;
+        const bool keep = in && P.adv.evict[i] == 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0) s_wsum[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, kept = 0;
+        for (int w = 0; w < kFusedThreads / 32; ++w) {
+            const int c = s_wsum[w];
+            if (w < warp) before += c;
+            kept += c;
+        }
+        const int rank = before + __popc(bal & ((1u << lane) - 1u));
+        if (in) {
+            const int ni = keep ? base + rank : -1;
+            if (P.new_index) P.new_index[i] = ni;
+            if (keep) {
+                if (P.src_row) P.src_row[ni] = i;
+                s_src[rank] = i;
+                s_dst[rank] = ni;
+            }
+        }
+        __syncthreads();
+        if (P.word) move_chunk<uint32_t>(P, stage, s_src, s_dst, kept, tid);
+        else move_chunk<uint8_t>(P, stage, s_src, s_dst, kept, tid);
+        __syncthreads();
+        base += kept;
+    }
+    if (tid == 0) *P.A_out = base;
+}
+
+}  // namespace
+}  // namespace dllm
+
+extern "C" int dllm_advance_compact(const dllm_advance_args* a, const dllm_compact_args* c, void* stream) {
+    if (!a || !c || a->A < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->ld_gen < 0 || c->A != a->A) return DLLM_ERR_INVAL;
+    if (c->n_arrays < 0 || c->n_arrays > DLLM_COMPACT_MAX_ARRAYS || !c->A_out) return DLLM_ERR_INVAL;
+    if (a->A > 0 && (!a->advance || !a->rid || !a->K || !a->b || !a->input_ids || !a->conf_state ||
+                     !a->gen_tokens || !a->evict))
+        return DLLM_ERR_INVAL;
+    FusedParams P;
+    P.adv.A = a->A; P.adv.L = a->L; P.adv.mask_id = a->mask_id;
+    P.adv.advance = a->advance; P.adv.rid = a->rid; P.adv.K = a->K; P.adv.b = a->b; P.adv.ids = a->input_ids;
+    P.adv.cs = a->conf_state; P.adv.gen = a->gen_tokens; P.adv.ld_gen = a->ld_gen; P.adv.evict = a->evict;
+    P.adv.err = error_word_ptr();
+    if (!P.adv.err) return DLLM_ERR_CUDA;
+    P.n_arrays = c->n_arrays;
+    P.row_total = 0;
+    bool word = true;
+    for (int k = 0; k < c->n_arrays; ++k) {
+        if ((a->A > 0 && !c->arrays[k]) || c->row_bytes[k] <= 0) return DLLM_ERR_INVAL;
+        P.arrays[k] = static_cast<unsigned char*>(c->arrays[k]);
+        P.row_bytes[k] = c->row_bytes[k];
+        word = word && (c->row_bytes[k] % 4 == 0) && (reinterpret_cast<uintptr_t>(c->arrays[k]) % 4 == 0);
+    }
+    for (int k = 0; k < c->n_arrays; ++k) {
+        P.stage_off[k] = P.row_total;
+        P.row_total += (c->row_bytes[k] + 3) & ~3ll;   // 4-byte aligned slots
+    }
+    if (P.row_total > kFusedStageBytes) return DLLM_ERR_UNSUPPORTED;
+    P.word = word ? 1 : 0;
+    P.chunk_rows = P.row_total > 0 ? (int)std::min<long long>(kFusedThreads, kFusedStageBytes / P.row_total)
+                                   : kFusedThreads;
+    P.new_index = c->new_index; P.src_row = c->src_row; P.A_out = c->A_out;
+    int dev = 0;
+    DLLM_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return DLLM_ERR_UNSUPPORTED;
+    static std::atomic<bool> configured[64];
+    if (!configured[dev].load(std::memory_order_acquire)) {
+        DLLM_CUDA_TRY(cudaFuncSetAttribute(advance_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kFusedStageBytes));
+        configured[dev].store(true, std::memory_order_release);
+    }
+    advance_compact_kernel<<<1, kFusedThreads, kFusedStageBytes, as_stream(stream)>>>(P);
     DLLM_CUDA_TRY(cudaGetLastError());
     return DLLM_OK;
 }

@@ -140,6 +140,8 @@ __device__ __noinline__ unsigned long long poll_word(const unsigned long long* p
 
 struct StepParams {
     int B, L, V, NC, BL, mask_id, list_cap, static_cap, zero_cap;
+    int compact;              // logits rows hold only the masked positions, by rank
+    long long logits_rows;    // rows of a compact logits array
     FastDiv div_nc, div_g;   // division by NC and by the grid size
     long long ldv;
     const uint16_t* logits;
@@ -542,7 +544,7 @@ __device__ __forceinline__ void finalize_request(const StepParams& P, int b, boo
 // Row finisher: fold the chunk partials of `row` in a fixed order, write the
 // row results, then count the row towards its request.
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_gmask, int row, int lane) {
+__device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_gmask, int row, int lrow, int lane) {
     // Every chunk of the row has been counted, but the words holding the
     // partials are written with relaxed stores: a word still reading zero
     // is polled (bounded in time) until its store lands.  Each word is
@@ -589,7 +591,7 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     // argmax: first element equal to M inside that 2048-element batch; each
     // lane loads all of its vectors at once, then scans them in order
     const long long start = key * kBatchElems;
-    const uint16_t* rp = P.logits + (long long)row * P.ldv;
+    const uint16_t* rp = P.logits + (long long)lrow * P.ldv;
     uint4 v[kBatchVecs];
 #pragma unroll
     for (int k = 0; k < kBatchVecs; ++k) {
@@ -642,11 +644,11 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t*
     int h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
     h = __shfl_sync(0xffffffffu, h, 0);
     while (h < P.list_cap) {
-        int v = (lane == 0) ? ld_acquire_cta_shared(&s_queue[h]) : 0;
+        int v = (lane == 0) ? ld_acquire_cta_shared(&s_queue[2 * h]) : 0;
         v = __shfl_sync(0xffffffffu, v, 0);
         if (v != 0) {
             __syncwarp();   // lane 0's acquire orders the whole warp's reads
-            finish_row(P, s_gmask, v - 1, lane);
+            finish_row(P, s_gmask, v - 1, s_queue[2 * h + 1], lane);
             h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
             h = __shfl_sync(0xffffffffu, h, 0);
             continue;
@@ -655,7 +657,7 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t*
         nd = __shfl_sync(0xffffffffu, nd, 0);
         if (nd == kStreamWarps) {
             // every completed row is queued: slot h is filled now or never
-            int v2 = (lane == 0) ? ld_acquire_cta_shared(&s_queue[h]) : 0;
+            int v2 = (lane == 0) ? ld_acquire_cta_shared(&s_queue[2 * h]) : 0;
             if (__shfl_sync(0xffffffffu, v2, 0) != 0) continue;
             break;
         }
@@ -676,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     unsigned char* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStreamWarps) * kStages * kCopyBytes);
     int* s_list = reinterpret_cast<int*>(bars + kStreamWarps * kStages);
-    int* s_queue = s_list + P.list_cap;   // rows this CTA completed, for the finishers
-    int* s_zero = s_queue + P.list_cap;   // this CTA's requests without masked rows
+    int* s_queue = s_list + P.list_cap;   // rows this CTA completed: (position + 1, logits row) pairs
+    int* s_zero = s_queue + 2 * P.list_cap;   // this CTA's requests without masked rows
     uint16_t* s_gmask = reinterpret_cast<uint16_t*>(s_zero + P.zero_cap);   // masked bits, 16 positions each
     __shared__ int s_wsum[kWarpsTotal];
     __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last, s_next;
@@ -693,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         s_qhead = 0;
         s_ndone = 0;
     }
-    for (int i = tid; i < P.list_cap; i += kThreads) s_queue[i] = 0;
+    for (int i = tid; i < 2 * P.list_cap; i += kThreads) s_queue[i] = 0;
     if (tid < kStreamWarps * kStages) mbar_fence_init();
 
     // ---- S1: masked bits of the entry state, 16 positions per thread ------
@@ -740,6 +742,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const int before = wbase + incl - cnt;
     const int NC = P.NC;
     const int V = P.V;
+    if (P.compact && M > P.logits_rows) {
+        // a compact logits array too short for the batch: nothing is read
+        if (tid == 0 && cta == 0) set_error(P.err, DLLM_DEVERR_LOGITS_ROWS);
+        M = 0;
+    }
     const int U = M * NC;   // units fit in 32 bits (checked on the host)
     // The last T = min(ceil(M / kTailDen), kTailRowsMax) masked rows (the
     // tail) are taken one chunk at a time by any warp whose CTA has run out,
@@ -878,12 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         bool failed = false;
 
         auto start_chunk = [&](int gu) {
-            const int c = gu - fast_div(gu, P.div_nc) * NC;
-            const int row = row_of(gu);
+            const int rr = fast_div(gu, P.div_nc);
+            const int c = gu - rr * NC;
+            const int lrow = P.compact ? rr : row_of(gu);   // compact logits are indexed by rank
             p_unit = gu;
             p_q = 0;
             p_len = min(kChunkElems, V32 - c * kChunkElems);
-            p_src = (long long)row * P.ldv + (long long)c * kChunkElems;
+            p_src = (long long)lrow * P.ldv + (long long)c * kChunkElems;
         };
         auto issue = [&]() {
             if (p_done) return;
@@ -926,10 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         // warp's memory traffic).  The add's result is tested one group
         // later; the add that brings the counter to NC queues the row for
         // the finishers, who poll for the words still in flight.
-        int pend_old = -1, pend_k = 0, pend_row = 0;   // add issued, result not yet tested
+        int pend_old = -1, pend_k = 0, pend_row = 0, pend_lrow = 0;   // add issued, result not yet tested
         auto test_pending = [&]() {
-            if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC)
-                st_release_cta_shared(&s_queue[atomicAdd(&s_qtail, 1)], pend_row + 1);
+            if (lane == 1 && pend_old >= 0 && pend_old + pend_k == NC) {
+                const int q = atomicAdd(&s_qtail, 1);
+                s_queue[2 * q + 1] = pend_lrow;
+                st_release_cta_shared(&s_queue[2 * q], pend_row + 1);
+            }
             pend_old = -1;
         };
 
@@ -1018,6 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 pend_old = atom_add_relaxed_gpu(P.cnt + row, k);
                 pend_k = k;
                 pend_row = row;
+                pend_lrow = P.compact ? fast_div(gu, P.div_nc) : row;
             }
         }
         test_pending();
@@ -1130,7 +1142,7 @@ namespace dllm {
 namespace {
 
 // dllm_step and dllm_step_quota: quota null selects the threshold rule.
-int launch_step(const dllm_step_args* a, const int32_t* quota, void* stream) {
+int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, void* stream) {
     if (!a) return DLLM_ERR_INVAL;
     if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
     if (a->B == 0) return DLLM_OK;
@@ -1158,7 +1170,7 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, void* stream) {
     const int list_cap = static_cap + min((BL + kTailDen - 1) / kTailDen, kTailRowsMax);
     const int zero_cap = a->B / G + 1;
     const size_t smem = size_t(kStreamWarps) * kStages * kCopyBytes + size_t(kStreamWarps) * kStages * 8 +
-                        size_t(2 * list_cap + zero_cap) * 4 + size_t((BL + 15) / 16) * 2;
+                        size_t(3 * list_cap + zero_cap) * 4 + size_t((BL + 15) / 16) * 2;
     // per-device launch facts, queried once
     if (dev < 0 || dev >= 64) return DLLM_ERR_UNSUPPORTED;
     LaunchFacts& lf = g_launch_facts[dev];
@@ -1188,6 +1200,8 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, void* stream) {
     P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
     P.list_cap = list_cap; P.static_cap = static_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
     P.div_nc = make_fastdiv((uint32_t)NC);
+    P.compact = logits_rows >= 0 ? 1 : 0;
+    P.logits_rows = logits_rows;
     P.div_g = make_fastdiv((uint32_t)G);
     P.logits = a->logits; P.ids = a->input_ids; P.thr = a->thr; P.quota = quota; P.cs = a->conf_state;
     P.done = a->done; P.accept = a->accept_len; P.n_new = a->n_new; P.feats = a->feats;
@@ -1208,11 +1222,16 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, void* stream) {
 }  // namespace
 }  // namespace dllm
 
-extern "C" int dllm_step(const dllm_step_args* a, void* stream) { return launch_step(a, nullptr, stream); }
+extern "C" int dllm_step(const dllm_step_args* a, void* stream) { return launch_step(a, nullptr, -1, stream); }
 
 extern "C" int dllm_step_quota(const dllm_step_args* a, const int32_t* quota, void* stream) {
     if (!quota) return DLLM_ERR_INVAL;
-    return launch_step(a, quota, stream);
+    return launch_step(a, quota, -1, stream);
+}
+
+extern "C" int dllm_step_compact(const dllm_step_args* a, int64_t logits_rows, const int32_t* quota, void* stream) {
+    if (logits_rows < 0) return DLLM_ERR_INVAL;
+    return launch_step(a, quota, logits_rows, stream);
 }
 
 extern "C" int32_t dllm_transfer_quota(int32_t L, int32_t S, int32_t s) {

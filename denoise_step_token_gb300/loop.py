@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import admit, advance, compact, pack, pack_block, pack_plan, refill, step, transfer_quota
+from . import admit, advance_compact, pack, pack_block, pack_plan, refill, step, transfer_quota
 
 
 class DeviceLoop:
@@ -186,15 +186,14 @@ class DeviceLoop:
             return np.zeros(A, dtype=bool), None
         self.in_place = False
         adv_d = torch.as_tensor(adv.astype(np.uint8)).to(self.device)
-        evict_d = advance(adv_d, self.rid[:A], self.K[:A], self.b[:A], self.ids[:A], self.cs[:A], self.gen,
-                          mask_id=self.mask_id)
+        _, _, _, A_out = advance_compact(adv_d, self.rid[:A], self.K[:A], self.b[:A], self.ids[:A], self.cs[:A],
+                                         self.gen, [self.rid[:A], self.p[:A], self.b[:A], self.K[:A], self.thr[:A],
+                                                    self.ids[:A], self.cs[:A]], mask_id=self.mask_id)
         b = self.b_h.copy()
         s = self.s_h + stepped.astype(np.int32)
         b[adv] += 1
         s[adv] = 0
         evict = adv & (b >= self.K_all[self.rid_h])
-        _, _, A_out = compact(evict_d, [self.rid[:A], self.p[:A], self.b[:A], self.K[:A], self.thr[:A],
-                                        self.ids[:A], self.cs[:A]])
         keep = ~evict
         wait = done & ~adv
         self.rid_h, self.b_h, self.s_h, self.wait_h = self.rid_h[keep], b[keep], s[keep], wait[keep]

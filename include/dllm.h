@@ -52,6 +52,7 @@ extern "C" {
 #define DLLM_DEVERR_TIMEOUT 1     /* a bounded wait (bulk copy, partial word) expired */
 #define DLLM_DEVERR_ROW_WIDTH 2   /* dllm_pack: p + (b + 1) * L > W for a row */
 #define DLLM_DEVERR_BLOCK_INDEX 3 /* dllm_advance: block index outside [0, K) or output row too short */
+#define DLLM_DEVERR_LOGITS_ROWS 4 /* dllm_step_compact: more masked positions than logits rows */
 
 #define DLLM_MAX_L 1024
 #define DLLM_NUM_FEATURES 6
@@ -171,6 +172,19 @@ int dllm_step(const dllm_step_args* args, void* stream);
  * S4-S6, outputs, workspace rules); args->thr is not read and may be NULL.
  * Errors as dllm_step, plus DLLM_ERR_INVAL for a NULL quota. */
 int dllm_step_quota(const dllm_step_args* args, const int32_t* quota, void* stream);
+
+/* S1-S6 reading compact logits: args->logits holds logits_rows rows of the
+ * row stride args->ldv, and row k is the logits of the k-th masked position
+ * of the batch at entry, in position order (b * L + j ascending) -- the rows
+ * dllm_step reads, and only those (a model may compute its LM head for the
+ * masked positions alone; a host copies M rows instead of B * L).  quota
+ * NULL selects the threshold rule, else the fixed-steps rule as
+ * dllm_step_quota.  Everything else, including the results, is as
+ * dllm_step.  If the batch has more masked positions than logits_rows, no
+ * logits are read, the device error word gets DLLM_DEVERR_LOGITS_ROWS and
+ * the outputs of requests with masked positions are unspecified (the
+ * workspace stays valid).  DLLM_ERR_INVAL for logits_rows < 0. */
+int dllm_step_compact(const dllm_step_args* args, int64_t logits_rows, const int32_t* quota, void* stream);
 
 /* Host.  The fixed-steps quota of step s (0-based) of a block (BlockServe
  * page, section II-E): L spread evenly over S steps, floor(L / S) per step
@@ -380,6 +394,18 @@ typedef struct dllm_compact_args {
     void* workspace;                             /* device, dllm_compact_workspace_size() bytes */
     size_t workspace_bytes;
 } dllm_compact_args;
+
+/* dllm_advance followed by dllm_compact on the evict flags it computes, in
+ * one launch (one CTA): the batch-management tail of a serving-loop
+ * iteration (BlockServe Algorithm 1: commit, b += 1, evict; FDFO page,
+ * section "FDFO 的核心思想": done requests leave at once).  Results equal
+ * dllm_advance(adv) then dllm_compact(cmp) with cmp->evict = adv->evict;
+ * cmp->evict and cmp's workspace are not read.  The compacted arrays may
+ * include adv's b / input_ids / conf_state (they are compacted after the
+ * commit).  Errors as the two calls, plus DLLM_ERR_INVAL when cmp->A !=
+ * adv->A and DLLM_ERR_UNSUPPORTED when the arrays' bytes per row (each
+ * rounded up to 4) exceed 96 KiB. */
+int dllm_advance_compact(const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream);
 
 /* Workspace bytes for dllm_compact over these arrays (0 if invalid). */
 size_t dllm_compact_workspace_size(int32_t A, int32_t n_arrays, const int64_t* row_bytes);

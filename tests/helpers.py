@@ -124,6 +124,21 @@ def device_logits(inp, device, chunk_rows=2048):
     return d
 
 
+def device_logits_compact(inp, device, extra_rows=0, chunk_rows=2048):
+    """Device bf16 logits of the masked positions only, [M + extra_rows,
+    ldv]: row k is the k-th masked position in position order (extra rows
+    poisoned)."""
+    import torch
+    cfg = inp.cfg
+    rows = np.flatnonzero(inp.masked.reshape(-1))
+    d = torch.empty((len(rows) + extra_rows, cfg.row_stride), dtype=torch.int16, device=device)
+    d.fill_(int(np.int16(np.uint16(synth.POISON_BITS).view(np.int16))))
+    for s in range(0, len(rows), chunk_rows):
+        part = rows[s:s + chunk_rows]
+        d[s:s + len(part)] = torch.from_numpy(host_rows(inp, part).view(np.int16)).to(device)
+    return d
+
+
 def device_state(inp, device):
     import torch
     return (torch.from_numpy(inp.input_ids.copy()).to(device),

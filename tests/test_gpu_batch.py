@@ -147,3 +147,50 @@ def test_refill(dllm, device):
     # rows outside the range untouched
     assert (ids.cpu().numpy()[A0 + n:] == np.arange((A0 + n) * L, rows * L).reshape(-1, L)).all()
     assert (b.cpu().numpy()[:A0] == 5).all()
+
+
+
+@pytest.mark.parametrize("A,L,K", [(0, 32, 4), (1, 32, 2), (77, 32, 3), (256, 32, 8), (1500, 16, 2), (300, 64, 1)])
+def test_advance_compact_parity(dllm, device, A, L, K):
+    """dllm_advance_compact equals the oracle's advance followed by its
+    stable compaction (rows of several widths, chunked staging when the
+    rows do not fit one chunk)."""
+    V = 1000
+    reqs, rid, b, gen, blocks = _mixed_rows(A * 5 + L + 3, A, L, V, 0, 10, K)
+    rng = np.random.default_rng(A + 7)
+    adv = (rng.random(A) < 0.6).astype(np.uint8)
+    Kr = rng.integers(1, K + 1, size=A).astype(np.int32)
+    b = np.minimum(b, Kr - 1).astype(np.int32)
+    cs = rng.random((A, L)).astype(np.float32)
+    extra = rng.integers(0, 255, (A, 5)).astype(np.uint8)                     # a 5-byte row array
+    o_gen = {int(rid[i]): np.asarray(gen[int(rid[i])][: b[i] * L]) for i in range(A)}
+    o_b, o_ids, o_cs = b.astype(np.int64).copy(), blocks.astype(np.int64).copy(), cs.astype(np.float64).copy()
+    o_evict = oracle_advance(adv, rid, o_b, Kr, o_ids, o_cs, o_gen, V - 1)
+    o_new, o_src, o_A = oracle.compact(o_evict)
+    d = {k: _t(v, device) for k, v in dict(rid=rid, K=Kr, b=b, ids=blocks, cs=cs, extra=extra).items()}
+    d_gen = _t(gen, device)
+    # an odd A adds a 5-byte row array, which takes the byte-copy path
+    arrays = [d["rid"], d["K"], d["b"], d["ids"], d["cs"]] + ([d["extra"]] if A % 2 else [])
+    evict, new_index, src_row, A_out = dllm.advance_compact(
+        _t(adv, device), d["rid"], d["K"], d["b"], d["ids"], d["cs"], d_gen, arrays, mask_id=V - 1)
+    assert int(A_out.cpu().numpy()[0]) == o_A
+    if A:
+        np.testing.assert_array_equal(evict.cpu().numpy()[:A].astype(bool), o_evict)
+        np.testing.assert_array_equal(new_index.cpu().numpy()[:A], o_new)
+        np.testing.assert_array_equal(src_row.cpu().numpy()[:o_A], o_src)
+    np.testing.assert_array_equal(d["rid"].cpu().numpy()[:o_A], rid[o_src])
+    np.testing.assert_array_equal(d["K"].cpu().numpy()[:o_A], Kr[o_src])
+    np.testing.assert_array_equal(d["b"].cpu().numpy()[:o_A], o_b[o_src])
+    np.testing.assert_array_equal(d["ids"].cpu().numpy()[:o_A], o_ids[o_src])
+    if A % 2:
+        np.testing.assert_array_equal(d["extra"].cpu().numpy()[:o_A], extra[o_src])
+    got_cs = d["cs"].cpu().numpy()[:o_A]
+    want_cs = o_cs[o_src]
+    assert np.array_equal(np.isnan(got_cs), np.isnan(want_cs))
+    np.testing.assert_array_equal(got_cs[~np.isnan(got_cs)], want_cs[~np.isnan(want_cs)].astype(np.float32))
+    g = d_gen.cpu().numpy()
+    for i in range(A):
+        r = int(rid[i])
+        n = len(o_gen[r])
+        np.testing.assert_array_equal(g[r][:n], o_gen[r])
+    assert dllm.get_device_error(device) == 0

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import compare_step, device_logits, device_state, enforce_margins, oracle_step
+from helpers import compare_step, device_logits, device_logits_compact, device_state, enforce_margins, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -95,3 +95,20 @@ def test_quota_full_size_sampled(dllm, device):
     m_out = ids == cfg.mask_id
     assert np.array_equal(got["n_new"], np.minimum(np.maximum(quota, 0), m_in.sum(axis=1)))
     assert not (m_out & ~m_in).any()
+
+
+
+def test_quota_with_compact_logits(dllm, device):
+    import torch
+    cfg = CASES["l64"]
+    inp = synth.make_step_state(cfg, 3)
+    quota = np.random.default_rng(7).integers(0, cfg.L + 1, size=cfg.B).astype(np.int32)
+    enforce_margins(inp, quota=quota)
+    ref = oracle_step(inp, quota=quota)
+    logits = device_logits_compact(inp, device)
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step(logits, ids, None, cs, V=cfg.V, mask_id=cfg.mask_id, debug=True,
+                    quota=torch.from_numpy(quota).to(device), compact=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids.cpu().numpy(), cs.cpu().numpy())

@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import (CONF_TOL, compare_step, device_logits, device_state, enforce_margins, oracle_step)
+from helpers import (CONF_TOL, compare_step, device_logits, device_logits_compact, device_state, enforce_margins,
+                     oracle_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -208,3 +209,59 @@ def test_repeated_steps_to_completion(dllm, device):
         got = {k: v.cpu().numpy() for k, v in out.items()}
         compare_step(ref, got, list(range(cfg.B)), cfg.L, ids_d.cpu().numpy(), cs_d.cpu().numpy())
     assert not (ids_d.cpu().numpy() == cfg.mask_id).any()
+
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "l64", "all_masked", "v_small"])
+def test_compact_logits_parity_and_identity(dllm, device, name):
+    """dllm_step_compact (logits of the masked positions only, by rank)
+    equals the oracle and is bit-identical to dllm_step on the full
+    layout."""
+    cfg = SMALL_CASES[name]
+    inp = synth.make_step_state(cfg, 4)
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    full, ids_f, cs_f = run_gpu(dllm, inp, device)
+    logits = device_logits_compact(inp, device, extra_rows=3)
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step(logits, ids, thr, cs, V=cfg.V, mask_id=cfg.mask_id, debug=True, compact=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+    for k in ("conf", "lse", "tok", "feats", "done", "n_new", "accept_len"):
+        a, b = got[k], full[k]
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              b.view(np.uint32) if b.dtype == np.float32 else b), k
+    assert np.array_equal(ids.cpu().numpy(), ids_f)
+
+
+def test_compact_logits_full_size_sampled(dllm, device):
+    cfg = synth.STEP_CONFIGS["dream"]
+    inp = synth.make_step_state(cfg, 8)
+    rng = np.random.default_rng(5)
+    sample = sorted(rng.choice(cfg.B, size=10, replace=False).tolist())
+    enforce_margins(inp, sample)
+    ref = oracle_step(inp, sample)
+    logits = device_logits_compact(inp, device)
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step(logits, ids, thr, cs, V=cfg.V, mask_id=cfg.mask_id, debug=True, compact=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, sample, cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+
+
+def test_compact_logits_too_few_rows_is_reported(dllm, device):
+    """Fewer logits rows than masked positions: nothing is read, the device
+    error word says so, and the workspace serves the next call."""
+    cfg = SMALL_CASES["ragged"]
+    inp = synth.make_step_state(cfg, 6)
+    M = int(inp.masked.sum())
+    assert M > 2
+    logits = device_logits_compact(inp, device)[: M - 2].contiguous()
+    ids, thr, cs = device_state(inp, device)
+    dllm.step(logits, ids, thr, cs, V=cfg.V, mask_id=cfg.mask_id, compact=True)
+    assert dllm.get_device_error(device) == 4          # DLLM_DEVERR_LOGITS_ROWS
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    got, ids2, cs2 = run_gpu(dllm, inp, device)
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids2, cs2)
