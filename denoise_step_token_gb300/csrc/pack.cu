@@ -471,6 +471,8 @@ namespace {
 
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedStageBytes = 96 * 1024;
+constexpr int kFusedBatch = 8;   // global loads in flight per thread
+constexpr int kFusedMapWords = 2048;   // elements per staged row the element map covers
 
 struct FusedParams {
     AdvanceParams adv;
@@ -493,10 +495,12 @@ __device__ __forceinline__ void advance_rows(const AdvanceParams& P, long long* 
         long long dst = -1;
         bool ev = false;
         if (i < P.A) {
-            if (P.advance[i]) {
-                const int r = P.rid[i];
-                const int b = P.b[i];
-                const int K = P.K[i];
+            // all four loads in flight together
+            const int adv = P.advance[i];
+            const int r = P.rid[i];
+            const int b = P.b[i];
+            const int K = P.K[i];
+            if (adv) {
                 if (b < 0 || b >= K || (long long)(b + 1) * P.L > P.ld_gen) {
                     set_error(P.err, DLLM_DEVERR_BLOCK_INDEX);
                 } else {
@@ -511,18 +515,30 @@ __device__ __forceinline__ void advance_rows(const AdvanceParams& P, long long* 
         s_ev[tid] = ev ? 1 : 0;
         __syncthreads();
         const int rows = min(kFusedThreads, P.A - c0);
-        const long long n = (long long)rows * P.L;
+        const int n = rows * P.L;   // <= 1024 * DLLM_MAX_L
+        int* ids = P.ids + (long long)c0 * P.L;
+        float* cs = P.cs + (long long)c0 * P.L;
         const float qnan = __int_as_float(0x7fc00000);
-        for (long long t = tid; t < n; t += kFusedThreads) {
-            const int row = (int)(t / P.L);
-            const long long d = s_dst[row];
-            if (d < 0) continue;
-            const int j = (int)(t - (long long)row * P.L);
-            const long long src = (long long)(c0 + row) * P.L + j;
-            P.gen[d + j] = P.ids[src];
-            if (!s_ev[row]) {
-                P.ids[src] = P.mask_id;
-                P.cs[src] = qnan;
+        // kFusedBatch tokens per thread in flight: every load, then the stores
+        for (int t0 = tid; t0 < n; t0 += kFusedBatch * kFusedThreads) {
+            int v[kFusedBatch];
+#pragma unroll
+            for (int u = 0; u < kFusedBatch; ++u) {
+                const int t = t0 + u * kFusedThreads;
+                v[u] = (t < n && s_dst[t / P.L] >= 0) ? ids[t] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kFusedBatch; ++u) {
+                const int t = t0 + u * kFusedThreads;
+                if (t >= n) break;
+                const int row = t / P.L;
+                const long long d = s_dst[row];
+                if (d < 0) continue;
+                P.gen[d + (t - row * P.L)] = v[u];
+                if (!s_ev[row]) {
+                    ids[t] = P.mask_id;
+                    cs[t] = qnan;
+                }
             }
         }
         __syncthreads();
@@ -531,30 +547,43 @@ __device__ __forceinline__ void advance_rows(const AdvanceParams& P, long long* 
 
 template <typename E>
 __device__ __forceinline__ void move_chunk(const FusedParams& P, unsigned char* stage, const int* s_src,
-                                           const int* s_dst, int kept, int tid) {
-    // stage: kept row k of array a at stage + k * row_total + stage_off[a]
-    for (int a = 0; a < P.n_arrays; ++a) {
-        const long long n = P.row_bytes[a] / (long long)sizeof(E);
-        const long long total = n * kept;
-        const E* base = reinterpret_cast<const E*>(P.arrays[a]);
-        for (long long t = tid; t < total; t += kFusedThreads) {
-            const int k = (int)(t / n);
-            const long long j = t - (long long)k * n;
-            *reinterpret_cast<E*>(stage + (long long)k * P.row_total + P.stage_off[a] + j * (long long)sizeof(E)) =
-                base[(long long)s_src[k] * n + j];
+                                           const int* s_dst, const short* s_arr, const int* s_off, int kept,
+                                           int tid) {
+    // Staged row k (all arrays side by side) at stage + k * row_total.  The
+    // chunk's elements over every array form one flat range (32-bit
+    // indices: the stage holds at most 96 KiB); s_arr / s_off map an
+    // element's place in a staged row to its array (-1: padding) and its
+    // byte offset in that array's row.  kFusedBatch loads per thread are in
+    // flight before their stores.
+    const int per_row = (int)(P.row_total / (long long)sizeof(E));
+    const int total = per_row * kept;
+    for (int t0 = tid; t0 < total; t0 += kFusedBatch * kFusedThreads) {
+        E v[kFusedBatch];
+#pragma unroll
+        for (int u = 0; u < kFusedBatch; ++u) {
+            const int t = t0 + u * kFusedThreads;
+            v[u] = E(0);
+            if (t < total) {
+                const int k = t / per_row;
+                const int w = t - k * per_row;
+                const int a = s_arr[w];
+                if (a >= 0) v[u] = *reinterpret_cast<const E*>(P.arrays[a] + (long long)s_src[k] * P.row_bytes[a] + s_off[w]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kFusedBatch; ++u) {
+            const int t = t0 + u * kFusedThreads;
+            if (t < total) reinterpret_cast<E*>(stage)[t] = v[u];
         }
     }
     __syncthreads();
-    for (int a = 0; a < P.n_arrays; ++a) {
-        const long long n = P.row_bytes[a] / (long long)sizeof(E);
-        const long long total = n * kept;
-        E* base = reinterpret_cast<E*>(P.arrays[a]);
-        for (long long t = tid; t < total; t += kFusedThreads) {
-            const int k = (int)(t / n);
-            const long long j = t - (long long)k * n;
-            base[(long long)s_dst[k] * n + j] = *reinterpret_cast<const E*>(
-                stage + (long long)k * P.row_total + P.stage_off[a] + j * (long long)sizeof(E));
-        }
+    for (int t = tid; t < total; t += kFusedThreads) {
+        const int k = t / per_row;
+        const int w = t - k * per_row;
+        const int a = s_arr[w];
+        if (a >= 0)
+            *reinterpret_cast<E*>(P.arrays[a] + (long long)s_dst[k] * P.row_bytes[a] + s_off[w]) =
+                reinterpret_cast<const E*>(stage)[t];
     }
 }
 
@@ -564,8 +593,30 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
     __shared__ int s_src[kFusedThreads], s_dst[kFusedThreads];
     __shared__ long long s_gen_dst[kFusedThreads];
     __shared__ uint8_t s_ev[kFusedThreads];
+    __shared__ short s_arr[kFusedMapWords];
+    __shared__ int s_off[kFusedMapWords];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int A = P.adv.A;
+    // element map of a staged row: array index (-1 in padding) and offset
+    {
+        const int es = P.word ? 4 : 1;
+        const int per_row = (int)(P.row_total / es);
+        for (int w = tid; w < per_row; w += kFusedThreads) {
+            const long long off = (long long)w * es;
+            int arr = -1, o = 0;
+            for (int a = P.n_arrays - 1; a >= 0; --a) {
+                if (off >= P.stage_off[a]) {
+                    if (off - P.stage_off[a] < P.row_bytes[a]) {
+                        arr = a;
+                        o = (int)(off - P.stage_off[a]);
+                    }
+                    break;
+                }
+            }
+            s_arr[w] = (short)arr;
+            s_off[w] = o;
+        }
+    }
     advance_rows(P.adv, s_gen_dst, s_ev, tid);   // ends with a barrier: evict, ids, cs, b visible CTA-wide
     int base = 0;      // survivors before the chunk
     for (int c0 = 0; c0 < A; c0 += P.chunk_rows) {
@@ -592,8 +643,8 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
             }
         }
         __syncthreads();
-        if (P.word) move_chunk<uint32_t>(P, stage, s_src, s_dst, kept, tid);
-        else move_chunk<uint8_t>(P, stage, s_src, s_dst, kept, tid);
+        if (P.word) move_chunk<uint32_t>(P, stage, s_src, s_dst, s_arr, s_off, kept, tid);
+        else move_chunk<uint8_t>(P, stage, s_src, s_dst, s_arr, s_off, kept, tid);
         __syncthreads();
         base += kept;
     }
@@ -630,6 +681,7 @@ extern "C" int dllm_advance_compact(const dllm_advance_args* a, const dllm_compa
     }
     if (P.row_total > kFusedStageBytes) return DLLM_ERR_UNSUPPORTED;
     P.word = word ? 1 : 0;
+    if (P.row_total / (word ? 4 : 1) > kFusedMapWords) return DLLM_ERR_UNSUPPORTED;
     P.chunk_rows = P.row_total > 0 ? (int)std::min<long long>(kFusedThreads, kFusedStageBytes / P.row_total)
                                    : kFusedThreads;
     P.new_index = c->new_index; P.src_row = c->src_row; P.A_out = c->A_out;

@@ -403,8 +403,10 @@ typedef struct dllm_compact_args {
  * cmp->evict and cmp's workspace are not read.  The compacted arrays may
  * include adv's b / input_ids / conf_state (they are compacted after the
  * commit).  Errors as the two calls, plus DLLM_ERR_INVAL when cmp->A !=
- * adv->A and DLLM_ERR_UNSUPPORTED when the arrays' bytes per row (each
- * rounded up to 4) exceed 96 KiB. */
+ * adv->A and DLLM_ERR_UNSUPPORTED when a row of all the arrays (each
+ * array's part rounded up to 4 bytes) holds more than 2048 elements: 4-byte
+ * elements when every row size and array address is a multiple of 4, else
+ * bytes. */
 int dllm_advance_compact(const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream);
 
 /* Workspace bytes for dllm_compact over these arrays (0 if invalid). */
