@@ -55,6 +55,7 @@ WORKLOADS = {
 LOOP_K = 8                     # blocks per request (gen 256 / L 32)
 BUDGET = 1 << 20               # token budget of eq. (1)
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0       # GB300 HBM3e nominal, for context beside the measured peak
 RING = 64
 
 
@@ -766,6 +767,8 @@ def main():
             "step_kernel_ms": step_ms,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                         "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,
+                         "all_rows_logits_bytes_per_launch": cfg.B * cfg.L * cfg.V * 2,
                          "kernel": "step_kernel (dllm_step_quota)" if fixed else "step_kernel (dllm_step)",
                          "algorithmic_bytes_per_launch": alg},
             "cpu_baseline": cpu,

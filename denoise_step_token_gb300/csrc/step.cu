@@ -551,6 +551,12 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     // cleared once read, ready for the next call.
     const int NC = P.NC;
     const int b = row / P.L;
+    // Claim the row on its request's counter first: the add's round trip
+    // overlaps the fold and the argmax re-read.  The request's last claimer
+    // finalises it, polling for the words of rows other warps are still
+    // finishing.
+    int old = 0;
+    if (lane == 0) old = atom_add_relaxed_gpu(P.cnt + P.BL + b, 1);
     // masked rows of this request at entry, from this CTA's scan bitmask
     int mb = 0;
     {
@@ -613,9 +619,7 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     best = __reduce_min_sync(0xffffffffu, best);
     const float conf = __fdiv_rn(1.0f, S);
     const float lse = M + logf(S);
-    // the row's word and its count on the request are both relaxed: the
-    // request's finalizer polls for words still in flight
-    int old = 0;
+    // publish the row's word (relaxed: the request's finalizer polls)
     if (lane == 0) {
         P.row_tok[row] = (int)best;
         if (P.conf_out) P.conf_out[row] = conf;
@@ -623,10 +627,10 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
         if (P.tok_out) P.tok_out[row] = (int)best;
         P.cnt[row] = 0;
         st_relaxed_gpu_u64(P.row_word + row, pack_row(conf, (int)best));
-        old = atom_add_relaxed_gpu(P.cnt + P.BL + b, 1);
     }
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old == mb - 1) {
+        __syncwarp();   // lane 0's word store is ordered before the other lanes' loads
         finalize_request(P, b, true, lane);
     }
 }
