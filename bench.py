@@ -596,8 +596,9 @@ def run_loop_bench(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     dllm.load()
     lcfg = synth.LOOP_CONFIGS[args.workload]
-    on = serve_queue(lcfg, 2000 + rank, device, reloop=True)
-    off = serve_queue(lcfg, 2000 + rank, device, reloop=False)
+    on = serve_queue(lcfg, 2000 + rank, device, reloop=True, native=True)
+    off = serve_queue(lcfg, 2000 + rank, device, reloop=False, native=True)
+    py = serve_queue(lcfg, 2000 + rank, device, reloop=True, native=False)
     secs = on["secs"]
     out = {
         "metric": METRIC, "value": on["masked"] / secs, "unit": UNIT, "n_gpus": world, "steps": on["iters"],
@@ -605,17 +606,18 @@ def run_loop_bench(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "requests": lcfg.R, "prompt_len": [lcfg.p_lo, lcfg.p_hi],
                    "gen": lcfg.gen, "L": lcfg.L, "V": lcfg.V, "token_budget": lcfg.budget,
-                   "threshold": lcfg.threshold, "mode": "fdfo", "in_place_reloop": True,
+                   "threshold": lcfg.threshold, "mode": "fdfo", "in_place_reloop": True, "driver": "native (dllm_loop_*)",
                    "timed": "admit+refill+pack+step+done readback+advance+compact per iteration"},
         "loop": {"iterations": on["iters"], "timed_s": secs, "masked_positions": on["masked"],
                  "mean_active_rows": on["mean_A"],
                  "logits_gbs": on["masked"] * lcfg.V * 2 / secs / 1e9,
-                 "step_call_ms_total": on["step_ms"], "step_call_share": on["step_ms"] / 1e3 / secs,
                  "reloop_iterations": on["reloops"]},
         "without_reloop": {"value": off["masked"] / off["secs"], "timed_s": off["secs"],
                            "iterations": off["iters"], "ms_per_step": off["secs"] * 1e3 / off["iters"]},
+        "python_driver": {"value": py["masked"] / py["secs"], "timed_s": py["secs"],
+                          "iterations": py["iters"], "ms_per_step": py["secs"] * 1e3 / py["iters"]},
     }
-    assert on["iters"] == off["iters"] and on["masked"] == off["masked"]
+    assert on["iters"] == off["iters"] == py["iters"] and on["masked"] == off["masked"] == py["masked"]
     out["threshold_control"] = time_threshold_control(lcfg, seed=3000 + rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -647,11 +649,12 @@ def time_threshold_control(lcfg, seed, A=256, reps=200):
             "mean_threshold": float(thr.mean()), "capped_requests": int((cap < 4).sum())}
 
 
-def serve_queue(lcfg, seed, device, reloop):
-    """Serve one generated queue to completion; returns the timed seconds,
-    iterations, masked positions, step-call milliseconds and re-loops."""
+def serve_queue(lcfg, seed, device, reloop, native=True):
+    """Serve one generated queue to completion, with libdllm's native loop
+    (two calls per iteration) or the Python DeviceLoop; returns the timed
+    seconds, iterations, masked positions and re-loops."""
     import torch
-    from denoise_step_token_gb300.loop import DeviceLoop
+    from denoise_step_token_gb300.loop import DeviceLoop, NativeLoop
     reqs = synth.make_loop_requests(lcfg, seed)
     L, V, ldv = lcfg.L, lcfg.V, lcfg.row_stride
     pool_rows = 4096
@@ -659,15 +662,37 @@ def serve_queue(lcfg, seed, device, reloop):
     keys = synth.logits_row_keys(seed, np.arange(pool_rows), 0, 0, 0, 0)
     synth.fill_logits_rows(pool_h, V, np.arange(pool_rows), keys, lcfg.offset_max, lcfg.mask_id)
     pool = torch.from_numpy(pool_h.view(np.int16)).to(device)
-    loop = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V,
-                      mask_id=lcfg.mask_id, pad_id=lcfg.pad_id, budget=lcfg.budget, device=device, mode="fdfo",
-                      reloop=reloop)
+    cls = NativeLoop if native else DeviceLoop
+    loop = cls(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V,
+               mask_id=lcfg.mask_id, pad_id=lcfg.pad_id, budget=lcfg.budget, device=device, mode="fdfo",
+               reloop=reloop)
     logits = torch.empty((lcfg.R * L, ldv), dtype=torch.int16, device=device)
     ev = []
-    step_ms = []
     active = []
     masked_total = 0
     iters = 0
+    if native:
+        while not loop.finished():
+            # timed: admission, refill, pack (dllm_loop_begin)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            inf = loop.begin()
+            torch.cuda.synchronize()
+            t_begin = time.perf_counter() - t0
+            # untimed: the model forward's stand-in
+            rows = loop.masked_rows()
+            _fill_loop_logits(logits, pool, rows, seed, pool_rows, device)
+            # timed: step, done readback, advance + compaction (dllm_loop_end)
+            torch.cuda.synchronize()
+            t1 = time.perf_counter()
+            active.append(inf.A)
+            loop.end(logits[: max(inf.A, 1) * L])
+            torch.cuda.synchronize()
+            ev.append(t_begin + time.perf_counter() - t1)
+            iters += 1
+            masked_total += len(rows)
+        return {"secs": sum(ev), "iters": iters, "masked": masked_total, "reloops": loop.info().reloops,
+                "mean_A": float(np.mean(active)) if active else 0.0}
     while not loop.finished():
         # timed: admission (host) and refill
         torch.cuda.synchronize()
@@ -677,31 +702,34 @@ def serve_queue(lcfg, seed, device, reloop):
         t_admit = time.perf_counter() - t0
         # untimed: the model forward's stand-in -- pool rows for the masked positions
         rows = loop.masked_rows()
-        if rows:
-            flat = torch.as_tensor([r[0] for r in rows], device=device)
-            h = synth.out(np.uint64(seed), np.asarray([((r[1] * 64 + r[2]) * 4096 + r[3]) * 64 + r[4]
-                                                       for r in rows], dtype=np.uint64))
-            pick = torch.as_tensor((h % np.uint64(pool_rows)).astype(np.int64), device=device)
-            logits[flat] = pool[pick]
+        _fill_loop_logits(logits, pool, rows, seed, pool_rows, device)
         # timed: pack, step, done readback, advance, compaction
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
         loop.pack_phase()
         active.append(loop.A)
-        e0.record()
         done, _ = loop.step_phase(logits[: loop.A * L])
-        e1.record()
         loop.finish_phase(done)
         torch.cuda.synchronize()
-        t_rest = time.perf_counter() - t1
-        ev.append(t_admit + t_rest)
-        step_ms.append(e0.elapsed_time(e1))
+        ev.append(t_admit + time.perf_counter() - t1)
         iters += 1
         masked_total += len(rows)
-    return {"secs": sum(ev), "iters": iters, "masked": masked_total, "step_ms": sum(step_ms),
-            "reloops": loop.reloops, "mean_A": float(np.mean(active)) if active else 0.0}
+    return {"secs": sum(ev), "iters": iters, "masked": masked_total, "reloops": loop.reloops,
+            "mean_A": float(np.mean(active)) if active else 0.0}
+
+
+def _fill_loop_logits(logits, pool, rows, seed, pool_rows, device):
+    """The model forward's stand-in (not timed): each masked position's
+    logits row is a pool row chosen by a hash of (request, block, step,
+    position)."""
+    import torch
+    if not rows:
+        return
+    flat = torch.as_tensor([r[0] for r in rows], device=device)
+    h = synth.out(np.uint64(seed), np.asarray([((r[1] * 64 + r[2]) * 4096 + r[3]) * 64 + r[4] for r in rows],
+                                              dtype=np.uint64))
+    pick = torch.as_tensor((h % np.uint64(pool_rows)).astype(np.int64), device=device)
+    logits[flat] = pool[pick]
 
 
 def main():

@@ -75,6 +75,19 @@ class AdvanceArgs(ctypes.Structure):
                 ("gen_tokens", _p), ("ld_gen", _i64), ("evict", _p)]
 
 
+class LoopConfig(ctypes.Structure):
+    _fields_ = [("R", _i32), ("L", _i32), ("V", _i32), ("mask_id", _i32), ("pad_id", _i32), ("mode", _i32),
+                ("reloop", _i32), ("S", _i32), ("capacity", _i32), ("pad0", _i32), ("budget", _i64)]
+
+
+class LoopInfo(ctypes.Structure):
+    _fields_ = [("A", _i32), ("W", _i32), ("cost", _i64), ("iteration", _i32), ("reloops", _i32),
+                ("pending", _i32), ("admitted_last", _i32), ("finished", _i32), ("in_place", _i32),
+                ("ld_gen", _i64), ("block_ids", _p), ("conf_state", _p), ("box_ids", _p), ("box_attn", _p),
+                ("box_pos", _p), ("box_pad", _p), ("box_blk_start", _p), ("gen_tokens", _p), ("done", _p),
+                ("n_new", _p), ("accept_len", _p), ("feats", _p)]
+
+
 class RefillArgs(ctypes.Structure):
     _fields_ = [("A0", _i32), ("n", _i32), ("L", _i32), ("mask_id", _i32),
                 ("new_rid", _p), ("new_p", _p), ("new_K", _p), ("new_thr", _p),
@@ -107,6 +120,14 @@ _SIGNATURES = {
     "dllm_admit": (ctypes.c_int, [_i32, _p, _i32, _p, _p, _i32, _i64, _p, ctypes.POINTER(_i32)]),
     "dllm_pack": (ctypes.c_int, [ctypes.POINTER(PackArgs), _p]),
     "dllm_pack_block": (ctypes.c_int, [ctypes.POINTER(PackArgs), _p]),
+    "dllm_loop_workspace_size": (_sz, [ctypes.POINTER(LoopConfig), _p, _p]),
+    "dllm_loop_create": (ctypes.c_int, [ctypes.POINTER(LoopConfig), _p, _p, _p, _p, _p, _p, _sz, _p,
+                                        ctypes.POINTER(_p)]),
+    "dllm_loop_destroy": (None, [_p]),
+    "dllm_loop_begin": (ctypes.c_int, [_p, _p]),
+    "dllm_loop_end": (ctypes.c_int, [_p, _p, _i64, _p]),
+    "dllm_loop_info": (ctypes.c_int, [_p, ctypes.POINTER(LoopInfo)]),
+    "dllm_loop_rows": (ctypes.c_int, [_p, _p, _p, _p]),
     "dllm_advance_compact": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), ctypes.POINTER(CompactArgs), _p]),
     "dllm_advance": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), _p]),
     "dllm_compact_workspace_size": (_sz, [_i32, _i32, _p]),
@@ -145,7 +166,7 @@ def load(build=True):
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs)):
+        for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs, LoopConfig, LoopInfo)):
             if lib.dllm_struct_size(which) != ctypes.sizeof(cls):
                 raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {lib.dllm_struct_size(which)} "
                                    f"bytes, binding {ctypes.sizeof(cls)}")

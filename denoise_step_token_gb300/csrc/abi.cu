@@ -85,6 +85,8 @@ extern "C" size_t dllm_struct_size(int which) {
         case 2: return sizeof(dllm_compact_args);
         case 3: return sizeof(dllm_advance_args);
         case 4: return sizeof(dllm_refill_args);
+        case 5: return sizeof(dllm_loop_config);
+        case 6: return sizeof(dllm_loop_info_t);
         default: return 0;
     }
 }

@@ -221,3 +221,94 @@ class DeviceLoop:
 
     def generated(self):
         return self.gen.cpu().numpy()
+
+
+class NativeLoop:
+    """The same loop driven by libdllm's native loop (dllm_loop_*): two
+    calls per iteration, ``begin()`` before the model forward and
+    ``end(logits)`` after it; all of the loop's device arrays live in one
+    workspace tensor.  ``mode``, ``reloop`` and ``S`` as for DeviceLoop."""
+
+    def __init__(self, p, K, prompt_off, prompt_tokens, thr, *, L, V, mask_id, pad_id, budget, device,
+                 mode="fdfo", reloop=False, S=None, capacity=None):
+        import ctypes
+        import torch
+        from . import LoopConfig, LoopInfo, _check, load
+        assert mode in ("fdfo", "sync")
+        self.torch, self.ctypes, self.LoopInfo, self._check = torch, ctypes, LoopInfo, _check
+        self.lib = load()
+        self.device = device
+        self.L, self.V = int(L), int(V)
+        p = np.ascontiguousarray(p, dtype=np.int32)
+        K = np.ascontiguousarray(K, dtype=np.int32)
+        thr = np.ascontiguousarray(thr, dtype=np.float32)
+        self.R = len(p)
+        cap = self.R if capacity is None else int(capacity)
+        self.cfg = LoopConfig(R=self.R, L=self.L, V=self.V, mask_id=int(mask_id), pad_id=int(pad_id),
+                              mode=0 if mode == "fdfo" else 1, reloop=1 if reloop else 0, S=0 if S is None else int(S),
+                              capacity=max(cap, 1), budget=int(budget))
+        vp = ctypes.c_void_p
+        need = int(self.lib.dllm_loop_workspace_size(ctypes.byref(self.cfg), vp(p.ctypes.data), vp(K.ctypes.data)))
+        if need == 0:
+            raise ValueError("invalid loop configuration")
+        self.ws = torch.empty(need, dtype=torch.uint8, device=device)
+        self.prompt_off = torch.as_tensor(np.asarray(prompt_off, dtype=np.int64)).to(device)
+        self.prompt_tokens = torch.as_tensor(np.asarray(prompt_tokens, dtype=np.int32)).to(device)
+        self.handle = vp()
+        self._stream = vp(torch.cuda.current_stream(device).cuda_stream)
+        _check("dllm_loop_create", self.lib.dllm_loop_create(
+            ctypes.byref(self.cfg), vp(p.ctypes.data), vp(K.ctypes.data), vp(thr.ctypes.data),
+            vp(self.prompt_off.data_ptr()), vp(self.prompt_tokens.data_ptr()) if self.prompt_tokens.numel() else None,
+            vp(self.ws.data_ptr()), need, self._stream, ctypes.byref(self.handle)))
+
+    def __del__(self):
+        if getattr(self, "handle", None) and self.handle.value:
+            self.lib.dllm_loop_destroy(self.handle)
+            self.handle = self.ctypes.c_void_p()
+
+    def info(self):
+        inf = self.LoopInfo()
+        self._check("dllm_loop_info", self.lib.dllm_loop_info(self.handle, self.ctypes.byref(inf)))
+        return inf
+
+    def view(self, ptr, shape, dtype):
+        """A tensor view of the workspace at device address ``ptr``."""
+        torch = self.torch
+        n = int(np.prod(shape))
+        size = torch.empty((), dtype=dtype).element_size()
+        off = int(ptr) - self.ws.data_ptr()
+        return self.ws[off:off + n * size].view(dtype).view(*shape)
+
+    def begin(self):
+        self._check("dllm_loop_begin", self.lib.dllm_loop_begin(self.handle, self._stream))
+        return self.info()
+
+    def end(self, logits):
+        self._check("dllm_loop_end", self.lib.dllm_loop_end(self.handle, self.ctypes.c_void_p(logits.data_ptr()),
+                                                            logits.shape[-1], self._stream))
+        return self.info()
+
+    def rows(self):
+        A = self.info().A
+        rid, b, s = (np.zeros(max(A, 1), dtype=np.int32) for _ in range(3))
+        vp = self.ctypes.c_void_p
+        self._check("dllm_loop_rows", self.lib.dllm_loop_rows(self.handle, vp(rid.ctypes.data), vp(b.ctypes.data),
+                                                              vp(s.ctypes.data)))
+        return rid[:A], b[:A], s[:A]
+
+    def masked_rows(self):
+        """(row * L + j, rid, b, s, j) of every masked position."""
+        inf = self.info()
+        if inf.A == 0:
+            return []
+        ids = self.view(inf.block_ids, (inf.A, self.L), self.torch.int32).cpu().numpy()
+        rid, b, s = self.rows()
+        rows, js = np.nonzero(ids == self.cfg.mask_id)
+        return [(int(i) * self.L + int(j), int(rid[i]), int(b[i]), int(s[i]), int(j)) for i, j in zip(rows, js)]
+
+    def generated(self):
+        inf = self.info()
+        return self.view(inf.gen_tokens, (self.R, inf.ld_gen), self.torch.int32).cpu().numpy()
+
+    def finished(self):
+        return bool(self.info().finished)

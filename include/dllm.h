@@ -71,7 +71,8 @@ int dllm_last_cuda_error(const char** name);
 
 /* sizeof() of the argument structs below, for binding self-checks:
  * which = 0 dllm_step_args, 1 dllm_pack_args, 2 dllm_compact_args,
- * 3 dllm_advance_args, 4 dllm_refill_args.  Returns 0 for an unknown `which`. */
+ * 3 dllm_advance_args, 4 dllm_refill_args, 5 dllm_loop_config,
+ * 6 dllm_loop_info_t.  Returns 0 for an unknown `which`. */
 size_t dllm_struct_size(int which);
 
 /* Synchronise `stream`, then return in *code the first device error
@@ -443,6 +444,92 @@ typedef struct dllm_refill_args {
 } dllm_refill_args;
 
 int dllm_refill(const dllm_refill_args* args, void* stream);
+
+/* ======================================================================
+ * The serving loop, native (BlockServe Algorithm 1, section II-C, in the
+ * FDFO or sync mode of the FDFO page, sections "FDFO 的核心思想" and
+ * "工程设计一"; the in-place re-loop of its section "工程设计四"; optionally
+ * the fixed-steps rule of BlockServe section II-E).
+ *
+ * One iteration is two calls around the caller's model forward:
+ *   dllm_loop_begin: sand-fill admission (dllm_admit) and refill
+ *     (dllm_refill) of the pending queue, then the box of eq. (1)
+ *     (dllm_pack; dllm_pack_block after a step that committed nothing, when
+ *     re-loop is on -- admission is skipped then: it would admit nothing);
+ *   dllm_loop_end: the step over the caller's logits ([A * L][ldv], row
+ *     i * L + j = position j of active row i), the readback of the done
+ *     flags (it synchronises the stream), then, if any row advances (FDFO:
+ *     its block is done; sync: every block is done), the block commit and
+ *     compaction in one launch (dllm_advance_compact).
+ * Device memory: everything lives in the caller's workspace
+ * (dllm_loop_workspace_size bytes, 256-byte aligned); the loop object
+ * itself is host memory, freed by dllm_loop_destroy.  The pending queue is
+ * every request, sorted by prompt length (ties by request id).
+ * ====================================================================== */
+typedef struct dllm_loop dllm_loop;
+
+typedef struct dllm_loop_config {
+    int32_t R;          /* requests */
+    int32_t L;          /* block length, 1..DLLM_MAX_L */
+    int32_t V;          /* vocabulary size */
+    int32_t mask_id;
+    int32_t pad_id;
+    int32_t mode;       /* 0 FDFO, 1 sync */
+    int32_t reloop;     /* 1: in-place re-loop */
+    int32_t S;          /* 0: threshold rule (per-request thresholds); > 0: fixed-steps rule, S steps per block */
+    int32_t capacity;   /* most active rows at once (admission beyond it returns DLLM_ERR_UNSUPPORTED) */
+    int32_t pad0;
+    int64_t budget;     /* token budget of eq. (1) */
+} dllm_loop_config;
+
+typedef struct dllm_loop_info_t {
+    int32_t A;              /* active rows */
+    int32_t W;              /* box width */
+    int64_t cost;           /* eq. (1) of the active set */
+    int32_t iteration;      /* completed iterations */
+    int32_t reloops;        /* iterations that ran in place */
+    int32_t pending;        /* requests not yet admitted */
+    int32_t admitted_last;  /* requests the last dllm_loop_begin admitted */
+    int32_t finished;       /* nothing pending and nothing active */
+    int32_t in_place;       /* the next iteration re-loops */
+    int64_t ld_gen;         /* row stride of gen_tokens */
+    int32_t* block_ids;     /* device [A][L] current blocks */
+    float* conf_state;      /* device [A][L] */
+    int32_t* box_ids;       /* device [A][W] */
+    uint8_t* box_attn;      /* device [A][W] */
+    int32_t* box_pos;       /* device [A][W] */
+    int32_t* box_pad;       /* device [A] */
+    int32_t* box_blk_start; /* device [A] */
+    int32_t* gen_tokens;    /* device [R][ld_gen]: committed blocks per request */
+    uint8_t* done;          /* device [A], last step's (pre-compaction rows) */
+    int32_t* n_new;
+    int32_t* accept_len;
+    float* feats;           /* device [A][6] */
+} dllm_loop_info_t;
+
+/* Workspace bytes for the loop (0 if the configuration is invalid).  p, K:
+ * host [R] prompt lengths (>= 0) and blocks to generate (>= 1). */
+size_t dllm_loop_workspace_size(const dllm_loop_config* cfg, const int32_t* p, const int32_t* K);
+
+/* Create a loop.  thr: host [R] thresholds (threshold rule); prompt_off:
+ * device [R + 1] offsets into prompt_tokens (device; may be NULL when every
+ * p is 0).  The workspace's step counters are cleared on `stream`.  Errors:
+ * DLLM_ERR_INVAL, DLLM_ERR_WORKSPACE, DLLM_ERR_CUDA. */
+int dllm_loop_create(const dllm_loop_config* cfg, const int32_t* p, const int32_t* K, const float* thr,
+                     const int64_t* prompt_off, const int32_t* prompt_tokens, void* workspace,
+                     size_t workspace_bytes, void* stream, dllm_loop** out);
+
+void dllm_loop_destroy(dllm_loop* loop);
+
+int dllm_loop_begin(dllm_loop* loop, void* stream);
+int dllm_loop_end(dllm_loop* loop, const uint16_t* logits, int64_t ldv, void* stream);
+
+/* State after the last call, with device pointers into the workspace. */
+int dllm_loop_info(const dllm_loop* loop, dllm_loop_info_t* out);
+
+/* Host copies of the active rows' request ids, block indices and steps taken
+ * in the current block (A entries each; any pointer may be NULL). */
+int dllm_loop_rows(const dllm_loop* loop, int32_t* rid, int32_t* b, int32_t* s);
 
 #ifdef __cplusplus
 }

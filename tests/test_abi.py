@@ -37,7 +37,8 @@ def test_library_exports_every_declared_function():
 
 def test_struct_sizes_match_binding():
     lib = dllm.load()
-    for which, cls in enumerate((dllm.StepArgs, dllm.PackArgs, dllm.CompactArgs, dllm.AdvanceArgs)):
+    for which, cls in enumerate((dllm.StepArgs, dllm.PackArgs, dllm.CompactArgs, dllm.AdvanceArgs, dllm.RefillArgs,
+                                 dllm.LoopConfig, dllm.LoopInfo)):
         assert lib.dllm_struct_size(which) == ctypes.sizeof(cls)
     assert lib.dllm_struct_size(99) == 0
 

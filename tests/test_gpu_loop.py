@@ -265,3 +265,73 @@ def test_loop_runs_under_the_library_controller(dllm, device):
         assert set(np.unique(used).tolist()) <= set(np.float32(cand).tolist())
         mean_thr[slo] = float(used.mean())
     assert mean_thr[0.02] < mean_thr[10.0]
+
+
+def _lockstep_native(dllm, device, cfg, mode, seed, reloop=False, S=None, max_iters=10000):
+    """libdllm's native loop (dllm_loop_*) in lockstep with the oracle loop:
+    admissions, box, masked rows, step outputs, commits, evictions and the
+    final tokens."""
+    import torch
+    from denoise_step_token_gb300.loop import NativeLoop
+    reqs = synth.make_loop_requests(cfg, seed)
+    R, L, V = cfg.R, cfg.L, cfg.V
+    prompts = [reqs.prompt_tokens[reqs.prompt_off[r]:reqs.prompt_off[r + 1]] for r in range(R)]
+    ol = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode, S=S)
+    nl = NativeLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V, mask_id=cfg.mask_id,
+                    pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode, reloop=reloop, S=S)
+    salts = {}
+    while not ol.finished() and ol.iteration < max_iters:
+        assert not nl.finished()
+        new_o = ol.admit_phase()
+        inf = nl.begin()
+        assert inf.admitted_last == len(new_o), ol.iteration
+        rid, b, s = nl.rows()
+        assert rid.tolist() == ol.rid and b.tolist() == ol.b
+        box_o = ol.box()
+        if ol.rid:
+            assert inf.W == box_o["W"] and inf.cost == ol.cost()
+            A, W = inf.A, inf.W
+            for k, ptr, dt in (("ids", inf.box_ids, torch.int32), ("attn", inf.box_attn, torch.uint8),
+                               ("pos", inf.box_pos, torch.int32)):
+                np.testing.assert_array_equal(nl.view(ptr, (A, W), dt).cpu().numpy(), box_o[k], err_msg=k)
+            np.testing.assert_array_equal(nl.view(inf.box_pad, (A,), torch.int32).cpu().numpy(), box_o["pad"])
+        rows_o = ol.masked_rows()
+        assert rows_o == nl.masked_rows()
+        thr_of_row = np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32)
+        logits = _loop_logits(seed, rows_o, len(ol.rid), L, V, cfg.offset_max, cfg.mask_id, thr_of_row, salts,
+                              cfg.row_stride, ol.quota())
+        ref = ol.step_phase(logits[: len(ol.rid) * L])
+        A = len(ol.rid)
+        inf = nl.end(torch.from_numpy(logits[: max(A, 1) * L].view(np.int16)).to(device))
+        if A:
+            np.testing.assert_array_equal(nl.view(inf.done, (A,), torch.uint8).cpu().numpy(), ref["done"])
+            np.testing.assert_array_equal(nl.view(inf.n_new, (A,), torch.int32).cpu().numpy(), ref["n_new"])
+            np.testing.assert_allclose(nl.view(inf.feats, (A, 6), torch.float32).cpu().numpy(), ref["feats"],
+                                       rtol=0, atol=1e-5, equal_nan=True)
+        ol.finish_phase(ref["done"])
+        inf = nl.info()
+        assert inf.A == len(ol.rid) and inf.iteration == ol.iteration
+        rid, b, s = nl.rows()
+        assert rid.tolist() == ol.rid and b.tolist() == ol.b
+        if inf.A:
+            np.testing.assert_array_equal(nl.view(inf.block_ids, (inf.A, L), torch.int32).cpu().numpy(), ol.ids)
+    assert ol.finished() and nl.finished()
+    gen = nl.generated()
+    for r in range(R):
+        np.testing.assert_array_equal(gen[r][: reqs.K[r] * L], ol.gen[r])
+    assert dllm.get_device_error(device) == 0
+    return ol, nl
+
+
+@pytest.mark.parametrize("mode,reloop,S", [("fdfo", False, None), ("fdfo", True, None), ("sync", True, None),
+                                           ("fdfo", True, 8)])
+def test_native_loop_lockstep(dllm, device, mode, reloop, S):
+    small_batch = synth.LoopConfig("small_batch", 16, 3, 60, 24, 8, 4099, 220, 0.9, 10.0)
+    ol, nl = _lockstep_native(dllm, device, small_batch, mode, seed=12, reloop=reloop, S=S)
+    if reloop:
+        assert nl.info().reloops > 0
+
+
+def test_native_loop_blockserve_shape_reduced_vocab(dllm, device):
+    cfg = synth.LoopConfig("bs_small_v", 256, 64, 1024, 256, 32, 1031, 1 << 20, 0.9, 8.0)
+    _lockstep_native(dllm, device, cfg, "fdfo", seed=5, reloop=True)
