@@ -46,6 +46,8 @@ struct PackParams {
 };
 
 __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams P) {
+    pdl_wait();
+    pdl_release();
     const long long total = (long long)P.A * P.W;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -403,8 +405,7 @@ extern "C" int dllm_pack(const dllm_pack_args* a, void* stream) {
     const int sms = sm_count();
     long long blocks = (total + 255) / 256;
     blocks = std::min<long long>(blocks, (long long)std::max(sms, 1) * 8);
-    pack_kernel<<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(P);
-    DLLM_CUDA_TRY(cudaGetLastError());
+    DLLM_CUDA_TRY(launch_dependent(pack_kernel, dim3((unsigned)blocks), dim3(256), 0, as_stream(stream), P));
     return DLLM_OK;
 }
 
@@ -597,6 +598,8 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
     __shared__ int s_off[kFusedMapWords];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int A = P.adv.A;
+    pdl_wait();
+    pdl_release();
     // element map of a staged row: array index (-1 in padding) and offset
     {
         const int es = P.word ? 4 : 1;
@@ -694,8 +697,8 @@ extern "C" int dllm_advance_compact(const dllm_advance_args* a, const dllm_compa
                                            kFusedStageBytes));
         configured[dev].store(true, std::memory_order_release);
     }
-    advance_compact_kernel<<<1, kFusedThreads, kFusedStageBytes, as_stream(stream)>>>(P);
-    DLLM_CUDA_TRY(cudaGetLastError());
+    DLLM_CUDA_TRY(launch_dependent(advance_compact_kernel, dim3(1), dim3(kFusedThreads), (size_t)kFusedStageBytes,
+                                   as_stream(stream), P));
     return DLLM_OK;
 }
 

@@ -701,6 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     for (int i = tid; i < 2 * P.list_cap; i += kThreads) s_queue[i] = 0;
     if (tid < kStreamWarps * kStages) mbar_fence_init();
+    // everything above touches shared memory only; the previous kernel's
+    // writes (input_ids, logits, state) are read from here on
+    pdl_wait();
+    pdl_release();
 
     // ---- S1: masked bits of the entry state, 16 positions per thread ------
     const int BL = P.BL;
@@ -1218,8 +1222,7 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
     P.sel = data + w.off_sel;
     P.err = error_word_ptr();
     if (!P.err) return DLLM_ERR_CUDA;
-    step_kernel<<<G, kThreads, smem, as_stream(stream)>>>(P);
-    DLLM_CUDA_TRY(cudaGetLastError());
+    DLLM_CUDA_TRY(launch_dependent(step_kernel, dim3(G), dim3(kThreads), smem, as_stream(stream), P));
     return DLLM_OK;
 }
 
