@@ -472,10 +472,12 @@ def compact(evict, arrays, *, new_index=None, src_row=None, A_out=None):
 
 
 def advance_compact(adv, rid, K, b, input_ids, conf_state, gen_tokens, arrays, *, mask_id, evict=None,
-                    new_index=None, src_row=None, A_out=None):
+                    new_index=None, src_row=None, A_out=None, workspace=True):
     """dllm_advance_compact: commit the advanced rows' blocks, then compact
     ``arrays`` (which may include b / input_ids / conf_state) by the evict
-    flags, in one launch.  Returns (evict, new_index, src_row, A_out)."""
+    flags.  With ``workspace`` a compaction workspace is passed, which lets
+    large batches take the multi-CTA path.  Returns (evict, new_index,
+    src_row, A_out)."""
     torch = _torch()
     dev = _require_cuda(adv, rid, K, b, input_ids, conf_state, gen_tokens, *arrays)
     A, L = input_ids.shape
@@ -498,8 +500,13 @@ def advance_compact(adv, rid, K, b, input_ids, conf_state, gen_tokens, arrays, *
     rb = [(t.numel() // A) * t.element_size() if A else 1 for t in arrays]
     rb_arr = (_i64 * COMPACT_MAX_ARRAYS)(*rb)
     arr_ptrs = (_p * COMPACT_MAX_ARRAYS)(*[t.data_ptr() for t in arrays])
+    ws = None
+    if workspace:
+        need = int(load().dllm_compact_workspace_size(A, len(arrays), ctypes.cast(rb_arr, ctypes.c_void_p)))
+        ws = _compact_ws.get(dev, need)
     ca = CompactArgs(A=A, n_arrays=len(arrays), evict=_ptr(evict), new_index=_ptr(new_index),
-                     src_row=_ptr(src_row), A_out=_ptr(A_out), arrays=arr_ptrs, row_bytes=rb_arr)
+                     src_row=_ptr(src_row), A_out=_ptr(A_out), arrays=arr_ptrs, row_bytes=rb_arr,
+                     workspace=_ptr(ws), workspace_bytes=0 if ws is None else ws.numel())
     _check("dllm_advance_compact", load().dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), _stream(dev)))
     return evict, new_index, src_row, A_out
 

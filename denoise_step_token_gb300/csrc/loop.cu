@@ -49,7 +49,17 @@ struct dllm_loop {
     int32_t *quota = nullptr, *new_rid_d = nullptr, *new_p_d = nullptr, *new_K_d = nullptr;
     void* step_ws = nullptr;
     size_t step_ws_bytes = 0;
+    void* compact_ws = nullptr;
+    size_t compact_ws_bytes = 0;
 };
+
+namespace {
+// the batch arrays compacted after each commit: rid, p, b, K, thr, ids, cs
+inline void compact_row_bytes(int32_t L, int64_t* rb) {
+    for (int k = 0; k < 5; ++k) rb[k] = 4;
+    rb[5] = rb[6] = (int64_t)L * 4;
+}
+}  // namespace
 
 namespace {
 
@@ -94,6 +104,10 @@ size_t carve(dllm_loop* lp, unsigned char* base) {
     lp->new_p_d = (int32_t*)take(cap * 4);
     lp->new_K_d = (int32_t*)take(cap * 4);
     lp->new_thr_d = (float*)take(cap * 4);
+    int64_t rb[7];
+    compact_row_bytes(c.L, rb);
+    lp->compact_ws_bytes = dllm_compact_workspace_size(c.capacity, 7, rb);
+    lp->compact_ws = take(lp->compact_ws_bytes);
     return off;
 }
 
@@ -305,11 +319,14 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
     ca.A = A; ca.n_arrays = 7; ca.evict = lp->evict; ca.new_index = lp->new_index; ca.src_row = lp->src_row;
     ca.A_out = lp->A_out;
     void* arrays[7] = {lp->rid, lp->p, lp->b, lp->K, lp->thr, lp->ids, lp->cs};
-    const int64_t rb[7] = {4, 4, 4, 4, 4, (int64_t)c.L * 4, (int64_t)c.L * 4};
+    int64_t rb[7];
+    compact_row_bytes(c.L, rb);
     for (int k = 0; k < 7; ++k) {
         ca.arrays[k] = arrays[k];
         ca.row_bytes[k] = rb[k];
     }
+    ca.workspace = lp->compact_ws;
+    ca.workspace_bytes = lp->compact_ws_bytes;
     rc = dllm_advance_compact(&aa, &ca, stream);
     if (rc != DLLM_OK) return rc;
     // host mirrors: b += 1 and a fresh block for the advanced rows, evict b >= K

@@ -688,6 +688,16 @@ extern "C" int dllm_advance_compact(const dllm_advance_args* a, const dllm_compa
     P.chunk_rows = P.row_total > 0 ? (int)std::min<long long>(kFusedThreads, kFusedStageBytes / P.row_total)
                                    : kFusedThreads;
     P.new_index = c->new_index; P.src_row = c->src_row; P.A_out = c->A_out;
+    // rows beyond one staging chunk: one CTA would serialise them; with a
+    // compaction workspace, run the multi-CTA advance and compaction instead
+    if ((long long)a->A * P.row_total > kFusedStageBytes && c->workspace &&
+        c->workspace_bytes >= dllm_compact_workspace_size(c->A, c->n_arrays, c->row_bytes)) {
+        const int rc = dllm_advance(a, stream);
+        if (rc != DLLM_OK) return rc;
+        dllm_compact_args c2 = *c;
+        c2.evict = a->evict;
+        return dllm_compact(&c2, stream);
+    }
     int dev = 0;
     DLLM_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return DLLM_ERR_UNSUPPORTED;

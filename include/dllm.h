@@ -400,8 +400,12 @@ typedef struct dllm_compact_args {
  * one launch (one CTA): the batch-management tail of a serving-loop
  * iteration (BlockServe Algorithm 1: commit, b += 1, evict; FDFO page,
  * section "FDFO 的核心思想": done requests leave at once).  Results equal
- * dllm_advance(adv) then dllm_compact(cmp) with cmp->evict = adv->evict;
- * cmp->evict and cmp's workspace are not read.  The compacted arrays may
+ * dllm_advance(adv) then dllm_compact(cmp) with cmp->evict = adv->evict
+ * (cmp->evict is not read).  When the rows of all the arrays exceed one
+ * 96 KiB staging chunk and cmp supplies a workspace of at least
+ * dllm_compact_workspace_size bytes, the call runs exactly those two
+ * (several CTAs each); otherwise one CTA does both and the workspace is
+ * not read.  The compacted arrays may
  * include adv's b / input_ids / conf_state (they are compacted after the
  * commit).  Errors as the two calls, plus DLLM_ERR_INVAL when cmp->A !=
  * adv->A and DLLM_ERR_UNSUPPORTED when a row of all the arrays (each

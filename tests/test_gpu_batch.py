@@ -150,8 +150,9 @@ def test_refill(dllm, device):
 
 
 
+@pytest.mark.parametrize("workspace", [True, False])
 @pytest.mark.parametrize("A,L,K", [(0, 32, 4), (1, 32, 2), (77, 32, 3), (256, 32, 8), (1500, 16, 2), (300, 64, 1)])
-def test_advance_compact_parity(dllm, device, A, L, K):
+def test_advance_compact_parity(dllm, device, A, L, K, workspace):
     """dllm_advance_compact equals the oracle's advance followed by its
     stable compaction (rows of several widths, chunked staging when the
     rows do not fit one chunk)."""
@@ -172,7 +173,8 @@ def test_advance_compact_parity(dllm, device, A, L, K):
     # an odd A adds a 5-byte row array, which takes the byte-copy path
     arrays = [d["rid"], d["K"], d["b"], d["ids"], d["cs"]] + ([d["extra"]] if A % 2 else [])
     evict, new_index, src_row, A_out = dllm.advance_compact(
-        _t(adv, device), d["rid"], d["K"], d["b"], d["ids"], d["cs"], d_gen, arrays, mask_id=V - 1)
+        _t(adv, device), d["rid"], d["K"], d["b"], d["ids"], d["cs"], d_gen, arrays, mask_id=V - 1,
+        workspace=workspace)
     assert int(A_out.cpu().numpy()[0]) == o_A
     if A:
         np.testing.assert_array_equal(evict.cpu().numpy()[:A].astype(bool), o_evict)
