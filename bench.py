@@ -46,6 +46,7 @@ UNIT = "masked positions/s"
 WORKLOADS = {
     "dream": "dream7b_shaped_mixed_state_step",
     "dream_fixed_steps": "dream7b_shaped_mixed_state_step_fixed_steps_S32",
+    "dream_vocab4": "dream7b_shaped_mixed_state_step_4_vocab_shards",
     "llada": "llada8b_shaped_mixed_state_step",
     "stress": "large_batch_stress_step",
     "tiny": "tiny_step",
@@ -89,7 +90,7 @@ FIXED_STEPS_S = 32   # the pages' S = 32 denoising steps per block of L = 32
 def step_config_name(name):
     """Step configuration behind a workload name (the fixed-steps workload
     runs the Dream-shaped batch under the fixed-steps rule)."""
-    return "dream" if name in synth.LOOP_CONFIGS or name == "dream_fixed_steps" else name
+    return "dream" if name in synth.LOOP_CONFIGS or name in ("dream_fixed_steps", "dream_vocab4") else name
 
 
 def make_workload(seed, name="dream"):
@@ -214,7 +215,7 @@ class ClockSampler:
 class Pipeline:
     """Device buffers and prebuilt C-ABI argument structs for one batch."""
 
-    def __init__(self, cfg, inp, reqs, b, gen, pending_p, device, ring=RING, fixed_steps=None):
+    def __init__(self, cfg, inp, reqs, b, gen, pending_p, device, ring=RING, fixed_steps=None, vocab_shards=None):
         import torch
         import denoise_step_token_gb300 as dllm
         self.torch, self.dllm, self.lib = torch, dllm, dllm.load()
@@ -291,6 +292,21 @@ class Pipeline:
         # fixed-steps rule: request b has taken L - (its masked count) steps
         # of its block (one token per step at S = L), so its quota is
         # transfer_quota(L, S, that step)
+        # vocabulary shards: S2 shard by shard (dllm_step_shard), then one merge
+        self.shards = None
+        if vocab_shards:
+            n = int(vocab_shards)
+            width = -(-(cfg.V // n) // 8) * 8
+            bounds = [min(k * width, cfg.V) for k in range(n)] + [cfg.V]
+            BL = B * L
+            self.trip = [torch.empty((n, BL), dtype=dt, device=device) for dt in (torch.float32, torch.float32,
+                                                                                  torch.int32)]
+            self.shards = []
+            for k in range(n):
+                a = dllm.StepArgs.from_buffer_copy(self.args[0][1])
+                a.V = bounds[k + 1] - bounds[k]
+                a.logits = ctypes.c_void_p(self.logits.data_ptr() + bounds[k] * 2)
+                self.shards.append((bounds[k], a))
         self.quota = None
         if fixed_steps is not None:
             steps = L - inp.masked.sum(axis=1)
@@ -350,7 +366,15 @@ class Pipeline:
         rc = lib.dllm_pack(ctypes.byref(pa), stream)
         if ev_before is not None:
             ev_before.record()
-        if compact is not None:
+        if self.shards is not None and compact is None:
+            for k, (v0, a) in enumerate(self.shards):
+                a.input_ids = sa.input_ids
+                rc |= lib.dllm_step_shard(ctypes.byref(a), v0, *(ctypes.c_void_p(t[k].data_ptr()) for t in self.trip),
+                                          stream)
+            rc |= lib.dllm_step_merge(ctypes.byref(sa), len(self.shards), ctypes.c_void_p(self.trip[0].data_ptr()),
+                                      ctypes.c_void_p(self.trip[1].data_ptr()), ctypes.c_void_p(self.trip[2].data_ptr()),
+                                      self.B * self.L, None, stream)
+        elif compact is not None:
             buf, rows = compact
             saved = sa.logits
             sa.logits = ctypes.c_void_p(buf.data_ptr())
@@ -383,7 +407,8 @@ def run_gpu(args, rank, world, local_rank, dist):
     dllm.load()
     cfg, inp, reqs, b, gen, pending_p = make_workload(1000 + rank, args.workload)
     pipe = Pipeline(cfg, inp, reqs, b, gen, pending_p, device,
-                    fixed_steps=FIXED_STEPS_S if args.workload == "dream_fixed_steps" else None)
+                    fixed_steps=FIXED_STEPS_S if args.workload == "dream_fixed_steps" else None,
+                    vocab_shards=4 if args.workload == "dream_vocab4" else None)
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     K, W = args.steps, args.warmup
@@ -797,7 +822,9 @@ def main():
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,
                          "all_rows_logits_bytes_per_launch": cfg.B * cfg.L * cfg.V * 2,
-                         "kernel": "step_kernel (dllm_step_quota)" if fixed else "step_kernel (dllm_step)",
+                         "kernel": ("step_kernel (dllm_step_quota)" if fixed else
+                                    "4 x step_kernel (dllm_step_shard) + merge_kernel" if pipe.shards else
+                                    "step_kernel (dllm_step)"),
                          "algorithmic_bytes_per_launch": alg},
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -109,6 +109,9 @@ _SIGNATURES = {
     "dllm_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
     "dllm_step_quota": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p, _p]),
     "dllm_step_compact": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int64, _p, _p]),
+    "dllm_step_shard": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int32, _p, _p, _p, _p]),
+    "dllm_step_merge": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int32, _p, _p, _p, ctypes.c_int64, _p,
+                                       _p]),
     "dllm_predict_steps_stub": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_int32, _p, _p, _p, _p]),
     "dllm_load_control": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_double, _p]),
     "dllm_slo_thresholds": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p, _p, _p]),
@@ -311,6 +314,52 @@ def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=Fa
         _check("dllm_step", lib.dllm_step(ctypes.byref(a), _stream(dev)))
     else:
         _check("dllm_step_quota", lib.dllm_step_quota(ctypes.byref(a), _ptr(quota), _stream(dev)))
+    return out
+
+
+def step_sharded(logits, input_ids, thr, conf_state, *, V, mask_id, bounds, feats=True, debug=False, quota=None):
+    """The step with S2 split over vocabulary shards [bounds[k], bounds[k+1])
+    of one logits array (dllm_step_shard per shard, then dllm_step_merge):
+    the single-GPU form of a vocabulary-parallel or chunked LM head.  Each
+    bound must be a multiple of 8.  Returns the outputs of ``step``."""
+    torch = _torch()
+    dev = _require_cuda(logits, input_ids, conf_state, thr, quota)
+    B, L = input_ids.shape
+    ldv = logits.shape[-1]
+    BL = B * L
+    n = len(bounds) - 1
+    if n < 1 or bounds[0] != 0 or bounds[-1] != V or any(b % 8 for b in bounds[:-1]):
+        raise ValueError("bounds must run from 0 to V in multiples of 8")
+    tm = torch.empty((n, BL), dtype=torch.float32, device=dev)
+    ts = torch.empty((n, BL), dtype=torch.float32, device=dev)
+    ti = torch.empty((n, BL), dtype=torch.int32, device=dev)
+    lib = load()
+    base = logits.data_ptr()
+    for k in range(n):
+        v0, v1 = bounds[k], bounds[k + 1]
+        need = int(lib.dllm_step_workspace_size(B, L, v1 - v0))
+        ws = _step_ws.get(dev, need)
+        a = StepArgs(B=B, L=L, V=v1 - v0, mask_id=mask_id, ldv=ldv, logits=ctypes.c_void_p(base + v0 * 2),
+                     input_ids=_ptr(input_ids), workspace=_ptr(ws), workspace_bytes=ws.numel())
+        _check("dllm_step_shard", lib.dllm_step_shard(ctypes.byref(a), v0, _ptr(tm[k]), _ptr(ts[k]), _ptr(ti[k]),
+                                                      _stream(dev)))
+    out = {"done": torch.empty(B, dtype=torch.uint8, device=dev),
+           "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "n_new": torch.empty(B, dtype=torch.int32, device=dev)}
+    if feats:
+        out["feats"] = torch.empty((B, NUM_FEATURES), dtype=torch.float32, device=dev)
+    if debug:
+        out["conf"] = torch.full((B, L), float("nan"), dtype=torch.float32, device=dev)
+        out["lse"] = torch.full((B, L), float("nan"), dtype=torch.float32, device=dev)
+        out["tok"] = torch.full((B, L), -1, dtype=torch.int32, device=dev)
+    ws = _step_ws.get(dev, int(lib.dllm_step_workspace_size(B, L, 1)))
+    a = StepArgs(B=B, L=L, V=V, mask_id=mask_id, ldv=ldv, logits=None, input_ids=_ptr(input_ids), thr=_ptr(thr),
+                 conf_state=_ptr(conf_state), done=_ptr(out["done"]), accept_len=_ptr(out["accept_len"]),
+                 n_new=_ptr(out["n_new"]), feats=_ptr(out.get("feats")), conf_out=_ptr(out.get("conf")),
+                 lse_out=_ptr(out.get("lse")), tok_out=_ptr(out.get("tok")), workspace=_ptr(ws),
+                 workspace_bytes=ws.numel())
+    _check("dllm_step_merge", lib.dllm_step_merge(ctypes.byref(a), n, _ptr(tm), _ptr(ts), _ptr(ti), BL, _ptr(quota),
+                                                  _stream(dev)))
     return out
 
 

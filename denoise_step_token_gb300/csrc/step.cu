@@ -40,6 +40,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <string.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -142,6 +144,11 @@ struct StepParams {
     int B, L, V, NC, BL, mask_id, list_cap, static_cap, zero_cap;
     int compact;              // logits rows hold only the masked positions, by rank
     long long logits_rows;    // rows of a compact logits array
+    int shard;                // S2 only, over a vocabulary shard starting at token v0
+    int v0;
+    float* trip_m;            // [BL] shard max, sum of exp, global argmax
+    float* trip_s;
+    int* trip_i;
     FastDiv div_nc, div_g;   // division by NC and by the grid size
     long long ldv;
     const uint16_t* logits;
@@ -385,7 +392,7 @@ __device__ __forceinline__ void warp_features(const float (&val)[NK], const bool
 // workspace).
 // ---------------------------------------------------------------------------
 template <int NK>
-__device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool has_masked, int lane) {
+__device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool has_masked, int lane, bool direct) {
     // Row results arrive as zero-at-rest words (polled until they land);
     // requests without masked rows read only the launch's inputs.
     const int L = P.L;
@@ -411,7 +418,7 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     }
     // the scan count guards only the commit at the end: loaded after the
     // block's loads so that its acquire does not hold them back
-    const int scanned = (lane == 0 && has_masked) ? ld_acquire_gpu(P.ctl) : 0;
+    const int scanned = (lane == 0 && has_masked && !direct) ? ld_acquire_gpu(P.ctl) : 0;
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
@@ -520,7 +527,7 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     // last CTA commits (the add's high half counts the list's entries).
     if (!has_masked) return;
     __syncwarp();   // lane 0's acquire of the scan count orders the warp's writes
-    if (__shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
+    if (direct || __shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
 #pragma unroll
         for (int k = 0; k < NK; ++k) {
             if (selk[k]) P.ids[base + lane + 32 * k] = id[k];
@@ -532,12 +539,14 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     if (lane == 0) P.cnt[P.BL + b] = 0;   // request counter back to rest
 }
 
-__device__ __forceinline__ void finalize_request(const StepParams& P, int b, bool has_masked, int lane) {
+// direct: input_ids may be written at once (no other CTA still scans them).
+__device__ __forceinline__ void finalize_request(const StepParams& P, int b, bool has_masked, int lane,
+                                                 bool direct = false) {
     const int nk = (P.L + 31) >> 5;
-    if (nk <= 1) finalize_request_t<1>(P, b, has_masked, lane);
-    else if (nk <= 2) finalize_request_t<2>(P, b, has_masked, lane);
-    else if (nk <= 4) finalize_request_t<4>(P, b, has_masked, lane);
-    else finalize_request_t<32>(P, b, has_masked, lane);
+    if (nk <= 1) finalize_request_t<1>(P, b, has_masked, lane, direct);
+    else if (nk <= 2) finalize_request_t<2>(P, b, has_masked, lane, direct);
+    else if (nk <= 4) finalize_request_t<4>(P, b, has_masked, lane, direct);
+    else finalize_request_t<32>(P, b, has_masked, lane, direct);
 }
 
 // ---------------------------------------------------------------------------
@@ -556,7 +565,7 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     // finalises it, polling for the words of rows other warps are still
     // finishing.
     int old = 0;
-    if (lane == 0) old = atom_add_relaxed_gpu(P.cnt + P.BL + b, 1);
+    if (lane == 0 && !P.shard) old = atom_add_relaxed_gpu(P.cnt + P.BL + b, 1);
     // masked rows of this request at entry, from this CTA's scan bitmask
     int mb = 0;
     {
@@ -619,6 +628,15 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
     best = __reduce_min_sync(0xffffffffu, best);
     const float conf = __fdiv_rn(1.0f, S);
     const float lse = M + logf(S);
+    if (P.shard) {   // S2 of a vocabulary shard: the row's triple, nothing else
+        if (lane == 0) {
+            P.trip_m[row] = M;
+            P.trip_s[row] = S;
+            P.trip_i[row] = best == 0xffffffffu ? -1 : (int)best + P.v0;
+            P.cnt[row] = 0;
+        }
+        return;
+    }
     // publish the row's word (relaxed: the request's finalizer polls)
     if (lane == 0) {
         P.row_tok[row] = (int)best;
@@ -1062,7 +1080,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             __threadfence();
             atomicAdd(P.ctl, 1);   // this CTA no longer reads input_ids' entry state
         }
-        for (int k = warp - kFirstFinisher; k < s_nzero; k += kFinishWarps) finalize_request(P, s_zero[k], false, lane);
+        if (!P.shard)
+            for (int k = warp - kFirstFinisher; k < s_nzero; k += kFinishWarps)
+                finalize_request(P, s_zero[k], false, lane);
         drain_queue(P, s_gmask, s_queue, &s_qhead, &s_ndone, lane);
     }
 
@@ -1120,6 +1140,44 @@ __global__ void __launch_bounds__(256) features_kernel(int B, int L, int mask_id
     else features_one<32>(b, L, mask_id, ids, cs, feats, lane);
 }
 
+// ---------------------------------------------------------------------------
+// Merge of vocabulary-shard triples, then S3-S6: one warp per request.
+// Shard k's triple of position r is at m/s/idx[k * stride + r]; the shards
+// are folded in order with the finisher's combine (so the lowest global
+// argmax wins ties when the shards ascend through the vocabulary).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ StepParams P, int n_shards,
+                                                    const float* __restrict__ tm, const float* __restrict__ ts,
+                                                    const int* __restrict__ ti, long long stride) {
+    pdl_wait();      // the triples and the batch state come from earlier kernels
+    pdl_release();
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= P.B) return;
+    bool any = false;
+    for (int j = lane; j < P.L; j += 32) {
+        const long long r = (long long)b * P.L + j;
+        if (P.ids[r] != P.mask_id) continue;
+        any = true;
+        float M = -INFINITY, S = 0.f;
+        int tok = -1;
+        for (int k = 0; k < n_shards; ++k) {
+            const float mk = tm[k * stride + r];
+            if (mk > M || tok < 0) tok = ti[k * stride + r];
+            combine(M, S, mk, ts[k * stride + r]);
+        }
+        const float conf = __fdiv_rn(1.0f, S);
+        if (P.conf_out) P.conf_out[r] = conf;
+        if (P.lse_out) P.lse_out[r] = M + logf(S);
+        if (P.tok_out) P.tok_out[r] = tok;
+        P.row_tok[r] = tok;
+        st_relaxed_gpu_u64(P.row_word + r, pack_row(conf, tok));
+    }
+    any = __any_sync(0xffffffffu, any);
+    __syncwarp();
+    finalize_request(P, b, any, lane, true);
+}
+
 int g_smem_configured[64];
 
 struct LaunchFacts {
@@ -1149,15 +1207,26 @@ extern "C" int dllm_workspace_init(void* workspace, size_t bytes, void* stream) 
 namespace dllm {
 namespace {
 
-// dllm_step and dllm_step_quota: quota null selects the threshold rule.
-int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, void* stream) {
+struct ShardOut {
+    int v0;
+    float* m;
+    float* s;
+    int* idx;
+};
+
+// Host checks and launch of step_kernel.  quota null selects the threshold
+// rule; logits_rows >= 0 the compact layout; shard non-null S2 alone over a
+// vocabulary shard.
+int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
+                void* stream) {
     if (!a) return DLLM_ERR_INVAL;
     if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
     if (a->B == 0) return DLLM_OK;
     if ((long long)a->B * a->L > 0x7fffffffLL || a->B >= (1 << 16)) return DLLM_ERR_UNSUPPORTED;
-    if (!a->logits || !a->input_ids || (!quota && !a->thr) || !a->conf_state || !a->done || !a->accept_len ||
-        !a->n_new)
+    if (!a->logits || !a->input_ids) return DLLM_ERR_INVAL;
+    if (!shard && ((!quota && !a->thr) || !a->conf_state || !a->done || !a->accept_len || !a->n_new))
         return DLLM_ERR_INVAL;
+    if (shard && (!shard->m || !shard->s || !shard->idx || shard->v0 < 0)) return DLLM_ERR_INVAL;
     if ((a->ldv % 8) != 0 || (reinterpret_cast<uintptr_t>(a->logits) & 15u) != 0) return DLLM_ERR_ALIGN;
     if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return DLLM_ERR_WORKSPACE;
     WsLayout w;
@@ -1210,6 +1279,11 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
     P.div_nc = make_fastdiv((uint32_t)NC);
     P.compact = logits_rows >= 0 ? 1 : 0;
     P.logits_rows = logits_rows;
+    P.shard = shard ? 1 : 0;
+    P.v0 = shard ? shard->v0 : 0;
+    P.trip_m = shard ? shard->m : nullptr;
+    P.trip_s = shard ? shard->s : nullptr;
+    P.trip_i = shard ? shard->idx : nullptr;
     P.div_g = make_fastdiv((uint32_t)G);
     P.logits = a->logits; P.ids = a->input_ids; P.thr = a->thr; P.quota = quota; P.cs = a->conf_state;
     P.done = a->done; P.accept = a->accept_len; P.n_new = a->n_new; P.feats = a->feats;
@@ -1229,16 +1303,53 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
 }  // namespace
 }  // namespace dllm
 
-extern "C" int dllm_step(const dllm_step_args* a, void* stream) { return launch_step(a, nullptr, -1, stream); }
+extern "C" int dllm_step(const dllm_step_args* a, void* stream) { return launch_step(a, nullptr, -1, nullptr, stream); }
 
 extern "C" int dllm_step_quota(const dllm_step_args* a, const int32_t* quota, void* stream) {
     if (!quota) return DLLM_ERR_INVAL;
-    return launch_step(a, quota, -1, stream);
+    return launch_step(a, quota, -1, nullptr, stream);
 }
 
 extern "C" int dllm_step_compact(const dllm_step_args* a, int64_t logits_rows, const int32_t* quota, void* stream) {
     if (logits_rows < 0) return DLLM_ERR_INVAL;
-    return launch_step(a, quota, logits_rows, stream);
+    return launch_step(a, quota, logits_rows, nullptr, stream);
+}
+
+extern "C" int dllm_step_shard(const dllm_step_args* a, int32_t v0, float* m, float* s, int32_t* idx, void* stream) {
+    ShardOut sh{v0, m, s, idx};
+    return launch_step(a, nullptr, -1, &sh, stream);
+}
+
+extern "C" int dllm_step_merge(const dllm_step_args* a, int32_t n_shards, const float* m, const float* s,
+                               const int32_t* idx, int64_t shard_stride, const int32_t* quota, void* stream) {
+    if (!a || a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1) return DLLM_ERR_INVAL;
+    if (a->B == 0) return DLLM_OK;
+    if ((long long)a->B * a->L > 0x7fffffffLL || a->B >= (1 << 16)) return DLLM_ERR_UNSUPPORTED;
+    if (n_shards < 1 || !m || !s || !idx || shard_stride < (int64_t)a->B * a->L) return DLLM_ERR_INVAL;
+    if (!a->input_ids || (!quota && !a->thr) || !a->conf_state || !a->done || !a->accept_len || !a->n_new)
+        return DLLM_ERR_INVAL;
+    if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return DLLM_ERR_WORKSPACE;
+    WsLayout w;   // only the zero-at-rest row words and the data end are used: any V lays them out
+    if (!ws_layout(a->B, a->L, 1, a->workspace_bytes, &w)) return DLLM_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+    unsigned char* data = ws + ((a->workspace_bytes - w.data_bytes) & ~size_t(255));
+    StepParams P;
+    memset(&P, 0, sizeof(P));
+    P.B = a->B; P.L = a->L; P.V = a->V; P.BL = a->B * a->L; P.mask_id = a->mask_id;
+    P.ids = a->input_ids; P.thr = a->thr; P.quota = quota; P.cs = a->conf_state;
+    P.done = a->done; P.accept = a->accept_len; P.n_new = a->n_new; P.feats = a->feats;
+    P.conf_out = a->conf_out; P.lse_out = a->lse_out; P.tok_out = a->tok_out;
+    P.ctl = reinterpret_cast<int*>(ws);
+    P.cnt = reinterpret_cast<int*>(ws + 64);
+    P.row_word = reinterpret_cast<unsigned long long*>(ws + w.off_row);
+    P.row_tok = reinterpret_cast<int*>(data + w.off_tok);
+    P.sel = data + w.off_sel;
+    P.err = error_word_ptr();
+    if (!P.err) return DLLM_ERR_CUDA;
+    const int wpb = 8;
+    DLLM_CUDA_TRY(launch_dependent(merge_kernel, dim3((a->B + wpb - 1) / wpb), dim3(wpb * 32), 0, as_stream(stream), P,
+                                   n_shards, m, s, idx, (long long)shard_stride));
+    return DLLM_OK;
 }
 
 extern "C" int32_t dllm_transfer_quota(int32_t L, int32_t S, int32_t s) {

@@ -187,6 +187,30 @@ int dllm_step_quota(const dllm_step_args* args, const int32_t* quota, void* stre
  * workspace stays valid).  DLLM_ERR_INVAL for logits_rows < 0. */
 int dllm_step_compact(const dllm_step_args* args, int64_t logits_rows, const int32_t* quota, void* stream);
 
+/* S1-S2 over one vocabulary shard (a vocabulary-parallel LM head -- the
+ * tensor parallelism of the DiLaServe review, section 2.2.2 -- or an LM head
+ * computed in vocabulary chunks).  args->logits points at the shard's first
+ * column, global token v0 (v0 % 8 == 0 keeps the rows 16-byte aligned),
+ * args->V is the shard's width and args->ldv the full row stride.  For every
+ * masked position r (input_ids[r] == mask_id) it writes the shard's triple
+ * m[r] = max, s[r] = sum of exp(x - m) over the shard, idx[r] = the lowest
+ * global index attaining m; nothing else (input_ids unchanged; thr,
+ * conf_state and the outputs are not read or written).  m, s, idx: device
+ * [B * L].  The workspace rules are dllm_step's (sized for the shard's V). */
+int dllm_step_shard(const dllm_step_args* args, int32_t v0, float* m, float* s, int32_t* idx, void* stream);
+
+/* S3-S6 from the triples of n_shards vocabulary shards: shard k's triple of
+ * position r at m / s / idx[k * shard_stride + r] (device), shards in
+ * ascending vocabulary order.  They are folded in that order as the step's
+ * finisher folds chunk partials (M = max, S = sum of s_k exp(m_k - M), the
+ * first shard attaining M gives the token: the lowest global index), then
+ * selection, update, done and features exactly as dllm_step (quota NULL:
+ * threshold rule; else the fixed-steps rule).  args->logits is not read; the
+ * workspace must be sized for (B, L, any V >= 1).  Errors as dllm_step, plus
+ * DLLM_ERR_INVAL for n_shards < 1, shard_stride < B * L or NULL triples. */
+int dllm_step_merge(const dllm_step_args* args, int32_t n_shards, const float* m, const float* s,
+                    const int32_t* idx, int64_t shard_stride, const int32_t* quota, void* stream);
+
 /* Host.  The fixed-steps quota of step s (0-based) of a block (BlockServe
  * page, section II-E): L spread evenly over S steps, floor(L / S) per step
  * plus one for each of the first L mod S steps; a step past the schedule

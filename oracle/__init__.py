@@ -84,6 +84,45 @@ def rows_stats(logits_bits, rows, V):
     return conf, lse, tok
 
 
+def shard_triple(x, v0):
+    """S2 over one vocabulary shard: (max m, sum_j exp(x_j - m), lowest
+    global index attaining m) of the shard's values ``x`` (float64), whose
+    first column is global token ``v0``.  A vocabulary-parallel LM head
+    (DiLaServe review, section 2.2.2: tensor parallelism) or a chunked one
+    hands the step one such shard at a time."""
+    m = x.max()
+    return float(m), float(np.exp(x - m).sum()), int(v0 + np.flatnonzero(x == m)[0])
+
+
+def merge_triples(triples):
+    """Fold per-shard (m, s, idx) triples, in shard order (ascending
+    vocabulary ranges), into the row's (conf, lse, tok): M = max m_k,
+    S = sum_k s_k exp(m_k - M), tok = the idx of the first shard attaining M
+    (its lowest index, the shards being ordered); conf = 1/S, lse = M + ln S,
+    as ``row_stats`` of the whole row."""
+    M = max(t[0] for t in triples)
+    S = sum(t[1] * np.exp(t[0] - M) for t in triples)
+    tok = next(t[2] for t in triples if t[0] == M)
+    return 1.0 / S, M + np.log(S), tok
+
+
+def step_sharded(logits_bits, V, bounds, input_ids, thr, conf_state, mask_id, quota=None):
+    """``step`` with S2 computed shard by shard over the vocabulary ranges
+    [bounds[k], bounds[k+1]) and merged (``shard_triple``, ``merge_triples``);
+    S3-S6 as ``step``."""
+    input_ids = np.asarray(input_ids)
+    B, L = input_ids.shape
+    rows = np.flatnonzero((input_ids == mask_id).reshape(-1))
+    conf = np.empty(len(rows))
+    lse = np.empty(len(rows))
+    tok = np.empty(len(rows), dtype=np.int64)
+    for i, r in enumerate(rows):
+        x = bf16_to_f64(logits_bits[r, :V])
+        tr = [shard_triple(x[bounds[k]:bounds[k + 1]], bounds[k]) for k in range(len(bounds) - 1)]
+        conf[i], lse[i], tok[i] = merge_triples(tr)
+    return _finish_step(input_ids, thr, conf_state, mask_id, rows, conf, lse, tok, quota)
+
+
 # ---------------------------------------------------------------------------
 # S3: LowConfidence selection with fallback.
 # ---------------------------------------------------------------------------
@@ -212,14 +251,20 @@ def step(logits_bits, V, input_ids, thr, conf_state, mask_id, quota=None):
     entry).  Inputs are not modified.
     """
     input_ids = np.array(input_ids, dtype=np.int64)
+    rows = np.flatnonzero((input_ids == mask_id).reshape(-1))      # S1
+    c, l, t = rows_stats(logits_bits, rows, V)                      # S2
+    return _finish_step(input_ids, thr, conf_state, mask_id, rows, c, l, t, quota)
+
+
+def _finish_step(input_ids, thr, conf_state, mask_id, rows, c, l, t, quota):
+    """S3-S6 of ``step`` from the masked rows' (conf, lse, tok)."""
+    input_ids = np.array(input_ids, dtype=np.int64)
     conf_state = np.array(conf_state, dtype=np.float64)
     B, L = input_ids.shape
-    masked = input_ids == mask_id                                   # S1
+    masked = input_ids == mask_id
     conf = np.full((B, L), np.nan)
     lse = np.full((B, L), np.nan)
     tok = np.full((B, L), -1, dtype=np.int64)
-    rows = np.flatnonzero(masked.reshape(-1))
-    c, l, t = rows_stats(logits_bits, rows, V)                      # S2
     conf.reshape(-1)[rows] = c
     lse.reshape(-1)[rows] = l
     tok.reshape(-1)[rows] = t

@@ -265,3 +265,40 @@ def test_compact_logits_too_few_rows_is_reported(dllm, device):
     ref = oracle_step(inp)
     got, ids2, cs2 = run_gpu(dllm, inp, device)
     compare_step(ref, got, list(range(cfg.B)), cfg.L, ids2, cs2)
+
+
+@pytest.mark.parametrize("name,bounds", [("ragged", [0, 16000, 40001]), ("l64", [0, 8, 4096, 20000, 33000]),
+                                         ("all_masked", [0, 20000]), ("tiny", [0, 512, 1024])])
+def test_vocab_sharded_step(dllm, device, name, bounds):
+    """dllm_step_shard over vocabulary shards of one logits array, then
+    dllm_step_merge: equal to the oracle (tokens exact, confidences within
+    1e-5) and to the unsharded step's tokens."""
+    cfg = SMALL_CASES[name] if name in SMALL_CASES else synth.STEP_CONFIGS[name]
+    inp = synth.make_step_state(cfg, 13)
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    full, ids_f, _ = run_gpu(dllm, inp, device)
+    logits = device_logits(inp, device)
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step_sharded(logits, ids, thr, cs, V=cfg.V, mask_id=cfg.mask_id, bounds=bounds, debug=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+    assert np.array_equal(got["tok"], full["tok"]) and np.array_equal(ids.cpu().numpy(), ids_f)
+
+
+def test_vocab_sharded_dream_sampled(dllm, device):
+    cfg = synth.STEP_CONFIGS["dream"]
+    inp = synth.make_step_state(cfg, 14)
+    rng = np.random.default_rng(6)
+    sample = sorted(rng.choice(cfg.B, size=10, replace=False).tolist())
+    enforce_margins(inp, sample)
+    ref = oracle_step(inp, sample)
+    logits = device_logits(inp, device)
+    ids, thr, cs = device_state(inp, device)
+    # four shards of a tensor-parallel LM head (V / 4 rounded to 8)
+    out = dllm.step_sharded(logits, ids, thr, cs, V=cfg.V, mask_id=cfg.mask_id,
+                            bounds=[0, 37984, 75968, 113952, cfg.V], debug=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, sample, cfg.L, ids.cpu().numpy(), cs.cpu().numpy())

@@ -698,3 +698,43 @@ def test_slo_threshold_hand_cases():
     assert slo_threshold(steps, 0.01, 1.0) == 2
     assert slo_threshold(steps, 0.01, 1.0, max_allowed=0) == 0
     assert slo_threshold(steps, 0.01, 0.05) == 0          # nothing fits: the fastest
+
+
+# --------------------------------------------------------------------------
+# Vocabulary-sharded S2 (triples and their merge)
+# --------------------------------------------------------------------------
+def test_merged_shard_triples_equal_the_whole_row():
+    # exp(a - M) = exp(a - m) exp(m - M): the shards' sums rescaled to the
+    # global max add up to the whole row's sum, and the first shard holding
+    # the max holds its lowest index
+    rng = np.random.default_rng(16)
+    for _ in range(200):
+        V = int(rng.integers(2, 300))
+        x = oracle.bf16_to_f64(synth.f32_to_bf16_bits(rng.normal(size=V).astype(np.float32) * 2))
+        if rng.random() < 0.3:                       # a tie across shards
+            x[int(rng.integers(0, V))] = x.max()
+        cuts = sorted(set(rng.integers(1, V, size=int(rng.integers(0, 4))).tolist()))
+        bounds = [0] + cuts + [V]
+        tr = [oracle.shard_triple(x[bounds[k]:bounds[k + 1]], bounds[k]) for k in range(len(bounds) - 1)]
+        conf, lse, tok = oracle.merge_triples(tr)
+        c0, l0, t0 = oracle.row_stats(x)
+        assert tok == t0
+        assert conf == pytest.approx(c0, rel=1e-12)
+        assert lse == pytest.approx(l0, rel=1e-12, abs=1e-12)
+    # one shard is the row itself
+    x = np.array([0.5, 2.0, 2.0, -1.0])
+    m, s, i = oracle.shard_triple(x, 0)
+    assert (m, i) == (2.0, 1) and 1.0 / s == pytest.approx(oracle.row_stats(x)[0], rel=1e-15)
+
+
+def test_step_sharded_equals_step():
+    cfg = synth.StepConfig("sh", 4, 8, 200, 6.0, "fraction", (0.5, 0.7, 0.9))
+    inp = synth.make_step_state(cfg, 2)
+    rows = np.flatnonzero(inp.masked.reshape(-1))
+    logits = np.full((cfg.B * cfg.L, cfg.row_stride), synth.POISON_BITS, dtype=np.uint16)
+    synth.fill_logits_rows(logits, cfg.V, rows, synth.step_row_keys(inp, rows), cfg.offset_max, cfg.mask_id)
+    ref = oracle.step(logits, cfg.V, inp.input_ids, inp.thr, inp.conf_state, cfg.mask_id)
+    got = oracle.step_sharded(logits, cfg.V, [0, 64, 136, 200], inp.input_ids, inp.thr, inp.conf_state, cfg.mask_id)
+    for k in ("input_ids", "done", "n_new", "accept_len", "tok"):
+        np.testing.assert_array_equal(got[k], ref[k])
+    np.testing.assert_allclose(got["conf"], ref["conf"], rtol=1e-12, equal_nan=True)
