@@ -302,3 +302,73 @@ def test_vocab_sharded_dream_sampled(dllm, device):
     got = {k: v.cpu().numpy() for k, v in out.items()}
     assert dllm.get_device_error(device) == 0
     compare_step(ref, got, sample, cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+
+
+def test_steps_on_two_streams_with_their_own_workspaces(dllm, device):
+    """Two batches stepped concurrently on two streams, each with its own
+    workspace, give the same results as one after the other."""
+    import torch
+    cases = [synth.make_step_state(SMALL_CASES["ragged"], 21), synth.make_step_state(SMALL_CASES["l64"], 22)]
+    for inp in cases:
+        enforce_margins(inp)
+    refs = [oracle_step(inp) for inp in cases]
+    streams = [torch.cuda.Stream(device=device) for _ in cases]
+    state = []
+    for inp, st in zip(cases, streams):
+        logits = device_logits(inp, device)
+        ids, thr, cs = device_state(inp, device)
+        ws = torch.zeros(dllm.step_workspace_size(inp.cfg.B, inp.cfg.L, inp.cfg.V), dtype=torch.uint8, device=device)
+        state.append((inp, logits, ids, thr, cs, ws, st))
+    torch.cuda.synchronize()
+    outs = []
+    for inp, logits, ids, thr, cs, ws, st in state:
+        with torch.cuda.stream(st):
+            outs.append(dllm.step(logits, ids, thr, cs, V=inp.cfg.V, mask_id=inp.cfg.mask_id, debug=True,
+                                  workspace=ws))
+    torch.cuda.synchronize()
+    assert dllm.get_device_error(device) == 0
+    for (inp, logits, ids, thr, cs, ws, st), out, ref in zip(state, outs, refs):
+        got = {k: v.cpu().numpy() for k, v in out.items()}
+        compare_step(ref, got, list(range(inp.cfg.B)), inp.cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+
+
+def test_pipeline_captured_in_a_cuda_graph(dllm, device):
+    """pack, step and the fused commit/compaction (launched as programmatic
+    dependents) captured in a CUDA graph: a replay equals eager execution."""
+    import ctypes
+    import torch
+    import bench
+    cfg, inp, reqs, b, gen, pending_p = bench.make_workload(31, "tiny")
+    results = []
+    for use_graph in (False, True):
+        pipe = bench.Pipeline(cfg, inp, reqs, b, gen, pending_p, device, ring=2)
+        lib = pipe.lib
+        stream = torch.cuda.Stream(device=device)
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        pa, sa, aa, ca = pipe.args[0]
+
+        def body():
+            rc = lib.dllm_pack(ctypes.byref(pa), sh)
+            rc |= lib.dllm_step(ctypes.byref(sa), sh)
+            rc |= lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), sh)
+            assert rc == 0
+
+        with torch.cuda.stream(stream):
+            body()                        # first calls: per-device set-up outside any capture
+            torch.cuda.synchronize()
+            pipe.restore()
+            torch.cuda.synchronize()
+            if use_graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    body()
+                pipe.restore()
+                torch.cuda.synchronize()
+                g.replay()
+            else:
+                body()
+        torch.cuda.synchronize()
+        assert dllm.get_device_error(device) == 0
+        results.append((pipe.state[0].cpu().numpy(), pipe.done[0].cpu().numpy(), pipe.box_ids.cpu().numpy()))
+    for a, b2 in zip(results[0], results[1]):
+        np.testing.assert_array_equal(a, b2)
