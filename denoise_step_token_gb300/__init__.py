@@ -31,6 +31,7 @@ __all__ = ["load", "step", "step_host", "features", "pack_plan", "admit", "pack"
 
 LIB_PATH = _build.LIB_PATH
 NUM_FEATURES = 6
+ABI_VERSION = 2        # include/dllm.h DLLM_ABI_VERSION this binding was written for
 COMPACT_MAX_ARRAYS = 16
 
 DLLM_OK = 0
@@ -169,6 +170,8 @@ def load(build=True):
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
+        if lib.dllm_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"libdllm ABI version {lib.dllm_abi_version()}, binding expects {ABI_VERSION}")
         for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs, LoopConfig, LoopInfo)):
             if lib.dllm_struct_size(which) != ctypes.sizeof(cls):
                 raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {lib.dllm_struct_size(which)} "

@@ -1,8 +1,11 @@
 // Mixed-state batch management around the step (S7-S9):
 //   dllm_pack_plan / dllm_admit  host planning by eq. (1) and sand-fill,
 //   dllm_pack                    the left-padded bounding box,
+//   dllm_pack_block              its active-block columns only (in-place re-loop),
 //   dllm_advance                 block commit, b += 1, eviction flags,
-//   dllm_compact                 stable in-place compaction of row arrays.
+//   dllm_compact                 stable in-place compaction of row arrays,
+//   dllm_advance_compact         both of the last two in one launch,
+//   dllm_refill                  appending admitted requests.
 // BlockServe page ("BlockServe: 块粒度连续批处理实现高吞吐扩散大语言模型服务"),
 // sections II-C (Algorithm 1), II-D (eq. (1), sand-fill admission) and II-E
 // (logical position alignment, gather/scatter of the active block); FDFO page,

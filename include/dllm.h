@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DLLM_ABI_VERSION 1
+#define DLLM_ABI_VERSION 2
 
 #define DLLM_OK 0
 #define DLLM_ERR_INVAL (-1)       /* a size, pointer or value is out of range */

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(lib, n), n
     assert set(dllm.exported_symbols()) <= set(names)
-    assert lib.dllm_abi_version() == 1
+    assert lib.dllm_abi_version() == dllm.ABI_VERSION
 
 
 def test_struct_sizes_match_binding():
