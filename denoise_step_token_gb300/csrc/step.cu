@@ -307,9 +307,69 @@ __device__ __forceinline__ void combine(float& m, float& s, float mo, float so) 
 // Writes feats[0..5].  NK is a compile-time bound so that every array
 // index is a constant and the arrays stay in registers.
 // ---------------------------------------------------------------------------
+// Order-preserving 32-bit image of a float (for sorting): negative values
+// have every bit flipped, non-negative ones only the sign bit.
+__device__ __forceinline__ uint32_t float_order_key(float v) {
+    const uint32_t b = __float_as_uint(v + 0.0f);   // -0 sorts as +0
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float float_from_order_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Features of a block of at most 32 positions (one per lane): the unmasked
+// values are sorted by a 32-lane bitonic network on (value, position) --
+// positions outside U sort last -- and the order statistics are read from
+// their lanes.  Same results as the general rank count below.
+__device__ __forceinline__ void warp_features_32(float val, bool inU, int L, int lane, float* feats_out) {
+    const int n = __reduce_add_sync(0xffffffffu, inU ? 1u : 0u);
+    float sum = inU ? val : 0.f;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    float f[6];
+    if (n == 0) {
+        f[0] = f[1] = f[2] = f[3] = f[4] = __int_as_float(0x7fc00000);
+        f[5] = 0.f;
+    } else {
+        unsigned long long key = ((unsigned long long)(inU ? float_order_key(val) : 0xffffffffu) << 32) |
+                                 (unsigned)lane;
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, j);
+                const bool take_min = ((lane & k) == 0) == ((lane & j) == 0);
+                key = take_min ? (other < key ? other : key) : (other > key ? other : key);
+            }
+        }
+        const uint32_t hi = (uint32_t)(key >> 32);   // lane r: the r-th smallest value of U
+        const float qs[3] = {0.25f, 0.5f, 0.75f};
+        float lo_v[3], hi_v[3], frac[3];
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            const float h = qs[t] * float(n - 1);
+            const int lo = int(floorf(h));
+            frac[t] = h - float(lo);
+            lo_v[t] = float_from_order_key(__shfl_sync(0xffffffffu, hi, lo));
+            hi_v[t] = float_from_order_key(__shfl_sync(0xffffffffu, hi, min(lo + 1, n - 1)));
+        }
+        f[0] = float_from_order_key(__shfl_sync(0xffffffffu, hi, 0));
+        f[1] = lo_v[0] + frac[0] * (hi_v[0] - lo_v[0]);
+        f[2] = lo_v[1] + frac[1] * (hi_v[1] - lo_v[1]);
+        f[3] = sum / float(n);
+        f[4] = lo_v[2] + frac[2] * (hi_v[2] - lo_v[2]);
+        f[5] = float(n) / float(L);
+    }
+    if (lane < 6) feats_out[lane] = f[lane];
+}
+
 template <int NK>
 __device__ __forceinline__ void warp_features(const float (&val)[NK], const bool (&inU)[NK], int L, int lane,
                                               float* feats_out) {
+    if constexpr (NK == 1) {
+        warp_features_32(val[0], inU[0], L, lane, feats_out);
+        return;
+    }
     int n = 0;
     float sum = 0.f;
 #pragma unroll
@@ -329,22 +389,23 @@ __device__ __forceinline__ void warp_features(const float (&val)[NK], const bool
         f[0] = f[1] = f[2] = f[3] = f[4] = __int_as_float(0x7fc00000);
         f[5] = 0.f;
     } else {
-        // rank of each of my values among U (ties broken by position)
+        // rank of each of my values among U (ties broken by position); the
+        // update is branch-free so the shuffles of successive sources
+        // overlap instead of waiting one by one
         int rank[NK];
 #pragma unroll
         for (int k = 0; k < NK; ++k) rank[k] = 0;
 #pragma unroll
         for (int kk = 0; kk < NK; ++kk) {
-#pragma unroll 4
+#pragma unroll (NK == 1 ? 32 : 4)
             for (int src = 0; src < 32; ++src) {
                 const int jj = src + 32 * kk;
                 const float vo = __shfl_sync(0xffffffffu, val[kk], src);
-                const bool uo = __shfl_sync(0xffffffffu, inU[kk] ? 1 : 0, src) != 0;
-                if (!uo || jj >= L) continue;
+                const bool uo = (__shfl_sync(0xffffffffu, inU[kk] ? 1 : 0, src) != 0) && jj < L;
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
                     const int j = lane + 32 * k;
-                    if (inU[k] && (vo < val[k] || (vo == val[k] && jj < j))) ++rank[k];
+                    rank[k] += (uo && inU[k] && (vo < val[k] || (vo == val[k] && jj < j))) ? 1 : 0;
                 }
             }
         }
@@ -468,16 +529,15 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     if (P.quota) {
 #pragma unroll
         for (int kk = 0; kk < NK; ++kk) {
-#pragma unroll 4
+#pragma unroll (NK == 1 ? 32 : 4)
             for (int src = 0; src < 32; ++src) {
                 const int jj = src + 32 * kk;
                 const float co = __shfl_sync(0xffffffffu, c[kk], src);
                 const bool mo = __shfl_sync(0xffffffffu, msk[kk] ? 1 : 0, src) != 0;
-                if (!mo) continue;
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
                     const int j = lane + 32 * k;
-                    if (msk[k] && (co > c[k] || (co == c[k] && jj < j))) ++qrank[k];
+                    qrank[k] += (mo && msk[k] && (co > c[k] || (co == c[k] && jj < j))) ? 1 : 0;
                 }
             }
         }
