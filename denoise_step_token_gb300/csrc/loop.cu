@@ -8,12 +8,17 @@
 // One iteration is two calls around the caller's model forward:
 //   dllm_loop_begin: admission (host) and refill, then the box of eq. (1)
 //     (dllm_pack, or dllm_pack_block when the last step committed nothing);
-//   dllm_loop_end: the step over the caller's logits, the done-flag
-//     readback (the one host round trip), then -- if any row advanced -- the
-//     block commit and compaction in one launch, and the host mirrors.
+//   dllm_loop_end: the step over the caller's logits and the done-flag
+//     readback (the one host round trip), then the host mirrors.  In FDFO
+//     mode the block commit and compaction (one launch) follow the step on
+//     the stream before the readback: they read the done flags on the
+//     device and leave the batch as it is when no block finished.  In sync
+//     mode the host decides after the readback (a commit needs every block
+//     done).
 // The host keeps only what admission needs (prompt lengths, block indices,
-// steps in the current block); every array the kernels read lives in the
-// caller's device workspace.
+// steps in the current block) and a small pinned staging block for the
+// per-iteration copies; every array the kernels read lives in the caller's
+// device workspace.
 
 #include <stdint.h>
 #include <string.h>
@@ -32,9 +37,16 @@ struct dllm_loop {
     std::vector<int32_t> pending;     // request ids, queue order
     std::vector<int32_t> pending_p;   // their prompt lengths
     std::vector<int32_t> rid_h, b_h, s_h, p_act;
-    std::vector<uint8_t> wait_h, done_h;
-    std::vector<int32_t> admit_idx, quota_h, new_rid, new_p, new_K;
-    std::vector<float> new_thr;
+    std::vector<uint8_t> wait_h;
+    std::vector<int32_t> admit_idx;
+    // pinned host staging: done flags (readback), quotas and the refill
+    // rows (uploads); `staged` orders a rewrite after the last upload
+    void* pinned = nullptr;
+    uint8_t* done_h = nullptr;
+    int32_t* quota_h = nullptr;
+    int32_t* stage_h = nullptr;   // [4][n]: rid, p, K, thr bits of the admitted requests
+    cudaEvent_t staged = nullptr;
+    bool staged_pending = false;
     int32_t A = 0, W = 0, admitted_last = 0, iteration = 0, reloops = 0;
     int64_t cost = 0;
     bool in_place = false, have_box = false;
@@ -42,15 +54,20 @@ struct dllm_loop {
     const int32_t* prompt_tokens = nullptr;
     // device arrays, carved from the caller's workspace
     int32_t *rid = nullptr, *p = nullptr, *b = nullptr, *K = nullptr, *ids = nullptr, *gen = nullptr;
-    float *thr = nullptr, *cs = nullptr, *feats = nullptr, *new_thr_d = nullptr;
+    float *thr = nullptr, *cs = nullptr, *feats = nullptr;
     int32_t *box_ids = nullptr, *box_pos = nullptr, *box_pad = nullptr, *box_blk = nullptr;
     uint8_t *box_attn = nullptr, *done = nullptr, *evict = nullptr;
     int32_t *accept = nullptr, *n_new = nullptr, *new_index = nullptr, *src_row = nullptr, *A_out = nullptr;
-    int32_t *quota = nullptr, *new_rid_d = nullptr, *new_p_d = nullptr, *new_K_d = nullptr;
+    int32_t *quota = nullptr, *stage_d = nullptr;
     void* step_ws = nullptr;
     size_t step_ws_bytes = 0;
     void* compact_ws = nullptr;
     size_t compact_ws_bytes = 0;
+
+    ~dllm_loop() {
+        if (staged) cudaEventDestroy(staged);
+        if (pinned) cudaFreeHost(pinned);
+    }
 };
 
 namespace {
@@ -64,6 +81,49 @@ inline void compact_row_bytes(int32_t L, int64_t* rb) {
 namespace {
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Wait until the last upload from the pinned staging has been read, so the
+// staging can be rewritten (a no-op in the usual order: every dllm_loop_end
+// synchronises the stream).
+int staging_free(dllm_loop* lp) {
+    if (lp->staged_pending) {
+        if (cudaEventSynchronize(lp->staged) != cudaSuccess) return DLLM_ERR_CUDA;
+        lp->staged_pending = false;
+    }
+    return DLLM_OK;
+}
+
+int staging_used(dllm_loop* lp, cudaStream_t s) {
+    if (cudaEventRecord(lp->staged, s) != cudaSuccess) return DLLM_ERR_CUDA;
+    lp->staged_pending = true;
+    return DLLM_OK;
+}
+
+// Block commit and compaction of the A active rows in one launch: rows whose
+// device done flag is set advance (a fresh block, or eviction after their
+// last block); the survivors are compacted in order.
+int launch_commit(dllm_loop* lp, int32_t A, void* stream) {
+    const dllm_loop_config& c = lp->c;
+    dllm_advance_args aa;
+    memset(&aa, 0, sizeof(aa));
+    aa.A = A; aa.L = c.L; aa.mask_id = c.mask_id; aa.advance = lp->done; aa.rid = lp->rid; aa.K = lp->K; aa.b = lp->b;
+    aa.input_ids = lp->ids; aa.conf_state = lp->cs; aa.gen_tokens = lp->gen; aa.ld_gen = (int64_t)lp->Kmax * c.L;
+    aa.evict = lp->evict;
+    dllm_compact_args ca;
+    memset(&ca, 0, sizeof(ca));
+    ca.A = A; ca.n_arrays = 7; ca.evict = lp->evict; ca.new_index = lp->new_index; ca.src_row = lp->src_row;
+    ca.A_out = lp->A_out;
+    void* arrays[7] = {lp->rid, lp->p, lp->b, lp->K, lp->thr, lp->ids, lp->cs};
+    int64_t rb[7];
+    compact_row_bytes(c.L, rb);
+    for (int k = 0; k < 7; ++k) {
+        ca.arrays[k] = arrays[k];
+        ca.row_bytes[k] = rb[k];
+    }
+    ca.workspace = lp->compact_ws;
+    ca.workspace_bytes = lp->compact_ws_bytes;
+    return dllm_advance_compact(&aa, &ca, stream);
+}
 
 // Carve the loop's device arrays from `base` (or only size them when base is
 // null); returns the bytes used.
@@ -100,10 +160,7 @@ size_t carve(dllm_loop* lp, unsigned char* base) {
     lp->src_row = (int32_t*)take(cap * 4);
     lp->A_out = (int32_t*)take(4);
     lp->quota = (int32_t*)take(cap * 4);
-    lp->new_rid_d = (int32_t*)take(cap * 4);
-    lp->new_p_d = (int32_t*)take(cap * 4);
-    lp->new_K_d = (int32_t*)take(cap * 4);
-    lp->new_thr_d = (float*)take(cap * 4);
+    lp->stage_d = (int32_t*)take(cap * 16);
     int64_t rb[7];
     compact_row_bytes(c.L, rb);
     lp->compact_ws_bytes = dllm_compact_workspace_size(c.capacity, 7, rb);
@@ -169,8 +226,19 @@ extern "C" int dllm_loop_create(const dllm_loop_config* c, const int32_t* p, con
     lp->pending_p.resize(c->R);
     for (int32_t k = 0; k < c->R; ++k) lp->pending_p[k] = lp->p_all[lp->pending[k]];
     lp->admit_idx.resize(std::max(c->R, 1));
-    lp->done_h.resize(c->capacity);
-    lp->quota_h.resize(c->capacity);
+    {
+        const size_t cap = (size_t)c->capacity;
+        if (cudaHostAlloc(&lp->pinned, al256(cap) + al256(cap * 4) + cap * 16, cudaHostAllocDefault) != cudaSuccess ||
+            cudaEventCreateWithFlags(&lp->staged, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            delete lp;
+            return DLLM_ERR_CUDA;
+        }
+        unsigned char* h = static_cast<unsigned char*>(lp->pinned);
+        lp->done_h = h;
+        lp->quota_h = reinterpret_cast<int32_t*>(h + al256(cap));
+        lp->stage_h = reinterpret_cast<int32_t*>(h + al256(cap) + al256(cap * 4));
+    }
     // the step workspace must start zeroed (its counters are zero at rest)
     const int rc = dllm_workspace_init(lp->step_ws, lp->step_ws_bytes, stream);
     if (rc != DLLM_OK) {
@@ -199,16 +267,15 @@ extern "C" int dllm_loop_begin(dllm_loop* lp, void* stream) {
         if (rc != DLLM_OK) return rc;
         if (n > 0) {
             if (lp->A + n > c.capacity) return DLLM_ERR_UNSUPPORTED;
-            lp->new_rid.resize(n);
-            lp->new_p.resize(n);
-            lp->new_K.resize(n);
-            lp->new_thr.resize(n);
+            rc = staging_free(lp);
+            if (rc != DLLM_OK) return rc;
+            int32_t* st = lp->stage_h;
             for (int32_t k = 0; k < n; ++k) {
                 const int32_t r = lp->pending[lp->admit_idx[k]];
-                lp->new_rid[k] = r;
-                lp->new_p[k] = lp->p_all[r];
-                lp->new_K[k] = lp->K_all[r];
-                lp->new_thr[k] = lp->thr_all[r];
+                st[k] = r;
+                st[n + k] = lp->p_all[r];
+                st[2 * n + k] = lp->K_all[r];
+                memcpy(&st[3 * n + k], &lp->thr_all[r], 4);
             }
             // drop the admitted entries from the queue (indices descending)
             std::vector<int32_t> idx(lp->admit_idx.begin(), lp->admit_idx.begin() + n);
@@ -217,20 +284,21 @@ extern "C" int dllm_loop_begin(dllm_loop* lp, void* stream) {
                 lp->pending.erase(lp->pending.begin() + k);
                 lp->pending_p.erase(lp->pending_p.begin() + k);
             }
-            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->new_rid_d, lp->new_rid.data(), n * 4, cudaMemcpyHostToDevice, s));
-            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->new_p_d, lp->new_p.data(), n * 4, cudaMemcpyHostToDevice, s));
-            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->new_K_d, lp->new_K.data(), n * 4, cudaMemcpyHostToDevice, s));
-            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->new_thr_d, lp->new_thr.data(), n * 4, cudaMemcpyHostToDevice, s));
+            // the admitted rows' (rid, p, K, thr) in one upload
+            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->stage_d, st, (size_t)n * 16, cudaMemcpyHostToDevice, s));
+            rc = staging_used(lp, s);
+            if (rc != DLLM_OK) return rc;
             dllm_refill_args ra;
             memset(&ra, 0, sizeof(ra));
             ra.A0 = lp->A; ra.n = n; ra.L = c.L; ra.mask_id = c.mask_id;
-            ra.new_rid = lp->new_rid_d; ra.new_p = lp->new_p_d; ra.new_K = lp->new_K_d; ra.new_thr = lp->new_thr_d;
+            ra.new_rid = lp->stage_d; ra.new_p = lp->stage_d + n; ra.new_K = lp->stage_d + 2 * n;
+            ra.new_thr = reinterpret_cast<const float*>(lp->stage_d + 3 * n);
             ra.rid = lp->rid; ra.p = lp->p; ra.b = lp->b; ra.K = lp->K; ra.thr = lp->thr;
             ra.input_ids = lp->ids; ra.conf_state = lp->cs;
             rc = dllm_refill(&ra, stream);
             if (rc != DLLM_OK) return rc;
             for (int32_t k = 0; k < n; ++k) {
-                lp->rid_h.push_back(lp->new_rid[k]);
+                lp->rid_h.push_back(st[k]);
                 lp->b_h.push_back(0);
                 lp->s_h.push_back(0);
                 lp->wait_h.push_back(0);
@@ -280,26 +348,39 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
     sa.n_new = lp->n_new; sa.feats = lp->feats; sa.workspace = lp->step_ws; sa.workspace_bytes = lp->step_ws_bytes;
     int rc;
     if (c.S > 0) {
+        rc = staging_free(lp);
+        if (rc != DLLM_OK) return rc;
         for (int32_t i = 0; i < A; ++i) lp->quota_h[i] = dllm_transfer_quota(c.L, c.S, lp->s_h[i]);
-        DLLM_CUDA_TRY(cudaMemcpyAsync(lp->quota, lp->quota_h.data(), (size_t)A * 4, cudaMemcpyHostToDevice, s));
+        DLLM_CUDA_TRY(cudaMemcpyAsync(lp->quota, lp->quota_h, (size_t)A * 4, cudaMemcpyHostToDevice, s));
+        rc = staging_used(lp, s);
+        if (rc != DLLM_OK) return rc;
         rc = dllm_step_quota(&sa, lp->quota, stream);
     } else {
         rc = dllm_step(&sa, stream);
     }
     if (rc != DLLM_OK) return rc;
+    // FDFO: every done row advances, so the commit and compaction can
+    // follow the step at once (the advance flags are the device's done
+    // flags; with none set they leave the batch unchanged)
+    const bool fdfo = c.mode == 0;
+    if (fdfo) {
+        rc = launch_commit(lp, A, stream);
+        if (rc != DLLM_OK) return rc;
+    }
     // the per-step readback: one byte per row
-    DLLM_CUDA_TRY(cudaMemcpyAsync(lp->done_h.data(), lp->done, (size_t)A, cudaMemcpyDeviceToHost, s));
+    DLLM_CUDA_TRY(cudaMemcpyAsync(lp->done_h, lp->done, (size_t)A, cudaMemcpyDeviceToHost, s));
     DLLM_CUDA_TRY(cudaStreamSynchronize(s));
+    lp->staged_pending = false;
     bool all_done = true, any_done = false;
     for (int32_t i = 0; i < A; ++i) {
         all_done = all_done && lp->done_h[i];
         any_done = any_done || lp->done_h[i];
     }
     // FDFO: every done row advances; sync: all of them once every row is done
-    const bool advance = c.mode == 0 ? any_done : all_done;
+    const bool advance = fdfo ? any_done : all_done;
     ++lp->iteration;
     if (!advance) {
-        // nothing commits: advance and compaction would be no-ops
+        // nothing commits (FDFO: the commit launch changed nothing)
         for (int32_t i = 0; i < A; ++i) {
             if (!lp->wait_h[i]) ++lp->s_h[i];
             lp->wait_h[i] = lp->done_h[i];
@@ -308,27 +389,10 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
         return DLLM_OK;
     }
     lp->in_place = false;
-    // the advance flags are the done flags themselves (FDFO, or sync with all done)
-    dllm_advance_args aa;
-    memset(&aa, 0, sizeof(aa));
-    aa.A = A; aa.L = c.L; aa.mask_id = c.mask_id; aa.advance = lp->done; aa.rid = lp->rid; aa.K = lp->K; aa.b = lp->b;
-    aa.input_ids = lp->ids; aa.conf_state = lp->cs; aa.gen_tokens = lp->gen; aa.ld_gen = (int64_t)lp->Kmax * c.L;
-    aa.evict = lp->evict;
-    dllm_compact_args ca;
-    memset(&ca, 0, sizeof(ca));
-    ca.A = A; ca.n_arrays = 7; ca.evict = lp->evict; ca.new_index = lp->new_index; ca.src_row = lp->src_row;
-    ca.A_out = lp->A_out;
-    void* arrays[7] = {lp->rid, lp->p, lp->b, lp->K, lp->thr, lp->ids, lp->cs};
-    int64_t rb[7];
-    compact_row_bytes(c.L, rb);
-    for (int k = 0; k < 7; ++k) {
-        ca.arrays[k] = arrays[k];
-        ca.row_bytes[k] = rb[k];
+    if (!fdfo) {
+        rc = launch_commit(lp, A, stream);
+        if (rc != DLLM_OK) return rc;
     }
-    ca.workspace = lp->compact_ws;
-    ca.workspace_bytes = lp->compact_ws_bytes;
-    rc = dllm_advance_compact(&aa, &ca, stream);
-    if (rc != DLLM_OK) return rc;
     // host mirrors: b += 1 and a fresh block for the advanced rows, evict b >= K
     int32_t kept = 0;
     for (int32_t i = 0; i < A; ++i) {

@@ -485,14 +485,18 @@ int dllm_refill(const dllm_refill_args* args, void* stream);
  *     (dllm_pack; dllm_pack_block after a step that committed nothing, when
  *     re-loop is on -- admission is skipped then: it would admit nothing);
  *   dllm_loop_end: the step over the caller's logits ([A * L][ldv], row
- *     i * L + j = position j of active row i), the readback of the done
- *     flags (it synchronises the stream), then, if any row advances (FDFO:
- *     its block is done; sync: every block is done), the block commit and
- *     compaction in one launch (dllm_advance_compact).
+ *     i * L + j = position j of active row i), the block commit and
+ *     compaction in one launch (dllm_advance_compact) and the readback of
+ *     the done flags (it synchronises the stream).  FDFO: the commit
+ *     follows the step on the stream before the readback (done rows
+ *     advance; with no row done it leaves the batch unchanged).  Sync: it
+ *     is launched after the readback, and only when every block is done.
  * Device memory: everything lives in the caller's workspace
  * (dllm_loop_workspace_size bytes, 256-byte aligned); the loop object
- * itself is host memory, freed by dllm_loop_destroy.  The pending queue is
- * every request, sorted by prompt length (ties by request id).
+ * itself is host memory, with a small pinned block (about 21 bytes per
+ * row of capacity) for the per-iteration copies, all freed by
+ * dllm_loop_destroy.  The pending queue is every request, sorted by prompt
+ * length (ties by request id).
  * ====================================================================== */
 typedef struct dllm_loop dllm_loop;
 
