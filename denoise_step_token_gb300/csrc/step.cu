@@ -318,9 +318,11 @@ __device__ __forceinline__ float float_from_order_key(uint32_t k) {
 }
 
 // Features of a block of at most 32 positions (one per lane): the unmasked
-// values are sorted by a 32-lane bitonic network on (value, position) --
-// positions outside U sort last -- and the order statistics are read from
-// their lanes.  Same results as the general rank count below.
+// values are sorted by a 32-lane bitonic network on their order-preserving
+// bits -- positions outside U carry the largest key and sort last -- and the
+// order statistics are read from their lanes.  Equal values are
+// interchangeable, so no tie-break is needed; the results are those of the
+// general rank count below.
 __device__ __forceinline__ void warp_features_32(float val, bool inU, int L, int lane, float* feats_out) {
     const int n = __reduce_add_sync(0xffffffffu, inU ? 1u : 0u);
     float sum = inU ? val : 0.f;
@@ -331,18 +333,17 @@ __device__ __forceinline__ void warp_features_32(float val, bool inU, int L, int
         f[0] = f[1] = f[2] = f[3] = f[4] = __int_as_float(0x7fc00000);
         f[5] = 0.f;
     } else {
-        unsigned long long key = ((unsigned long long)(inU ? float_order_key(val) : 0xffffffffu) << 32) |
-                                 (unsigned)lane;
+        uint32_t key = inU ? float_order_key(val) : 0xffffffffu;
 #pragma unroll
         for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
             for (int j = k >> 1; j > 0; j >>= 1) {
-                const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, j);
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, key, j);
                 const bool take_min = ((lane & k) == 0) == ((lane & j) == 0);
-                key = take_min ? (other < key ? other : key) : (other > key ? other : key);
+                key = take_min ? min(other, key) : max(other, key);
             }
         }
-        const uint32_t hi = (uint32_t)(key >> 32);   // lane r: the r-th smallest value of U
+        const uint32_t hi = key;   // lane r: the r-th smallest value of U
         const float qs[3] = {0.25f, 0.5f, 0.75f};
         float lo_v[3], hi_v[3], frac[3];
 #pragma unroll

@@ -188,6 +188,29 @@ def test_features_kernel(dllm, device):
     np.testing.assert_allclose(got, ref, rtol=0, atol=CONF_TOL, equal_nan=True)
 
 
+@pytest.mark.parametrize("L", [1, 5, 31, 32, 33, 64, 100])
+def test_features_kernel_adversarial_values(dllm, device, L):
+    """S6 on values chosen to break a sort: ties (values drawn from a small
+    set), negatives, signed zeros and tiny magnitudes, every mask density
+    from none to all.  L <= 32 takes the one-warp sort, longer blocks the
+    rank count.  The minimum is one of the values, so it must match
+    exactly; the interpolated quantiles and the mean within 1e-5."""
+    import torch
+    import oracle
+    rng = np.random.default_rng(100 + L)
+    B, mask_id = 96, 7
+    pool = np.array([-1.5, -0.25, -0.0, 0.0, 1e-40, 1e-30, 0.125, 0.5, 0.5000001, 1.0, 1.75], dtype=np.float32)
+    cs = np.where(rng.random((B, L)) < 0.5, rng.choice(pool, (B, L)),
+                  rng.uniform(-2.0, 2.0, (B, L))).astype(np.float32)
+    frac = np.concatenate([[0.0, 1.0], rng.random(B - 2)])
+    ids = np.where(rng.random((B, L)) < frac[:, None], mask_id, 3).astype(np.int32)
+    got = dllm.features(torch.from_numpy(ids).to(device), torch.from_numpy(cs).to(device),
+                        mask_id=mask_id).cpu().numpy()
+    ref = oracle.features(ids, cs, mask_id)
+    np.testing.assert_array_equal(got[:, 0], ref[:, 0].astype(np.float32))
+    np.testing.assert_allclose(got, ref, rtol=0, atol=CONF_TOL, equal_nan=True)
+
+
 def test_repeated_steps_to_completion(dllm, device):
     """Step the same batch with fresh logits each step until every block is
     done; the oracle follows in lockstep."""
