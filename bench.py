@@ -414,7 +414,7 @@ class Pipeline:
 
 FUSED_STAGE_BYTES = 96 * 1024   # state rows dllm_advance_compact stages in one CTA (one launch)
 ROOF_EVERY = 8          # steps between roofline event pairs
-CPU_BASELINE_CPU_S = 12.0   # CPU time the oracle baseline runs for (whole passes)
+ORACLE_SAMPLE_CPU_S = 12.0   # CPU time the oracle baseline runs for (whole passes)
 E2E_ROUNDS = 3              # timed rounds of the end-to-end leg (the median is reported)
 
 
@@ -584,7 +584,7 @@ def cpu_baseline(inp, quota=None):
     threads = os.cpu_count() or 1
     reqs = list(range(inp.cfg.B))
     c0 = time.process_time()
-    rows, secs, passes = oracle_over_requests(inp, reqs, threads, quota, min_cpu_s=CPU_BASELINE_CPU_S)
+    rows, secs, passes = oracle_over_requests(inp, reqs, threads, quota, min_cpu_s=ORACLE_SAMPLE_CPU_S)
     cpu_s = time.process_time() - c0
     return {"value": rows / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{passes} full passes of the oracle over the {inp.cfg.B}-request batch "
