@@ -416,6 +416,7 @@ FUSED_STAGE_BYTES = 96 * 1024   # state rows dllm_advance_compact stages in one 
 ROOF_EVERY = 8          # steps between roofline event pairs
 ORACLE_SAMPLE_CPU_S = 12.0   # CPU time the oracle baseline runs for (whole passes)
 E2E_ROUNDS = 3              # timed rounds of the end-to-end leg (the median is reported)
+REFERENCE_RUN_S = 90.0      # the reference arm's whole run (warm-up and timed steps), about
 
 
 def run_gpu(args, rank, world, local_rank, dist):
@@ -553,16 +554,20 @@ def fixed_steps_quota(inp, S):
     return np.array([oracle.transfer_quota(L, S, int(L - m)) for m in inp.masked.sum(axis=1)], dtype=np.int64)
 
 
-def oracle_over_requests(inp, reqs, threads, quota=None, min_cpu_s=0.0, max_wall_s=30.0):
+def oracle_over_requests(inp, reqs, threads, quota=None, min_cpu_s=0.0, max_wall_s=30.0, cache=None):
     """Run the oracle's step on each listed request (one sub-batch each) on a
     thread pool; returns (masked rows processed, wall seconds of the oracle
     calls alone, passes).  Whole passes over ``reqs`` repeat until the
     process has used ``min_cpu_s`` seconds of CPU time or ``max_wall_s`` of
     wall time.  ``quota``: per-request counts of the fixed-steps rule, or
-    None for the threshold rule."""
+    None for the threshold rule.  ``cache``: a dict of requests' logits kept
+    across calls (built outside the timed part either way)."""
     import oracle
     cfg = inp.cfg
-    logits = {b: oracle_request_logits(inp, b) for b in reqs}
+    logits = cache if cache is not None else {}
+    for b in dict.fromkeys(reqs):
+        if b not in logits:
+            logits[b] = oracle_request_logits(inp, b)
     rows = int(sum(inp.masked[b].sum() for b in reqs))
 
     def one(b):
@@ -597,19 +602,22 @@ def run_reference(args, rank, world):
     cfg, inp, *_ = make_workload(1000, args.workload)
     quota = fixed_steps_quota(inp, FIXED_STEPS_S) if args.workload == "dream_fixed_steps" else None
     threads = os.cpu_count() or 1
-    # probe: one request, to size each step's sample so the run ends in ~2 min
-    probe_rows, probe_s, _ = oracle_over_requests(inp, [int(np.argmax(inp.masked.sum(axis=1)))], 1)
-    per_row = probe_s / max(probe_rows, 1) / threads
-    total_steps = args.steps + args.warmup
-    budget_rows = 120.0 / max(per_row, 1e-6)
-    target_rows = max(1, int(budget_rows / total_steps))
     order = [b for b in range(cfg.B) if inp.masked[b].any()]
+    # probe: one pass over the batch on every thread, to size each step's
+    # sample so that the whole run takes about REFERENCE_RUN_S
+    cache = {}
+    probe_rows, probe_s, _ = oracle_over_requests(inp, order, threads, quota, cache=cache)
+    rate = probe_rows / max(probe_s, 1e-9)
+    total_steps = args.steps + args.warmup
+    target_rows = max(1, int(REFERENCE_RUN_S * rate / total_steps))
     cursor = 0
 
     def sample():
+        # whole requests in batch order, wrapping around (a request may
+        # repeat) until the step holds target_rows masked rows
         nonlocal cursor
         picked, rows = [], 0
-        while rows < target_rows and len(picked) < len(order):
+        while rows < target_rows:
             b = order[cursor % len(order)]
             cursor += 1
             picked.append(b)
@@ -617,23 +625,28 @@ def run_reference(args, rank, world):
         return picked
 
     for _ in range(args.warmup):
-        oracle_over_requests(inp, sample(), threads, quota)
+        oracle_over_requests(inp, sample(), threads, quota, cache=cache)
     units = 0
     secs = 0.0
+    busy = 1   # threads with work: one request per task
     for _ in range(args.steps):
-        r, s, _ = oracle_over_requests(inp, sample(), threads, quota)
+        reqs = sample()
+        busy = max(busy, min(threads, len(reqs)))
+        r, s, _ = oracle_over_requests(inp, reqs, threads, quota, cache=cache)
         units += r
         secs += s
     value = units / secs
+    rows_per_step = units / args.steps
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": {"workload": WORKLOADS[args.workload], "B": cfg.B, "L": cfg.L, "V": cfg.V,
-                   "sample_rows_per_step": target_rows},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"each step: about {target_rows} masked rows of the Dream-shaped batch, "
-                                   f"whole requests, one request per task on {threads} threads"},
+                   "sample_rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": busy, "kind": "oracle",
+                         "sample": f"each step: {rows_per_step:.0f} masked rows on average, whole requests of the "
+                                   f"{cfg.B}-request batch taken in order (wrapping around), one request per task "
+                                   f"on up to {busy} of {threads} threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
