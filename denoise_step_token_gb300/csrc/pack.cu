@@ -599,11 +599,11 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
     __shared__ uint8_t s_ev[kFusedThreads];
     __shared__ short s_arr[kFusedMapWords];
     __shared__ int s_off[kFusedMapWords];
+    __shared__ int s_skip;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int A = P.adv.A;
-    pdl_wait();
-    pdl_release();
     // element map of a staged row: array index (-1 in padding) and offset
+    // (launch parameters only: built before waiting on the previous kernel)
     {
         const int es = P.word ? 4 : 1;
         const int per_row = (int)(P.row_total / es);
@@ -623,6 +623,8 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
             s_off[w] = o;
         }
     }
+    pdl_wait();
+    pdl_release();
     advance_rows(P.adv, s_gen_dst, s_ev, tid);   // ends with a barrier: evict, ids, cs, b visible CTA-wide
     int base = 0;      // survivors before the chunk
     for (int c0 = 0; c0 < A; c0 += P.chunk_rows) {
@@ -631,6 +633,7 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
         const bool keep = in && P.adv.evict[i] == 0;
         const unsigned bal = __ballot_sync(0xffffffffu, keep);
         if (lane == 0) s_wsum[warp] = __popc(bal);
+        if (tid == 0) s_skip = 0x7fffffff;
         __syncthreads();
         int before = 0, kept = 0;
         for (int w = 0; w < kFusedThreads / 32; ++w) {
@@ -639,6 +642,11 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
             kept += c;
         }
         const int rank = before + __popc(bal & ((1u << lane) - 1u));
+        // survivors ahead of the first evicted row keep their index: they
+        // are a prefix of the chunk's survivors and need no move
+        const bool moves = keep && base + rank != i;
+        const unsigned mv = __ballot_sync(0xffffffffu, moves);
+        if (mv && lane == __ffs(mv) - 1) atomicMin(&s_skip, rank);
         if (in) {
             const int ni = keep ? base + rank : -1;
             if (P.new_index) P.new_index[i] = ni;
@@ -649,8 +657,9 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
             }
         }
         __syncthreads();
-        if (P.word) move_chunk<uint32_t>(P, stage, s_src, s_dst, s_arr, s_off, kept, tid);
-        else move_chunk<uint8_t>(P, stage, s_src, s_dst, s_arr, s_off, kept, tid);
+        const int skip = min(s_skip, kept);
+        if (P.word) move_chunk<uint32_t>(P, stage, s_src + skip, s_dst + skip, s_arr, s_off, kept - skip, tid);
+        else move_chunk<uint8_t>(P, stage, s_src + skip, s_dst + skip, s_arr, s_off, kept - skip, tid);
         __syncthreads();
         base += kept;
     }
