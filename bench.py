@@ -871,6 +871,9 @@ def main():
                        "state_ring": RING, "roofline_events": f"around every {ROOF_EVERY}th step kernel"},
             "logits_gbs": pipe.M * cfg.V * 2 * K / res["seconds"] / 1e9 / world,
             "step_kernel_ms": step_ms,
+            "step_kernel_ms_median": statistics.median(res["step_ms"]),
+            "step_kernel_ms_min": min(res["step_ms"]),
+            "step_kernel_samples": len(res["step_ms"]),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,

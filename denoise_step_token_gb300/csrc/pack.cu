@@ -56,8 +56,10 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
          idx += (long long)gridDim.x * blockDim.x) {
         const int i = (int)(idx / P.W);
         const int c = (int)(idx - (long long)i * P.W);
+        // the row's scalars together: the token source below hangs off rid
         const int p = __ldg(P.p + i);
         const int b = __ldg(P.b + i);
+        const int r = __ldg(P.rid + i);
         const long long width = (long long)p + (long long)(b + 1) * P.L;
         if (p < 0 || b < 0 || width > P.W || (p > 0 && !P.prompt_tokens) || (b > 0 && !P.gen_tokens)) {
             if (c == 0) set_error(P.err, DLLM_DEVERR_ROW_WIDTH);
@@ -73,7 +75,6 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
             const int k = c - pad;   // logical position: cumulative index over the mask
             a = 1;
             ps = k;
-            const int r = __ldg(P.rid + i);
             if (k < p) {
                 tok = __ldg(P.prompt_tokens + __ldg(P.prompt_off + r) + k);
             } else if (k < p + b * P.L) {
