@@ -65,6 +65,9 @@ struct dllm_loop {
     size_t compact_ws_bytes = 0;
 
     ~dllm_loop() {
+        // an upload from the staging may still be in flight (a begin with
+        // no end after it): let it finish before the memory goes
+        if (staged && staged_pending) cudaEventSynchronize(staged);
         if (staged) cudaEventDestroy(staged);
         if (pinned) cudaFreeHost(pinned);
     }

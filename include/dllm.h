@@ -551,6 +551,9 @@ int dllm_loop_create(const dllm_loop_config* cfg, const int32_t* p, const int32_
                      const int64_t* prompt_off, const int32_t* prompt_tokens, void* workspace,
                      size_t workspace_bytes, void* stream, dllm_loop** out);
 
+/* Frees the loop object and its pinned staging (after any upload from it
+ * has finished).  The workspace stays the caller's: do not free it while
+ * the loop's kernels may still run on the stream. */
 void dllm_loop_destroy(dllm_loop* loop);
 
 int dllm_loop_begin(dllm_loop* loop, void* stream);
