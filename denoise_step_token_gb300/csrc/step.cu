@@ -42,6 +42,7 @@
 
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -1239,11 +1240,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Step
     finalize_request(P, b, any, lane, true);
 }
 
-int g_smem_configured[64];
+// per-device launch state, read without the lock on the launch path:
+// atomics publish it (release) and read it (acquire)
+std::atomic<int> g_smem_configured[64];
 
 struct LaunchFacts {
-    volatile bool ready;
-    long long max_dynamic;   // dynamic shared memory available to step_kernel
+    std::atomic<bool> ready{false};
+    long long max_dynamic = 0;   // dynamic shared memory available to step_kernel (written before ready)
 };
 LaunchFacts g_launch_facts[64];
 std::mutex g_launch_mu;
@@ -1312,23 +1315,23 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
     // per-device launch facts, queried once
     if (dev < 0 || dev >= 64) return DLLM_ERR_UNSUPPORTED;
     LaunchFacts& lf = g_launch_facts[dev];
-    if (!lf.ready) {
+    if (!lf.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_launch_mu);
-        if (!lf.ready) {
+        if (!lf.ready.load(std::memory_order_relaxed)) {
             int max_optin = 0;
             DLLM_CUDA_TRY(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
             cudaFuncAttributes fa;
             DLLM_CUDA_TRY(cudaFuncGetAttributes(&fa, step_kernel));
             lf.max_dynamic = max_optin - (long long)fa.sharedSizeBytes;
-            lf.ready = true;
+            lf.ready.store(true, std::memory_order_release);
         }
     }
     if ((long long)smem > lf.max_dynamic) return DLLM_ERR_UNSUPPORTED;
-    if (g_smem_configured[dev] < (int)smem) {
+    if (g_smem_configured[dev].load(std::memory_order_acquire) < (int)smem) {
         std::lock_guard<std::mutex> lock(g_launch_mu);
-        if (g_smem_configured[dev] < (int)smem) {
+        if (g_smem_configured[dev].load(std::memory_order_relaxed) < (int)smem) {
             DLLM_CUDA_TRY(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-            g_smem_configured[dev] = (int)smem;
+            g_smem_configured[dev].store((int)smem, std::memory_order_release);
         }
     }
 

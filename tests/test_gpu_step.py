@@ -355,6 +355,55 @@ def test_steps_on_two_streams_with_their_own_workspaces(dllm, device):
         compare_step(ref, got, list(range(inp.cfg.B)), inp.cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
 
 
+def test_steps_from_several_host_threads(dllm, device):
+    """Four host threads call the step at once, each on its own stream with
+    its own workspace and batch shape (so the library's per-device launch
+    state is read and grown concurrently); every result equals the
+    oracle's."""
+    import threading
+    import torch
+    names = ["ragged", "l64", "tiny", "all_masked"]
+    cases = [synth.make_step_state(SMALL_CASES[n], 40 + k) for k, n in enumerate(names)]
+    for inp in cases:
+        enforce_margins(inp)
+    refs = [oracle_step(inp) for inp in cases]
+    prepared = []
+    for inp in cases:
+        logits = device_logits(inp, device)
+        ids, thr, cs = device_state(inp, device)
+        ws = torch.zeros(dllm.step_workspace_size(inp.cfg.B, inp.cfg.L, inp.cfg.V), dtype=torch.uint8, device=device)
+        prepared.append((inp, logits, ids, thr, cs, ws, torch.cuda.Stream(device=device)))
+    torch.cuda.synchronize()
+    start = threading.Barrier(len(prepared))
+    outs, errors = [None] * len(prepared), []
+
+    def run(k):
+        inp, logits, ids, thr, cs, ws, st = prepared[k]
+        try:
+            start.wait()
+            with torch.cuda.stream(st):
+                for _ in range(3):   # the last call's outputs are checked; ids/cs move on each call
+                    ids.copy_(torch.from_numpy(inp.input_ids).to(device))
+                    cs.copy_(torch.from_numpy(inp.conf_state).to(device))
+                    outs[k] = dllm.step(logits, ids, thr, cs, V=inp.cfg.V, mask_id=inp.cfg.mask_id, debug=True,
+                                        workspace=ws)
+            st.synchronize()
+        except Exception as e:   # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(k,)) for k in range(len(prepared))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert dllm.get_device_error(device) == 0
+    for (inp, logits, ids, thr, cs, ws, st), out, ref in zip(prepared, outs, refs):
+        got = {k: v.cpu().numpy() for k, v in out.items()}
+        compare_step(ref, got, list(range(inp.cfg.B)), inp.cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+
+
 def test_pipeline_captured_in_a_cuda_graph(dllm, device):
     """pack, step and the fused commit/compaction (launched as programmatic
     dependents) captured in a CUDA graph: a replay equals eager execution."""
