@@ -52,7 +52,7 @@ namespace {
 
 // Pipeline shape (tunable at build time; the defaults are the measured best).
 #ifndef DLLM_STEP_WARPS
-#define DLLM_STEP_WARPS 16
+#define DLLM_STEP_WARPS 14
 #endif
 #ifndef DLLM_STEP_FINISHERS
 #define DLLM_STEP_FINISHERS 2
