@@ -55,7 +55,7 @@ namespace {
 #define DLLM_STEP_WARPS 14
 #endif
 #ifndef DLLM_STEP_FINISHERS
-#define DLLM_STEP_FINISHERS 2
+#define DLLM_STEP_FINISHERS 1
 #endif
 #ifndef DLLM_STEP_STAGES
 #define DLLM_STEP_STAGES 3
