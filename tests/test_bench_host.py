@@ -1,0 +1,46 @@
+"""bench.py's host-side arithmetic on CPU: the algorithmic bytes of a step,
+the launches of one pipeline step, the traffic read from the committed
+profile only while the kernel source matches, and the clock summary."""
+import types
+
+import pytest
+
+
+def test_algorithmic_bytes_dream():
+    import bench
+    import synth
+    cfg = synth.STEP_CONFIGS["dream"]
+    # masked rows x V x 2 + per-position state (ids and conf_state, read and
+    # written) + per-request thr, done, accept_len, n_new, six features
+    assert bench.algorithmic_bytes(cfg, 1851) == 1851 * 151936 * 2 + 128 * 32 * 16 + 128 * (4 + 1 + 4 + 4 + 24)
+    assert bench.algorithmic_bytes(cfg, 1851) == 562537344
+
+
+@pytest.mark.parametrize("B,L,shards,expected", [(128, 32, None, 3), (512, 64, None, 5), (128, 32, 4, 7),
+                                                 (3000, 8, None, 5)])
+def test_launches_per_step(B, L, shards, expected):
+    import bench
+    pipe = types.SimpleNamespace(B=B, shards=list(range(shards)) if shards else None,
+                                 rb_arr=[L * 4, L * 4, 4, 4, 4, 4, 4])
+    # pack + the step (or each shard and the merge) + commit/compaction (one
+    # launch while the rows fit the fused kernel's staging, else three)
+    assert bench.Pipeline.launches_per_step(pipe) == expected
+
+
+def test_traffic_only_for_the_profiled_source():
+    import bench
+    sha = bench.step_source_sha()
+    traffic = bench.load_traffic(sha)
+    assert traffic is not None and traffic > bench.algorithmic_bytes(__import__("synth").STEP_CONFIGS["dream"], 1851)
+    assert bench.load_traffic("0" * 16) is None
+
+
+def test_clock_summary():
+    import bench
+    lines = ["1965, 2070, 1012.3, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "2070, 2070, 980.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "2070, 2070, 990.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "garbage line", "[N/A], 2070, 1, 0, Not Active, Not Active, Not Active, Not Active"]
+    out = bench.ClockSampler.summarize(lines)
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert bench.ClockSampler.summarize([]) is None
