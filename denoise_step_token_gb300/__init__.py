@@ -270,6 +270,11 @@ def step(logits, input_ids, thr, conf_state, *, V, mask_id, feats=True, debug=Fa
     compact:    logits hold only the masked positions' rows, in position
                 order (dllm_step_compact); any number of rows >= the masked
                 count
+    workspace:  uint8 CUDA tensor of at least dllm_step_workspace_size
+                bytes, zeroed once before first use; without one, a
+                workspace cached per device is used, so steps that may run
+                at the same time (on different streams) must each pass their
+                own
     Returns a dict of output tensors: done (uint8 [B]), accept_len, n_new
     (int32 [B]), feats (float32 [B, 6]) and, with debug, conf / lse / tok [B, L].
     """
