@@ -106,6 +106,15 @@ def make_workload(seed, name="dream"):
     return cfg, inp, reqs, b, gen, pending_p
 
 
+def workload_config(name, cfg, inp, W, cost, fixed):
+    """The ``config`` object of the JSON line: what the workload is, the
+    same for the GPU arm and the reference arm."""
+    return {"workload": WORKLOADS[name], "B": cfg.B, "L": cfg.L, "V": cfg.V, "masked_rows": int(inp.masked.sum()),
+            "rule": (f"fixed steps, S = {FIXED_STEPS_S} per block" if fixed else
+                     "threshold per request from {0.5,0.6,0.7,0.8,0.9}"),
+            "mask_fraction": "U[0,1] per request", "box_W": int(W), "box_cost": int(cost), "token_budget": BUDGET}
+
+
 def algorithmic_bytes(cfg, M):
     """Bytes one dllm_step launch must move: the masked logits rows plus the
     per-position state (input_ids and conf_state read and written) and the
@@ -124,21 +133,22 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def load_traffic(step_src_sha):
-    """ncu DRAM bytes per launch of the step kernel, from the committed
-    profile summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "step_kernel_dream.md")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "step_kernel_dream.json")
+
+
+def load_traffic(step_src_sha, path=TRAFFIC_JSON):
+    """ncu DRAM bytes per launch of the step kernel on the Dream-shaped
+    batch, from the committed capture record, if that capture was taken on
+    the current kernel source; else None."""
     try:
-        text = open(path, encoding="utf-8").read()
-    except OSError:
+        with open(path, encoding="utf-8") as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    sha = traffic = None
-    for line in text.splitlines():
-        if line.startswith("source_sha256:"):
-            sha = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
-    return traffic if sha == step_src_sha else None
+    if rec.get("source_sha256") != step_src_sha:
+        return None
+    v = rec.get("dram_bytes_per_launch")
+    return float(v) if v is not None else None
 
 
 def step_source_sha():
@@ -380,6 +390,20 @@ class Pipeline:
         rc = lib.dllm_pack(ctypes.byref(pa), stream)
         if ev_before is not None:
             ev_before.record()
+        rc |= self.launch_step(slot, stream, compact)
+        if ev_after is not None:
+            ev_after.record()
+        rc |= lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream)
+        if rc:
+            raise RuntimeError("a dllm call failed inside the timed loop")
+
+    def launch_step(self, slot, stream, compact=None):
+        """The step of one pipeline step on state slot ``slot`` (dllm_step,
+        dllm_step_quota, the vocabulary shards plus their merge, or
+        dllm_step_compact); returns the OR of the status codes."""
+        lib = self.lib
+        sa = self.args[slot][1]
+        rc = 0
         if self.shards is not None and compact is None:
             for k, (v0, a) in enumerate(self.shards):
                 a.input_ids = sa.input_ids
@@ -399,11 +423,7 @@ class Pipeline:
             rc |= lib.dllm_step(ctypes.byref(sa), stream)
         else:
             rc |= lib.dllm_step_quota(ctypes.byref(sa), self.quota_ptr, stream)
-        if ev_after is not None:
-            ev_after.record()
-        rc |= lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream)
-        if rc:
-            raise RuntimeError("a dllm call failed inside the timed loop")
+        return rc
 
     def restore(self):
         self.state.copy_(self.pristine)
@@ -420,10 +440,54 @@ class Pipeline:
 
 
 FUSED_STAGE_BYTES = 96 * 1024   # state rows dllm_advance_compact stages in one CTA (one launch)
-ROOF_EVERY = 8          # steps between roofline event pairs
+KERNEL_TIMING_LAUNCHES = 48   # step launches timed alone for the roofline (fixed, whatever --steps is)
 ORACLE_SAMPLE_CPU_S = 12.0   # CPU time the oracle baseline runs for (whole passes)
 E2E_ROUNDS = 3              # timed rounds of the end-to-end leg (the median is reported)
 REFERENCE_RUN_S = 90.0      # the reference arm's whole run (warm-up and timed steps), about
+
+
+def time_step_kernel(pipe, stream, n=KERNEL_TIMING_LAUNCHES):
+    """Launch duration of the step alone (the roofline's kernel), measured
+    two ways on fresh state slots (the ring is restored first, outside
+    every event):
+
+    * per launch: ``n`` step launches, each between its own pair of CUDA
+      events on the launching stream, after one untimed launch (so the first
+      timed launch does not follow a host synchronisation); mean, median
+      and minimum over the n;
+    * back to back: ``n`` step launches in a row, each a programmatic
+      dependent of the previous one as in the pipeline, between one pair
+      of events; their mean.
+
+    The count is fixed (independent of the pipeline's step count)."""
+    torch = pipe.torch
+    n = min(n, pipe.ring - 1)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    pipe.restore()
+    torch.cuda.synchronize()
+    rc = pipe.launch_step(0, stream)
+    for k in range(n):
+        ev[k][0].record()
+        rc |= pipe.launch_step(k + 1, stream)
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    pipe.restore()
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    rc |= pipe.launch_step(0, stream)
+    b0.record()
+    for k in range(n):
+        rc |= pipe.launch_step(k + 1, stream)
+    b1.record()
+    torch.cuda.synchronize()
+    if rc:
+        raise RuntimeError("a dllm call failed in the step-kernel timing pass")
+    pipe.restore()
+    return {"n": n, "mean_ms": statistics.fmean(per_launch), "median_ms": statistics.median(per_launch),
+            "min_ms": min(per_launch), "max_ms": max(per_launch),
+            "back_to_back_mean_ms": b0.elapsed_time(b1) / n}
 
 
 def run_gpu(args, rank, world, local_rank, dist):
@@ -448,12 +512,6 @@ def run_gpu(args, rank, world, local_rank, dist):
     if dllm.get_device_error(device):
         raise RuntimeError("device error during warm-up")
     pipe.restore()
-    # the step kernel's launch duration for the roofline: CUDA events around
-    # every ROOF_EVERY-th step of the timed region (events cost the
-    # pipeline a few microseconds per step, so not around every step)
-    sampled = [k for k in range(K) if k % ROOF_EVERY == 0]
-    ev_b = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
-    ev_a = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     gpu_uuid = None
@@ -474,20 +532,22 @@ def run_gpu(args, rank, world, local_rank, dist):
         slot = k % pipe.ring
         if slot == 0 and k > 0:
             pipe.restore()
-        pipe.run(slot, sh, ev_b.get(k), ev_a.get(k))
+        pipe.run(slot, sh)
     t1.record()
     torch.cuda.synchronize()
     if dist is not None and dist.is_initialized():
         dist.barrier()
+    # the step kernel alone, for the roofline (outside the timed pipeline
+    # region, so that its events do not slow the pipeline down)
+    kernel = time_step_kernel(pipe, sh)
     clocks = sampler.stop()
     err = dllm.get_device_error(device)
     if err:
         raise RuntimeError(f"device error {err} during the timed region")
     total_ms = t0.elapsed_time(t1)
-    step_ms = [ev_b[k].elapsed_time(ev_a[k]) for k in sampled]
     units, seconds = aggregate(pipe.M * K, total_ms / 1e3, dist)
     res = {
-        "pipe": pipe, "units": units, "seconds": seconds, "total_ms": total_ms, "step_ms": step_ms,
+        "pipe": pipe, "units": units, "seconds": seconds, "total_ms": total_ms, "kernel": kernel,
         "clocks": clocks, "cfg": cfg, "inp": inp, "device": device,
     }
     return res
@@ -606,8 +666,10 @@ def cpu_baseline(inp, quota=None):
 
 def run_reference(args, rank, world):
     """The oracle, as it stands, timed on the host cores (reference arm)."""
-    cfg, inp, *_ = make_workload(1000, args.workload)
-    quota = fixed_steps_quota(inp, FIXED_STEPS_S) if args.workload == "dream_fixed_steps" else None
+    import oracle
+    cfg, inp, lreqs, blk, *_ = make_workload(1000, args.workload)
+    fixed = args.workload == "dream_fixed_steps"
+    quota = fixed_steps_quota(inp, FIXED_STEPS_S) if fixed else None
     threads = os.cpu_count() or 1
     order = [b for b in range(cfg.B) if inp.masked[b].any()]
     # probe: one pass over the batch on every thread, to size each step's
@@ -648,8 +710,9 @@ def run_reference(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOADS[args.workload], "B": cfg.B, "L": cfg.L, "V": cfg.V,
-                   "sample_rows_per_step": rows_per_step},
+        "config": workload_config(args.workload, cfg, inp, oracle.box_width(list(lreqs.p), list(blk), cfg.L),
+                                  oracle.cost(list(lreqs.p), list(blk), cfg.L), fixed),
+        "sample_rows_per_step": rows_per_step,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": busy, "kind": "oracle",
                          "sample": f"each step: {rows_per_step:.0f} masked rows on average, whole requests of the "
                                    f"{cfg.B}-request batch taken in order (wrapping around), one request per task "
@@ -849,7 +912,8 @@ def main():
     res = run_gpu(args, rank, world, local_rank, dist)
     pipe, cfg = res["pipe"], res["cfg"]
     K = args.steps
-    step_ms = statistics.fmean(res["step_ms"])
+    kern = res["kernel"]
+    step_ms = kern["mean_ms"]
     alg = algorithmic_bytes(cfg, pipe.M)
     achieved = alg / (step_ms / 1e3) / 1e9
     peak, peak_src = load_peaks()
@@ -868,19 +932,20 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": res["seconds"] * 1e3 / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOADS[args.workload], "B": cfg.B, "L": cfg.L, "V": cfg.V, "masked_rows": pipe.M,
-                       "rule": (f"fixed steps, S = {FIXED_STEPS_S} per block" if fixed else
-                                "threshold per request from {0.5,0.6,0.7,0.8,0.9}"),
-                       "mask_fraction": "U[0,1] per request",
-                       "box_W": pipe.W, "box_cost": pipe.cost, "token_budget": BUDGET,
-                       "step": "admit(host)+pack+step+advance/compact (one launch)",
+            "config": workload_config(args.workload, cfg, res["inp"], pipe.W, pipe.cost, fixed),
+            "timing": {"step": (f"admit (host) + pack + step + advance/compact: "
+                                f"{pipe.launches_per_step()} kernel launches"),
                        "l2": "inputs larger than L2: 0.62 GB of masked logits rows per step, no flush",
-                       "state_ring": RING, "roofline_events": f"around every {ROOF_EVERY}th step kernel"},
+                       "state_ring": RING,
+                       "roofline": (f"{kern['n']} step launches after the timed region, each between "
+                                    f"its own CUDA events on fresh state; frac from their mean")},
             "logits_gbs": pipe.M * cfg.V * 2 * K / res["seconds"] / 1e9 / world,
             "step_kernel_ms": step_ms,
-            "step_kernel_ms_median": statistics.median(res["step_ms"]),
-            "step_kernel_ms_min": min(res["step_ms"]),
-            "step_kernel_samples": len(res["step_ms"]),
+            "step_kernel_ms_median": kern["median_ms"],
+            "step_kernel_ms_min": kern["min_ms"],
+            "step_kernel_ms_max": kern["max_ms"],
+            "step_kernel_samples": kern["n"],
+            "step_kernel_back_to_back_ms": kern["back_to_back_mean_ms"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,

@@ -116,6 +116,8 @@ _SIGNATURES = {
     "dllm_predict_steps_stub": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_int32, _p, _p, _p, _p]),
     "dllm_load_control": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_double, _p]),
     "dllm_slo_thresholds": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p, _p, _p]),
+    "dllm_threshold_control": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_int32, _p, _p, _p, _p, _p,
+                                              ctypes.c_double, ctypes.c_double, ctypes.c_double, _p, _p, _p]),
     "dllm_transfer_quota": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "dllm_step_noalloc": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p]),
     "dllm_step_noalloc_capacity": (_sz, []),

@@ -9,8 +9,9 @@ adjustment, ``dllm_slo_thresholds``) then takes the highest allowed threshold
 whose predicted remaining latency fits the request's remaining SLO budget.
 Remaining steps come from ``dllm_predict_steps_stub`` over the block
 features the step emits -- a stand-in for the review's trained step
-predictor.  All of it is host arithmetic in libdllm; this class marshals
-arrays.
+predictor.  All of it, loads and SLO budgets included, is host arithmetic
+in libdllm (``dllm_threshold_control``); this class marshals arrays and
+evaluates the caller's step-latency model at the batch size.
 """
 from __future__ import annotations
 
@@ -38,7 +39,7 @@ class ThresholdController:
             raise ValueError("candidates must be a non-empty ascending list")
         self.L = int(L)
         self.slo_s = float(slo_s)
-        self.capacity = float(tokens_per_s) * self.slo_s
+        self.tokens_per_s = float(tokens_per_s)
         self.step_latency_s = step_latency_s
 
     def choose(self, feats, masked, blocks_left, total_tokens, elapsed_s):
@@ -57,15 +58,13 @@ class ThresholdController:
         feats = np.ascontiguousarray(feats, dtype=np.float32).reshape(A, NUM_FEATURES)
         masked = np.ascontiguousarray(masked, dtype=np.int32)
         left = np.ascontiguousarray(blocks_left, dtype=np.int32)
+        total = np.ascontiguousarray(total_tokens, dtype=np.int64)
+        elapsed = np.ascontiguousarray(elapsed_s, dtype=np.float64)
         steps = np.empty((A, T), dtype=np.float64)
-        _check("dllm_predict_steps_stub",
-               lib.dllm_predict_steps_stub(A, T, _p(self.cand), self.L, _p(feats), _p(masked), _p(left), _p(steps)))
-        load_ = np.ascontiguousarray(steps * np.asarray(total_tokens, dtype=np.float64)[:, None])
         cap = np.empty(A, dtype=np.int32)
-        _check("dllm_load_control", lib.dllm_load_control(A, T, _p(load_), self.capacity, _p(cap)))
-        lat = np.full(A, float(self.step_latency_s(A)), dtype=np.float64)
-        slo_left = np.ascontiguousarray(self.slo_s - np.asarray(elapsed_s, dtype=np.float64))
         choice = np.empty(A, dtype=np.int32)
-        _check("dllm_slo_thresholds",
-               lib.dllm_slo_thresholds(A, T, _p(steps), _p(lat), _p(slo_left), _p(cap), _p(choice)))
+        _check("dllm_threshold_control",
+               lib.dllm_threshold_control(A, T, _p(self.cand), self.L, _p(feats), _p(masked), _p(left), _p(total),
+                                          _p(elapsed), self.slo_s, self.tokens_per_s,
+                                          float(self.step_latency_s(A)), _p(steps), _p(cap), _p(choice)))
         return self.cand[choice].astype(np.float32), choice, cap

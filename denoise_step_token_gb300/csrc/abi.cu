@@ -1,7 +1,7 @@
 // Library-wide entry points of libdllm.so: status strings, ABI checks, the
 // per-device error word and cached device facts.
 
-#include <mutex>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -11,10 +11,12 @@ namespace {
 // First device-side error since the last dllm_get_device_error (one per device).
 __device__ int g_error_word;
 
+// Per-device facts, looked up on first use and then read on every launch
+// without a lock: a lookup that races with another thread's stores the same
+// value, and the atomics publish it.
 constexpr int kMaxDevices = 64;
-int* g_err_ptr[kMaxDevices];
-int g_sm_count[kMaxDevices];
-std::mutex g_mu;
+std::atomic<int*> g_err_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
 
 }  // namespace
 
@@ -25,33 +27,31 @@ void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 int* error_word_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_err_ptr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
-        if (e != cudaSuccess) {
-            note_cuda_error(e);
-            return nullptr;
-        }
-        g_err_ptr[dev] = static_cast<int*>(p);
+    int* p = g_err_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* q = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&q, g_error_word);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return nullptr;
     }
-    return g_err_ptr[dev];
+    g_err_ptr[dev].store(static_cast<int*>(q), std::memory_order_release);
+    return static_cast<int*>(q);
 }
 
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_sm_count[dev] <= 0) {
-        int n = 0;
-        const cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) {
-            note_cuda_error(e);
-            return -1;
-        }
-        g_sm_count[dev] = n;
+    const int n0 = g_sm_count[dev].load(std::memory_order_acquire);
+    if (n0 > 0) return n0;
+    int n = 0;
+    const cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return -1;
     }
-    return g_sm_count[dev];
+    g_sm_count[dev].store(n, std::memory_order_release);
+    return n;
 }
 
 }  // namespace dllm

@@ -47,6 +47,38 @@ long long steps_to_clear(long long m, double P) {
     return n;
 }
 
+// Algorithm 2 over load(i, k): the index of each request's highest allowed
+// threshold.  worst case = committed + load(i, k) + rest[i], rest[i] = the
+// later requests at the lowest threshold summed from the back:
+// rest[R-1] = 0, rest[i] = load(i+1, 0) + rest[i+1].
+template <typename Load>
+void load_control_core(int32_t R, int32_t T, Load load, double capacity, int32_t* max_allowed) {
+    std::vector<double> rest_of((size_t)R, 0.0);
+    for (int32_t i = R - 2; i >= 0; --i) rest_of[i] = load(i + 1, 0) + rest_of[i + 1];
+    double committed = 0.0;
+    for (int32_t i = 0; i < R; ++i) {
+        const double rest = rest_of[i];
+        int32_t keep = 0;
+        for (int32_t k = T - 1; k >= 0; --k) {
+            const double worst = committed + load(i, k) + rest;
+            if (worst <= capacity) {
+                keep = k;
+                break;
+            }
+        }
+        max_allowed[i] = keep;
+        committed += load(i, keep);
+    }
+}
+
+// Algorithm 1 for request i: the highest k <= top whose remaining latency
+// rem_steps[k] * step_latency fits slo_left, else 0.
+int32_t slo_pick(int32_t top, const double* rem_steps, double step_latency, double slo_left) {
+    for (int32_t k = top; k >= 0; --k)
+        if (rem_steps[k] * step_latency <= slo_left) return k;
+    return 0;
+}
+
 }  // namespace
 
 extern "C" int dllm_predict_steps_stub(int32_t R, int32_t T, const double* cand, int32_t L, const float* feats,
@@ -69,25 +101,8 @@ extern "C" int dllm_load_control(int32_t R, int32_t T, const double* load, doubl
     if (R < 0 || T < 1) return DLLM_ERR_INVAL;
     if (R == 0) return DLLM_OK;
     if (!load || !max_allowed) return DLLM_ERR_INVAL;
-    // worst case = committed + load[i][k] + rest[i], rest[i] = the later
-    // requests at the lowest threshold summed from the back:
-    // rest[R-1] = 0, rest[i] = load[i+1][0] + rest[i+1]
-    std::vector<double> rest_of((size_t)R, 0.0);
-    for (int32_t i = R - 2; i >= 0; --i) rest_of[i] = load[(long long)(i + 1) * T] + rest_of[i + 1];
-    double committed = 0.0;
-    for (int32_t i = 0; i < R; ++i) {
-        const double rest = rest_of[i];
-        int32_t keep = 0;
-        for (int32_t k = T - 1; k >= 0; --k) {
-            const double worst = committed + load[(long long)i * T + k] + rest;
-            if (worst <= capacity) {
-                keep = k;
-                break;
-            }
-        }
-        max_allowed[i] = keep;
-        committed += load[(long long)i * T + keep];
-    }
+    load_control_core(R, T, [&](int32_t i, int32_t k) { return load[(long long)i * T + k]; }, capacity,
+                      max_allowed);
     return DLLM_OK;
 }
 
@@ -99,14 +114,33 @@ extern "C" int dllm_slo_thresholds(int32_t R, int32_t T, const double* rem_steps
     for (int32_t i = 0; i < R; ++i) {
         const int32_t top = max_allowed ? max_allowed[i] : T - 1;
         if (top < 0 || top >= T) return DLLM_ERR_INVAL;
-        int32_t pick = 0;
-        for (int32_t k = top; k >= 0; --k) {
-            if (rem_steps[(long long)i * T + k] * step_latency[i] <= slo_left[i]) {
-                pick = k;
-                break;
-            }
-        }
-        choice[i] = pick;
     }
+    for (int32_t i = 0; i < R; ++i)
+        choice[i] = slo_pick(max_allowed ? max_allowed[i] : T - 1, rem_steps + (long long)i * T, step_latency[i],
+                             slo_left[i]);
+    return DLLM_OK;
+}
+
+extern "C" int dllm_threshold_control(int32_t R, int32_t T, const double* cand, int32_t L, const float* feats,
+                                      const int32_t* masked, const int32_t* blocks_left,
+                                      const int64_t* total_tokens, const double* elapsed_s, double slo_s,
+                                      double tokens_per_s, double step_latency_s, double* steps_out,
+                                      int32_t* max_allowed, int32_t* choice) {
+    if (R < 0 || T < 1 || L < 1) return DLLM_ERR_INVAL;
+    if (R == 0) return DLLM_OK;
+    if (!total_tokens || !elapsed_s || !steps_out || !max_allowed || !choice) return DLLM_ERR_INVAL;
+    for (int32_t i = 0; i < R; ++i)
+        if (total_tokens[i] < 0) return DLLM_ERR_INVAL;
+    // item ③: remaining steps per candidate threshold
+    const int rc = dllm_predict_steps_stub(R, T, cand, L, feats, masked, blocks_left, steps_out);
+    if (rc != DLLM_OK) return rc;
+    // item ②: load = total tokens x remaining steps, capacity = tokens/s x SLO
+    load_control_core(
+        R, T, [&](int32_t i, int32_t k) { return steps_out[(long long)i * T + k] * (double)total_tokens[i]; },
+        tokens_per_s * slo_s, max_allowed);
+    // item ①: the highest allowed threshold whose remaining latency fits the
+    // SLO left since the request arrived
+    for (int32_t i = 0; i < R; ++i)
+        choice[i] = slo_pick(max_allowed[i], steps_out + (long long)i * T, step_latency_s, slo_s - elapsed_s[i]);
     return DLLM_OK;
 }

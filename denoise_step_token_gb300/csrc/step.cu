@@ -1278,11 +1278,21 @@ struct ShardOut {
     int* idx;
 };
 
-// Host checks and launch of step_kernel.  quota null selects the threshold
-// rule; logits_rows >= 0 the compact layout; shard non-null S2 alone over a
+// A checked step launch: grid, block, shared memory and parameters.
+struct StepLaunch {
+    bool empty;   // B == 0: nothing to launch
+    int grid;
+    size_t smem;
+    StepParams P;
+};
+
+// Host checks of a step call and its launch parameters; launches nothing
+// and writes no device memory.  quota null selects the threshold rule;
+// logits_rows >= 0 the compact layout; shard non-null S2 alone over a
 // vocabulary shard.
-int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
-                void* stream) {
+int prepare_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
+                 StepLaunch* out) {
+    out->empty = true;
     if (!a) return DLLM_ERR_INVAL;
     if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
     if (a->B == 0) return DLLM_OK;
@@ -1337,7 +1347,7 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
 
     unsigned char* ws = static_cast<unsigned char*>(a->workspace);
     unsigned char* data = ws + ((a->workspace_bytes - w.data_bytes) & ~size_t(255));
-    StepParams P;
+    StepParams& P = out->P;
     P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
     P.list_cap = list_cap; P.static_cap = static_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
     P.div_nc = make_fastdiv((uint32_t)NC);
@@ -1360,8 +1370,24 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
     P.sel = data + w.off_sel;
     P.err = error_word_ptr();
     if (!P.err) return DLLM_ERR_CUDA;
-    DLLM_CUDA_TRY(launch_dependent(step_kernel, dim3(G), dim3(kThreads), smem, as_stream(stream), P));
+    out->grid = G;
+    out->smem = smem;
+    out->empty = false;
     return DLLM_OK;
+}
+
+int launch_prepared(const StepLaunch& sl, void* stream) {
+    if (sl.empty) return DLLM_OK;
+    DLLM_CUDA_TRY(launch_dependent(step_kernel, dim3(sl.grid), dim3(kThreads), sl.smem, as_stream(stream), sl.P));
+    return DLLM_OK;
+}
+
+int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
+                void* stream) {
+    StepLaunch sl;
+    const int rc = prepare_step(a, quota, logits_rows, shard, &sl);
+    if (rc != DLLM_OK) return rc;
+    return launch_prepared(sl, stream);
 }
 
 }  // namespace
@@ -1485,11 +1511,16 @@ extern "C" int dllm_step_noalloc(const dllm_step_args* a, void* stream) {
     if (!dllm::ws_layout(a->B, a->L, a->V, dllm::kNoallocScratchBytes, &w)) return DLLM_ERR_SCRATCH_LIMIT;
     void* scratch = dllm::scratch_ptr();
     if (!scratch) return DLLM_ERR_CUDA;
-    // The array keeps whatever the previous call left; the step needs its
-    // counter region at zero, so clear exactly that part first.
-    DLLM_CUDA_TRY(cudaMemsetAsync(scratch, 0, w.counters_bytes, dllm::as_stream(stream)));
     dllm_step_args b = *a;
     b.workspace = scratch;
     b.workspace_bytes = dllm::kNoallocScratchBytes;
-    return dllm_step(&b, stream);
+    // Every check of dllm_step runs before anything touches the shared
+    // array, so a rejected call leaves it (and everything else) unchanged.
+    dllm::StepLaunch sl;
+    const int rc = dllm::prepare_step(&b, nullptr, -1, nullptr, &sl);
+    if (rc != DLLM_OK) return rc;
+    // The array keeps whatever the previous call left; the step needs its
+    // counter region at zero, so clear exactly that part first.
+    DLLM_CUDA_TRY(cudaMemsetAsync(scratch, 0, w.counters_bytes, dllm::as_stream(stream)));
+    return dllm::launch_prepared(sl, stream);
 }

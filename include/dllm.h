@@ -239,7 +239,9 @@ int32_t dllm_transfer_quota(int32_t L, int32_t S, int32_t s);
  *     other.  Order them on one stream.
  *   - Shapes whose workspace exceeds the buffer (dllm_step_workspace_size
  *     layout; for V near 150k, B * L * ceil(V / 8192) above about 480k) return
- *     DLLM_ERR_SCRATCH_LIMIT and launch nothing. */
+ *     DLLM_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - Every argument check of dllm_step runs before the memset: a call that
+ *     returns an error has queued nothing and left the buffer as it was. */
 int dllm_step_noalloc(const dllm_step_args* args, void* stream);
 
 /* Bytes of dllm_step_noalloc's built-in scratch buffer per device. */
@@ -289,6 +291,28 @@ int dllm_load_control(int32_t R, int32_t T, const double* load, double capacity,
  * DLLM_ERR_INVAL for a max_allowed entry outside [0, T). */
 int dllm_slo_thresholds(int32_t R, int32_t T, const double* rem_steps, const double* step_latency,
                         const double* slo_left, const int32_t* max_allowed, int32_t* choice);
+
+/* One decision of the whole controller for R active requests (items ③, ②
+ * and ① in that order), all host arithmetic in double precision:
+ *   steps_out[i][k]  = dllm_predict_steps_stub(cand, L, feats, masked,
+ *                      blocks_left) (remaining steps at threshold k);
+ *   load[i][k]       = steps_out[i][k] * total_tokens[i] (prompt + output
+ *                      tokens; item ②);
+ *   max_allowed[i]   = dllm_load_control over that load with capacity =
+ *                      tokens_per_s * slo_s;
+ *   choice[i]        = dllm_slo_thresholds with step latency step_latency_s
+ *                      (the latency of one step at the current batch size,
+ *                      from the instance's one-off profile) and
+ *                      slo_left[i] = slo_s - elapsed_s[i] (the SLO budget
+ *                      left since request i arrived).
+ * Outputs: steps_out [R][T], max_allowed [R], choice [R] (host).  Inputs
+ * as for dllm_predict_steps_stub, plus total_tokens [R] (>= 0) and
+ * elapsed_s [R] (host).  DLLM_ERR_INVAL for a NULL array, a negative token
+ * count or any input dllm_predict_steps_stub rejects. */
+int dllm_threshold_control(int32_t R, int32_t T, const double* cand, int32_t L, const float* feats,
+                           const int32_t* masked, const int32_t* blocks_left, const int64_t* total_tokens,
+                           const double* elapsed_s, double slo_s, double tokens_per_s, double step_latency_s,
+                           double* steps_out, int32_t* max_allowed, int32_t* choice);
 
 /* ======================================================================
  * Bounding-box planning and admission (host functions).

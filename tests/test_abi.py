@@ -175,6 +175,52 @@ def test_threshold_control_matches_oracle():
         np.testing.assert_array_equal(choice, [oc.slo_threshold(steps[i], lat[i], slo[i], keep[i]) for i in range(R)])
     bad = np.array([7], dtype=np.int32)
     one = np.ones(T)
+    # the same rejection when an entry is out of range after a valid one
+    two = np.array([0, 7], dtype=np.int32)
+    assert lib.dllm_slo_thresholds(2, T, _dptr(np.ones(2 * T)), _dptr(np.ones(2)), _dptr(np.ones(2)), _dptr(two),
+                                   _dptr(np.empty(2, dtype=np.int32))) == -1
     assert lib.dllm_slo_thresholds(1, T, _dptr(one), _dptr(one[:1]), _dptr(one[:1]), _dptr(bad),
                                    _dptr(np.empty(1, dtype=np.int32))) == -1
     assert lib.dllm_load_control(1, 0, None, 1.0, None) == -1
+
+
+def test_threshold_control_decision_matches_oracle():
+    """dllm_threshold_control (the whole decision: predicted steps, load =
+    steps x total tokens, Algorithm 2 at capacity = tokens/s x SLO, Algorithm
+    1 against the SLO left since arrival) equals the oracle's functions
+    composed in that order, exactly, on random inputs."""
+    from oracle import control as oc
+    lib = dllm.load()
+    rng = np.random.default_rng(16)
+    cand = np.array([0.5, 0.6, 0.7, 0.8, 0.9])
+    T, L = len(cand), 32
+    for trial in range(20):
+        R = int(rng.integers(1, 60))
+        q = np.sort(rng.random((R, 4)).astype(np.float32), axis=1)
+        feats = np.stack([q[:, 0], q[:, 1], q[:, 2], q.mean(axis=1), q[:, 3], rng.random(R)], axis=1).astype(np.float32)
+        feats[rng.random(R) < 0.2, :5] = np.nan
+        masked = rng.integers(0, L + 1, size=R).astype(np.int32)
+        left = rng.integers(0, 8, size=R).astype(np.int32)
+        total = rng.integers(64 + 256, 1024 + 256, size=R).astype(np.int64)
+        elapsed = rng.uniform(0.0, 2.0, size=R)
+        slo, tps, lat = float(rng.uniform(0.5, 3.0)), float(rng.uniform(1e4, 2e5)), float(rng.uniform(1e-3, 2e-2))
+        steps = np.empty((R, T))
+        cap = np.empty(R, dtype=np.int32)
+        choice = np.empty(R, dtype=np.int32)
+        assert lib.dllm_threshold_control(R, T, _dptr(cand), L, _dptr(feats), _dptr(masked), _dptr(left),
+                                          _dptr(total), _dptr(elapsed), slo, tps, lat, _dptr(steps), _dptr(cap),
+                                          _dptr(choice)) == 0
+        want_steps = np.array([[oc.predict_steps_stub(t, feats[i], masked[i], left[i], L) for t in cand]
+                               for i in range(R)])
+        np.testing.assert_array_equal(steps, want_steps)
+        want_cap = oc.load_control(want_steps * total[:, None].astype(np.float64), tps * slo)
+        np.testing.assert_array_equal(cap, want_cap)
+        want_choice = [oc.slo_threshold(want_steps[i], lat, slo - elapsed[i], want_cap[i]) for i in range(R)]
+        np.testing.assert_array_equal(choice, want_choice)
+    z = np.zeros(1)
+    assert lib.dllm_threshold_control(1, T, _dptr(cand), L, _dptr(np.zeros(6, np.float32)), _dptr(np.zeros(1, np.int32)),
+                                      _dptr(np.zeros(1, np.int32)), _dptr(np.array([-1], np.int64)), _dptr(z), 1.0,
+                                      1.0, 1.0, _dptr(np.empty(T)), _dptr(np.empty(1, np.int32)),
+                                      _dptr(np.empty(1, np.int32))) == -1
+    assert lib.dllm_threshold_control(0, T, None, L, None, None, None, None, None, 1.0, 1.0, 1.0, None, None,
+                                      None) == 0

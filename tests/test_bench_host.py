@@ -1,6 +1,7 @@
 """bench.py's host-side arithmetic on CPU: the algorithmic bytes of a step,
 the launches of one pipeline step, the traffic read from the committed
-profile only while the kernel source matches, and the clock summary."""
+capture record only while the kernel source matches, and the clock
+summary."""
 import types
 
 import pytest
@@ -27,12 +28,32 @@ def test_launches_per_step(B, L, shards, expected):
     assert bench.Pipeline.launches_per_step(pipe) == expected
 
 
-def test_traffic_only_for_the_profiled_source():
+def test_traffic_only_for_the_profiled_source(tmp_path):
+    import json
+
     import bench
     sha = bench.step_source_sha()
-    traffic = bench.load_traffic(sha)
-    assert traffic is not None and traffic > bench.algorithmic_bytes(__import__("synth").STEP_CONFIGS["dream"], 1851)
-    assert bench.load_traffic("0" * 16) is None
+    rec = tmp_path / "rec.json"
+    rec.write_text(json.dumps({"source_sha256": sha, "dram_bytes_per_launch": 573530624}))
+    assert bench.load_traffic(sha, path=str(rec)) == 573530624.0
+    # a capture of another kernel source is not reported
+    assert bench.load_traffic("0" * 16, path=str(rec)) is None
+    # no record, or a malformed one: no traffic
+    assert bench.load_traffic(sha, path=str(tmp_path / "missing.json")) is None
+    bad = tmp_path / "bad.json"
+    bad.write_text("not json")
+    assert bench.load_traffic(sha, path=str(bad)) is None
+
+
+def test_committed_traffic_record_is_well_formed():
+    import json
+
+    import bench
+    with open(bench.TRAFFIC_JSON, encoding="utf-8") as f:
+        rec = json.load(f)
+    assert len(rec["source_sha256"]) == 16 and "--clock-control none" in rec["command"]
+    # DRAM traffic can't be below the bytes the launch must move
+    assert rec["dram_bytes_per_launch"] >= bench.algorithmic_bytes(__import__("synth").STEP_CONFIGS["dream"], 1851)
 
 
 def test_clock_summary():

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import MARGIN
+from helpers import MARGIN, per_request_oracle_loop, request_block_logits
 from oracle.loop import OracleLoop
 
 pytestmark = pytest.mark.gpu
@@ -267,19 +267,28 @@ def test_loop_runs_under_the_library_controller(dllm, device):
     assert mean_thr[0.02] < mean_thr[10.0]
 
 
-def _lockstep_native(dllm, device, cfg, mode, seed, reloop=False, S=None, max_iters=10000):
+def _lockstep_native(dllm, device, cfg, mode, seed, reloop=False, S=None, max_iters=10000, per_request=False):
     """libdllm's native loop (dllm_loop_*) in lockstep with the oracle loop:
     admissions, box, masked rows, step outputs, commits, evictions and the
-    final tokens."""
+    final tokens.  ``per_request``: the oracle's step runs request by request
+    on the host's cores and the device receives only the masked positions'
+    rows (scattered into a poisoned [capacity * L, ldv] buffer), which keeps
+    a full-vocabulary run within minutes."""
     import torch
     from denoise_step_token_gb300.loop import NativeLoop
     reqs = synth.make_loop_requests(cfg, seed)
     R, L, V = cfg.R, cfg.L, cfg.V
     prompts = [reqs.prompt_tokens[reqs.prompt_off[r]:reqs.prompt_off[r + 1]] for r in range(R)]
-    ol = OracleLoop(reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode, S=S)
+    oargs = (reqs.p, reqs.K, prompts, reqs.thr, L, V, cfg.mask_id, cfg.pad_id, cfg.budget, mode)
+    ol = per_request_oracle_loop(*oargs, S=S) if per_request else OracleLoop(*oargs, S=S)
     nl = NativeLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V, mask_id=cfg.mask_id,
                     pad_id=cfg.pad_id, budget=cfg.budget, device=device, mode=mode, reloop=reloop, S=S)
+    poison = int(np.int16(np.uint16(synth.POISON_BITS).view(np.int16)))
+    dev_logits = None
+    if per_request:
+        dev_logits = torch.full((R * L, cfg.row_stride), poison, dtype=torch.int16, device=device)
     salts = {}
+    masked_total = 0
     while not ol.finished() and ol.iteration < max_iters:
         assert not nl.finished()
         new_o = ol.admit_phase()
@@ -297,12 +306,26 @@ def _lockstep_native(dllm, device, cfg, mode, seed, reloop=False, S=None, max_it
             np.testing.assert_array_equal(nl.view(inf.box_pad, (A,), torch.int32).cpu().numpy(), box_o["pad"])
         rows_o = ol.masked_rows()
         assert rows_o == nl.masked_rows()
-        thr_of_row = np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32)
-        logits = _loop_logits(seed, rows_o, len(ol.rid), L, V, cfg.offset_max, cfg.mask_id, thr_of_row, salts,
-                              cfg.row_stride, ol.quota())
-        ref = ol.step_phase(logits[: len(ol.rid) * L])
+        masked_total += len(rows_o)
         A = len(ol.rid)
-        inf = nl.end(torch.from_numpy(logits[: max(A, 1) * L].view(np.int16)).to(device))
+        if per_request:
+            q = ol.quota()
+            fn = lambda i, rows_i: request_block_logits(seed, rows_i, L, V, cfg.row_stride, cfg.offset_max,
+                                                        cfg.mask_id, reqs.thr[ol.rid[i]], salts,
+                                                        None if q is None else int(q[i]))
+            ref, blocks = ol.step_phase_per_request(fn)
+            idx = torch.as_tensor([r[0] for r in rows_o], dtype=torch.int64, device=device)
+            if len(rows_o):
+                rows_h = np.stack([blocks[r[0] // L][r[4]] for r in rows_o])
+                dev_logits.index_copy_(0, idx, torch.from_numpy(rows_h.view(np.int16)).to(device))
+            inf = nl.end(dev_logits[: max(A, 1) * L])
+            dev_logits.index_fill_(0, idx, poison)
+        else:
+            thr_of_row = np.array([reqs.thr[r] for r in ol.rid], dtype=np.float32)
+            logits = _loop_logits(seed, rows_o, len(ol.rid), L, V, cfg.offset_max, cfg.mask_id, thr_of_row, salts,
+                                  cfg.row_stride, ol.quota())
+            ref = ol.step_phase(logits[: len(ol.rid) * L])
+            inf = nl.end(torch.from_numpy(logits[: max(A, 1) * L].view(np.int16)).to(device))
         if A:
             np.testing.assert_array_equal(nl.view(inf.done, (A,), torch.uint8).cpu().numpy(), ref["done"])
             np.testing.assert_array_equal(nl.view(inf.n_new, (A,), torch.int32).cpu().numpy(), ref["n_new"])
@@ -320,6 +343,7 @@ def _lockstep_native(dllm, device, cfg, mode, seed, reloop=False, S=None, max_it
     for r in range(R):
         np.testing.assert_array_equal(gen[r][: reqs.K[r] * L], ol.gen[r])
     assert dllm.get_device_error(device) == 0
+    nl.masked_total = masked_total
     return ol, nl
 
 
@@ -335,3 +359,15 @@ def test_native_loop_lockstep(dllm, device, mode, reloop, S):
 def test_native_loop_blockserve_shape_reduced_vocab(dllm, device):
     cfg = synth.LoopConfig("bs_small_v", 256, 64, 1024, 256, 32, 1031, 1 << 20, 0.9, 8.0)
     _lockstep_native(dllm, device, cfg, "fdfo", seed=5, reloop=True)
+
+
+def test_native_loop_blockserve_full_vocabulary(dllm, device):
+    """The BlockServe mixed-state loop at its own size: 256 requests with
+    prompts U[64, 1024], 8 blocks of 32, V = 126464 (LLaDA-8B's vocabulary),
+    token budget 2^20, FDFO with the in-place re-loop, served to completion
+    in lockstep with the oracle loop (every admission, box, masked row, step
+    output, commit and eviction; the final tokens)."""
+    cfg = synth.LOOP_CONFIGS["blockserve"]
+    assert (cfg.R, cfg.L, cfg.V, cfg.budget) == (256, 32, 126464, 1 << 20)
+    ol, nl = _lockstep_native(dllm, device, cfg, "fdfo", seed=2000, reloop=True, per_request=True)
+    assert ol.iteration > 0 and nl.masked_total >= cfg.R * cfg.gen

@@ -77,18 +77,18 @@ def test_quota_schedule_unmasks_a_block_in_S_steps(dllm, device, S):
     assert not (inp.input_ids == cfg.mask_id).any()
 
 
-def test_quota_full_size_sampled(dllm, device):
+def test_quota_full_size(dllm, device):
     """Dream-shaped batch with per-request steps-in-block drawn at random and
-    S in {32, 8}: the oracle recomputes a sample of requests."""
+    S in {32, 8}: every request against the oracle."""
     cfg = synth.STEP_CONFIGS["dream"]
     inp = synth.make_step_state(cfg, 12)
     rng = np.random.default_rng(4)
     S = rng.choice([32, 8], size=cfg.B)
     s = rng.integers(0, 40, size=cfg.B)
     quota = np.array([oracle.transfer_quota(cfg.L, int(S[b]), int(s[b])) for b in range(cfg.B)], dtype=np.int32)
-    sample = sorted(rng.choice(cfg.B, size=12, replace=False).tolist())
-    enforce_margins(inp, sample, quota=quota)
-    ref = oracle_step(inp, sample, quota=quota)
+    sample = list(range(cfg.B))
+    enforce_margins(inp, quota=quota)
+    ref = oracle_step(inp, quota=quota)
     got, ids, cs = run_quota(dllm, inp, device, quota)
     compare_step(ref, got, sample, cfg.L, ids, cs)
     m_in = inp.masked

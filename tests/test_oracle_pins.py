@@ -661,6 +661,33 @@ def test_predict_steps_grows_with_the_threshold():
         assert steps[0] >= (1 if m else 0) + kb
 
 
+def test_predict_steps_stub_hand_values():
+    """The stub's composition worked out by hand (a pin of the whole
+    predictor, not of its parts alone).
+
+    Case 1: t = 0.7, features (min .5, q25 .6, median .8, avg -, q75 .9, -),
+    5 positions still masked, 2 blocks left, L = 4.
+      rate_above: 0.7 lies in [q25, median) = [.6, .8):
+        F = .25 + (.7 - .6) / (.8 - .6) * .25 = .375, so P = .625.
+      current block, m = 5: take floor(3.125) = 3 -> 2; floor(1.25) = 1 -> 1;
+        floor(.625) = 0, at least 1 -> 0: 3 steps.
+      a full block, m = 4: floor(2.5) = 2 -> 2; 1 -> 1; 1 -> 0: 3 steps.
+      total = 3 + 2 * 3 = 9.  (Counting the current block twice, or one
+      full block too many, gives 12; leaving it out gives 6.)
+    Case 2: nothing unmasked yet (NaN features) -> uniform: P = 1 - .5 = .5;
+      8 masked, 3 blocks left, L = 8: 8 -> 4 -> 2 -> 1 -> 0 is 4 steps, a
+      full block also 4: total = 4 + 3 * 4 = 16.
+    Case 3: t above q75's segment, at .95 in [.9, 1): F = .75 + .5 * .25 =
+      .875, P = .125; m = 3: floor(.375) = 0 -> 1 each step: 3 steps; no
+      block left: total 3."""
+    from oracle.control import predict_steps_stub
+    f = [0.5, 0.6, 0.8, 0.7, 0.9, 0.25]
+    assert predict_steps_stub(0.7, f, 5, 2, 4) == 9
+    nan = [float("nan")] * 5 + [0.0]
+    assert predict_steps_stub(0.5, nan, 8, 3, 8) == 16
+    assert predict_steps_stub(0.95, f, 3, 0, 4) == 3
+
+
 def test_load_control_hand_case():
     from oracle.control import load_control
     load = [[1, 2, 4], [1, 3, 5], [2, 2, 6]]

@@ -4,10 +4,12 @@ Such callers (an engine whose pool already owns all of HBM, a plain C host
 with no allocator, a loop where an allocation may not synchronise the
 device) call dllm_step_noalloc, which uses a buffer built into the library
 instead of a caller workspace.  This test calls it through the C ABI twice
-in a row and checks both results against dllm_step with a caller
-workspace, within the tolerances of the other step tests.  It lives in a
-file of its own that pytest collects last, and it passes both alone in a
-fresh process and after the rest of the suite.
+in a row -- the second call on a larger shape, so that the buffer's reuse
+across shapes is exercised -- and checks both results against dllm_step with
+a caller workspace and against the CPU oracle, within the tolerances of the
+other step tests.  It lives in a file of its own that pytest collects last,
+and it passes both alone in a fresh process and after the rest of the
+suite.
 """
 import ctypes
 
@@ -15,7 +17,7 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import CONF_TOL, device_logits, device_state, enforce_margins
+from helpers import CONF_TOL, compare_step, device_logits, device_state, enforce_margins, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -59,15 +61,25 @@ def _same(a, b, masked):
     np.testing.assert_allclose(a["feats"], b["feats"], rtol=0, atol=CONF_TOL, equal_nan=True)
 
 
-def test_noalloc_matches_step_twice(dllm):
+# two calls in a row: the second has more rows and chunks per row (a larger
+# counter region to clear, a data region placed elsewhere in the buffer)
+CALLS = [
+    synth.StepConfig("noalloc_a", 24, 32, 40001, 12.0, "fraction", synth.THRESHOLD_SET, ldv=40016),
+    synth.StepConfig("noalloc_b", 40, 64, 70000, 12.0, "fraction", synth.THRESHOLD_SET),
+]
+
+
+def test_noalloc_matches_step_and_oracle_twice(dllm):
     import torch
     device = torch.device("cuda", 0)
     lib = dllm.load()
     stream = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
-    cfg = synth.StepConfig("noalloc", 24, 32, 40001, 12.0, "fraction", synth.THRESHOLD_SET, ldv=40016)
-    for call, seed in enumerate((31, 32)):          # two calls in a row, different batches
+    nc = lambda c: -(-c.V // 8192)
+    assert CALLS[1].B * CALLS[1].L * nc(CALLS[1]) > CALLS[0].B * CALLS[0].L * nc(CALLS[0])
+    for call, (cfg, seed) in enumerate(zip(CALLS, (31, 32))):
         inp = synth.make_step_state(cfg, seed)
         enforce_margins(inp)
+        ref = oracle_step(inp)
         logits = device_logits(inp, device)
 
         ids, thr, cs = device_state(inp, device)
@@ -84,6 +96,7 @@ def test_noalloc_matches_step_twice(dllm):
         got = _host(out2, ids2, cs2)
         assert dllm.get_device_error(device) == 0
         _same(got, want, inp.masked)
+        compare_step(ref, got, list(range(cfg.B)), cfg.L, got["input_ids"], got["conf_state"])
 
 
 def test_noalloc_rejects_shapes_beyond_its_buffer(dllm):
@@ -95,3 +108,33 @@ def test_noalloc_rejects_shapes_beyond_its_buffer(dllm):
                       thr=0x30000, conf_state=0x40000, done=0x50000, accept_len=0x60000, n_new=0x70000)
     assert lib.dllm_step_workspace_size(4096, 64, 1 << 20) > cap
     assert lib.dllm_step_noalloc(ctypes.byref(a), None) == -7
+
+
+def test_noalloc_rejected_calls_then_a_good_one(dllm):
+    """Calls that fail dllm_step's own checks (alignment, stride, a missing
+    pointer) return that check's code -- the library runs every check before
+    it clears the buffer -- and the next valid call still matches the
+    oracle."""
+    import torch
+    device = torch.device("cuda", 0)
+    lib = dllm.load()
+    stream = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    cfg = CALLS[0]
+    inp = synth.make_step_state(cfg, 33)
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    logits = device_logits(inp, device)
+    ids, thr, cs = device_state(inp, device)
+    out = _outputs(torch, device, cfg.B, cfg.L)
+    good = _args(dllm, cfg, logits, ids, thr, cs, out)
+    # misaligned logits, a row stride that is not a multiple of 8, a missing
+    # output pointer: each rejected with its code before anything is queued
+    for field, value, code in (("logits", logits.data_ptr() + 2, -2), ("ldv", cfg.row_stride + 1, -2),
+                               ("n_new", None, -1)):
+        bad = dllm.StepArgs.from_buffer_copy(good)
+        setattr(bad, field, value)
+        assert lib.dllm_step_noalloc(ctypes.byref(bad), stream) == code, field
+    assert lib.dllm_step_noalloc(ctypes.byref(good), stream) == 0
+    got = _host(out, ids, cs)
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, got["input_ids"], got["conf_state"])
