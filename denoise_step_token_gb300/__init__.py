@@ -102,6 +102,7 @@ _lock = threading.Lock()
 _SIGNATURES = {
     "dllm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "dllm_abi_version": (ctypes.c_int, []),
+    "dllm_inject_cuda_error": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32]),
     "dllm_last_cuda_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_char_p)]),
     "dllm_struct_size": (_sz, [ctypes.c_int]),
     "dllm_get_device_error": (ctypes.c_int, [_p, ctypes.POINTER(_i32)]),

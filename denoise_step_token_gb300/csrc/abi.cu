@@ -21,8 +21,16 @@ std::atomic<int> g_sm_count[kMaxDevices];
 }  // namespace
 
 thread_local int t_last_cuda_error = 0;
+thread_local int t_inject_code = 0;        // status to report instead of a CUDA call
+thread_local int t_inject_countdown = 0;   // the call that reports it (1 = the next one)
 
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
+cudaError_t injected_cuda_error() {
+    if (t_inject_countdown <= 0) return cudaSuccess;
+    if (--t_inject_countdown > 0) return cudaSuccess;
+    return static_cast<cudaError_t>(t_inject_code);
+}
 
 int* error_word_ptr() {
     int dev = 0;
@@ -71,6 +79,13 @@ extern "C" const char* dllm_strerror(int code) {
 }
 
 extern "C" int dllm_abi_version(void) { return DLLM_ABI_VERSION; }
+
+extern "C" int dllm_inject_cuda_error(int32_t cuda_error, int32_t countdown) {
+    if (countdown < 0 || (countdown > 0 && cuda_error == 0)) return DLLM_ERR_INVAL;
+    dllm::t_inject_code = cuda_error;
+    dllm::t_inject_countdown = countdown;
+    return DLLM_OK;
+}
 
 extern "C" int dllm_last_cuda_error(const char** name) {
     const int e = dllm::t_last_cuda_error;

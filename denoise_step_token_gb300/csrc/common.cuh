@@ -17,13 +17,18 @@ namespace dllm {
 // Remember the failing CUDA status for dllm_last_cuda_error().
 void note_cuda_error(cudaError_t e);
 
-#define DLLM_CUDA_TRY(expr)                     \
-    do {                                        \
-        cudaError_t _e = (expr);                \
-        if (_e != cudaSuccess) {                \
-            ::dllm::note_cuda_error(_e);        \
-            return DLLM_ERR_CUDA;               \
-        }                                       \
+// Fault injection (dllm_inject_cuda_error): a CUDA status to report in
+// place of one of this thread's coming CUDA calls, or cudaSuccess.
+cudaError_t injected_cuda_error();
+
+#define DLLM_CUDA_TRY(expr)                                             \
+    do {                                                                \
+        cudaError_t _e = ::dllm::injected_cuda_error();                 \
+        if (_e == cudaSuccess) _e = (expr);                             \
+        if (_e != cudaSuccess) {                                        \
+            ::dllm::note_cuda_error(_e);                                \
+            return DLLM_ERR_CUDA;                                       \
+        }                                                               \
     } while (0)
 
 // Device address of the current device's error word (set up once per device).
@@ -111,15 +116,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of a barrier; gives up after `limit_ns` and
 // returns false (the caller records DLLM_DEVERR_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+#if defined(DLLM_WAIT_SLEEP_NS) && DLLM_WAIT_SLEEP_NS > 0
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t ts = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(DLLM_WAIT_SLEEP_NS);
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && globaltimer_ns() - ts > limit_ns) return false;
+    }
+#else
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
     }
+#endif
 }
 
 // Bulk (TMA-engine) copy global -> shared, completing on an mbarrier --------
@@ -143,6 +171,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Packed f32x2 arithmetic (sm_100 and later): a 64-bit register pair holds
+// two floats, low word first.
+__device__ __forceinline__ unsigned long long f32x2_splat(float x) {
+    const unsigned long long u = __float_as_uint(x);
+    return (u << 32) | u;
+}
+
+// acc += (2^(lo * s + n), 2^(hi * s + n)) for the two bf16 values of `w`
+// (lo = the low half, widened exactly by moving it to the top 16 bits; hi =
+// the high half with the low 16 bits cleared).  s and n are f32x2 pairs.
+// Each half is rounded exactly as fmaf, ex2.approx.ftz and a float add
+// would round it.
+__device__ __forceinline__ void acc_exp2_bf16x2(unsigned long long& acc, uint32_t w, unsigned long long s,
+                                                unsigned long long n) {
+    asm("{\n\t.reg .b32 l, h;\n\t.reg .b64 p;\n\t"
+        "prmt.b32 l, %1, 0, 0x1044;\n\t"
+        "and.b32 h, %1, 0xffff0000;\n\t"
+        "mov.b64 p, {l, h};\n\t"
+        "fma.rn.f32x2 p, p, %2, %3;\n\t"
+        "mov.b64 {l, h}, p;\n\t"
+        "ex2.approx.ftz.f32 l, l;\n\t"
+        "ex2.approx.ftz.f32 h, h;\n\t"
+        "mov.b64 p, {l, h};\n\t"
+        "add.rn.f32x2 %0, %0, p;\n\t}"
+        : "+l"(acc)
+        : "r"(w), "l"(s), "l"(n));
 }
 
 // Elementwise max of two packed bf16 pairs.

@@ -72,6 +72,12 @@ namespace {
 #ifndef DLLM_STEP_TAIL_DEN
 #define DLLM_STEP_TAIL_DEN 4
 #endif
+#ifndef DLLM_STEP_IDLE_NS
+#define DLLM_STEP_IDLE_NS 64  // a warp with an empty finish queue sleeps this long between polls
+#endif
+#ifndef DLLM_STEP_F32X2
+#define DLLM_STEP_F32X2 1     // packed f32x2 FMA / add in the element loop
+#endif
 
 constexpr int kStreamWarps = DLLM_STEP_WARPS;         // warps streaming logits
 constexpr int kFinishWarps = DLLM_STEP_FINISHERS;     // warps finishing rows and requests
@@ -90,7 +96,10 @@ constexpr int kBatchElems = kBatchVecs * 8 * 32;      // 2048 contiguous element
 constexpr int kBatchesPerCopy = kCopyElems / kBatchElems;
 constexpr int kBatchesPerChunk = kChunkElems / kBatchElems;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s for any single wait
+#ifndef DLLM_STEP_WAIT_LIMIT_NS
+#define DLLM_STEP_WAIT_LIMIT_NS 1000000000ull          // 1 s for any single wait
+#endif
+constexpr uint64_t kWaitLimitNs = DLLM_STEP_WAIT_LIMIT_NS;
 
 static_assert(kCopyElems % kBatchElems == 0, "a copy holds whole batches");
 static_assert(kChunkElems % kCopyElems == 0, "a chunk holds whole copies");
@@ -237,6 +246,24 @@ __device__ __forceinline__ void fold_batch(const uint4 (&v)[kBatchVecs], int kba
     }
     if (m == -INFINITY) return;   // nothing finite seen yet: the batch adds 0
     const float nb = -m * kLog2e;
+#if DLLM_STEP_F32X2
+    // Two elements per instruction: (lo, hi) of a bf16 pair as an f32x2,
+    // one packed FMA for the exponent arguments, two ex2, one packed add.
+    // Per lane the accumulators, their order and every rounding are those
+    // of the scalar loop below (a0 and a1 share one pair, a2 and a3 the
+    // other), so the two loops give bit-identical sums.
+    const unsigned long long s2 = f32x2_splat(kLog2e), n2 = f32x2_splat(nb);
+    unsigned long long p01 = 0ull, p23 = 0ull;
+#pragma unroll
+    for (int k = 0; k < kBatchVecs; ++k) {
+        acc_exp2_bf16x2(p01, v[k].x, s2, n2);
+        acc_exp2_bf16x2(p23, v[k].y, s2, n2);
+        acc_exp2_bf16x2(p01, v[k].z, s2, n2);
+        acc_exp2_bf16x2(p23, v[k].w, s2, n2);
+    }
+    const float a0 = __uint_as_float((uint32_t)p01), a1 = __uint_as_float((uint32_t)(p01 >> 32));
+    const float a2 = __uint_as_float((uint32_t)p23), a3 = __uint_as_float((uint32_t)(p23 >> 32));
+#else
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int k = 0; k < kBatchVecs; ++k) {
@@ -249,6 +276,7 @@ __device__ __forceinline__ void fold_batch(const uint4 (&v)[kBatchVecs], int kba
         a2 += ex2_approx(fmaf(bf16_lo(v[k].w), kLog2e, nb));
         a3 += ex2_approx(fmaf(bf16_hi(v[k].w), kLog2e, nb));
     }
+#endif
     s += (a0 + a1) + (a2 + a3);
 }
 
@@ -724,7 +752,7 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
 __device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t* s_gmask, int* s_queue, int* s_qhead,
                                             const int* s_ndone, int lane) {
     uint32_t idle = 0;
-    const uint64_t t0 = globaltimer_ns();
+    uint64_t t0 = globaltimer_ns();
     int h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
     h = __shfl_sync(0xffffffffu, h, 0);
     while (h < P.list_cap) {
@@ -733,6 +761,7 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t*
         if (v != 0) {
             __syncwarp();   // lane 0's acquire orders the whole warp's reads
             finish_row(P, s_gmask, v - 1, s_queue[2 * h + 1], lane);
+            t0 = globaltimer_ns();   // the limit bounds idle waiting, not work
             h = (lane == 0) ? atomicAdd(s_qhead, 1) : 0;
             h = __shfl_sync(0xffffffffu, h, 0);
             continue;
@@ -745,7 +774,7 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t*
             if (__shfl_sync(0xffffffffu, v2, 0) != 0) continue;
             break;
         }
-        __nanosleep(64);
+        __nanosleep(DLLM_STEP_IDLE_NS);
         if ((++idle & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
             if (lane == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
             break;

@@ -75,6 +75,15 @@ int dllm_last_cuda_error(const char** name);
  * 6 dllm_loop_info_t.  Returns 0 for an unknown `which`. */
 size_t dllm_struct_size(int which);
 
+/* Fault injection for tests of the status plumbing (host only; nothing
+ * reaches the GPU).  The `countdown`-th CUDA runtime call that this library
+ * makes next on the calling thread is not made: it reports `cuda_error` (a
+ * cudaError_t value) instead, so the entry point that made it returns
+ * DLLM_ERR_CUDA and dllm_last_cuda_error() names `cuda_error`.  Calls
+ * before it run normally; countdown 0 disarms.  DLLM_ERR_INVAL for a
+ * negative countdown or a zero cuda_error with a countdown. */
+int dllm_inject_cuda_error(int32_t cuda_error, int32_t countdown);
+
 /* Synchronise `stream`, then return in *code the first device error
  * recorded on the current device since the last call (DLLM_DEVERR_*), and
  * clear it.  Returns DLLM_ERR_CUDA if the synchronisation fails. */

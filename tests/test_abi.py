@@ -224,3 +224,38 @@ def test_threshold_control_decision_matches_oracle():
                                       _dptr(np.empty(1, np.int32))) == -1
     assert lib.dllm_threshold_control(0, T, None, L, None, None, None, None, None, 1.0, 1.0, 1.0, None, None,
                                       None) == 0
+
+
+def test_injected_cuda_error_reaches_the_caller():
+    """The status plumbing from a failing CUDA call to the caller, with the
+    failure injected on the host (the call is not made, so the fake pointer
+    below is never touched): the entry point returns DLLM_ERR_CUDA,
+    dllm_last_cuda_error names the injected status and the binding raises
+    DllmError with that name."""
+    lib = dllm.load()
+    OOM = 2                                     # cudaErrorMemoryAllocation
+    assert lib.dllm_inject_cuda_error(OOM, -1) == -1
+    assert lib.dllm_inject_cuda_error(0, 1) == -1
+    assert lib.dllm_inject_cuda_error(OOM, 1) == 0
+    assert lib.dllm_workspace_init(ctypes.c_void_p(0x100000), 256, None) == -3
+    name = ctypes.c_char_p()
+    assert lib.dllm_last_cuda_error(ctypes.byref(name)) == OOM
+    assert name.value == b"cudaErrorMemoryAllocation"
+    with pytest.raises(dllm.DllmError, match="cudaErrorMemoryAllocation"):
+        dllm._check("dllm_workspace_init", -3)
+    assert lib.dllm_inject_cuda_error(0, 0) == 0
+
+
+def test_injection_countdown_without_a_gpu():
+    """Countdown 2: the first CUDA call is made (and, with no GPU, fails with
+    its own status); the second reports the injected one."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the first call would really run")
+    lib = dllm.load()
+    OOM = 2
+    assert lib.dllm_inject_cuda_error(OOM, 2) == 0
+    assert lib.dllm_workspace_init(ctypes.c_void_p(0x100000), 256, None) == -3
+    assert lib.dllm_last_cuda_error(None) not in (0, OOM)
+    assert lib.dllm_workspace_init(ctypes.c_void_p(0x100000), 256, None) == -3
+    assert lib.dllm_last_cuda_error(None) == OOM
