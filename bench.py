@@ -331,6 +331,7 @@ class Pipeline:
                 a.V = bounds[k + 1] - bounds[k]
                 a.logits = ctypes.c_void_p(self.logits.data_ptr() + bounds[k] * 2)
                 self.shards.append((bounds[k], a))
+        self.fused = self.shards is None   # the vocabulary-sharded step keeps its separate commit
         self.quota = None
         if fixed_steps is not None:
             steps = L - inp.masked.sum(axis=1)
@@ -383,19 +384,39 @@ class Pipeline:
     def run(self, slot, stream, ev_before=None, ev_after=None, compact=None):
         """One pipeline step on state slot ``slot``.  ``compact``: (device
         logits of the masked rows only, their count) to read those through
-        dllm_step_compact instead of the full logits array."""
+        the compact layout instead of the full logits array.  With the fused
+        commit the step, block commit and compaction are one launch
+        (dllm_step_commit); otherwise the step, then dllm_advance_compact."""
         lib = self.lib
         pa, sa, aa, ca = self.args[slot]
         self.admit_host()
         rc = lib.dllm_pack(ctypes.byref(pa), stream)
         if ev_before is not None:
             ev_before.record()
-        rc |= self.launch_step(slot, stream, compact)
+        if self.fused:
+            rc |= self.launch_step_commit(slot, stream, compact)
+        else:
+            rc |= self.launch_step(slot, stream, compact)
         if ev_after is not None:
             ev_after.record()
-        rc |= lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream)
+        if not self.fused:
+            rc |= lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream)
         if rc:
             raise RuntimeError("a dllm call failed inside the timed loop")
+
+    def launch_step_commit(self, slot, stream, compact=None):
+        """The step with its block commit and compaction (dllm_step_commit)
+        on state slot ``slot``; returns the status code."""
+        pa, sa, aa, ca = self.args[slot]
+        quota = self.quota_ptr if self.quota is not None else None
+        if compact is None:
+            return self.lib.dllm_step_commit(ctypes.byref(sa), quota, -1, ctypes.byref(aa), ctypes.byref(ca), stream)
+        buf, rows = compact
+        saved = sa.logits
+        sa.logits = ctypes.c_void_p(buf.data_ptr())
+        rc = self.lib.dllm_step_commit(ctypes.byref(sa), quota, rows, ctypes.byref(aa), ctypes.byref(ca), stream)
+        sa.logits = saved
+        return rc
 
     def launch_step(self, slot, stream, compact=None):
         """The step of one pipeline step on state slot ``slot`` (dllm_step,
@@ -429,14 +450,25 @@ class Pipeline:
         self.state.copy_(self.pristine)
 
     def launches_per_step(self):
-        """Kernels one ``run`` launches: pack; the step (or one launch per
-        vocabulary shard plus the merge); advance + compaction, one fused
-        launch while the state rows fit its staging buffer, else advance,
-        scatter and copy-back."""
+        """Kernels one ``run`` launches: pack, then either the step with the
+        fused commit (one launch), or the step (one launch per vocabulary
+        shard plus the merge) and advance + compaction (one launch while the
+        state rows fit its staging buffer, else advance, scatter and
+        copy-back)."""
+        if getattr(self, "fused", False):
+            return 2
         step = len(self.shards) + 1 if self.shards is not None else 1
         row_total = sum(self.rb_arr[k] for k in range(7))
         commit = 1 if self.B * row_total <= FUSED_STAGE_BYTES else 3
         return 1 + step + commit
+
+    def commit_bytes_bound(self):
+        """Bytes the fused commit moves at most (every row committed and
+        moved): block tokens into the committed tokens, the row's b / K /
+        rid read, b and evict written, the compaction maps, and each row of
+        the compacted arrays read and written once."""
+        row_total = sum(self.rb_arr[k] for k in range(7))
+        return self.B * (4 * self.L + 12 + 5 + 8 + 2 * row_total)
 
 
 FUSED_STAGE_BYTES = 96 * 1024   # state rows dllm_advance_compact stages in one CTA (one launch)
@@ -446,10 +478,11 @@ E2E_ROUNDS = 3              # timed rounds of the end-to-end leg (the median is 
 REFERENCE_RUN_S = 90.0      # the reference arm's whole run (warm-up and timed steps), about
 
 
-def time_step_kernel(pipe, stream, n=KERNEL_TIMING_LAUNCHES):
-    """Launch duration of the step alone (the roofline's kernel), measured
-    two ways on fresh state slots (the ring is restored first, outside
-    every event):
+def time_step_kernel(pipe, stream, launch, n=KERNEL_TIMING_LAUNCHES):
+    """Launch duration of the step kernel as ``launch(slot, stream)`` issues
+    it (the pipeline's step, with or without its fused commit), measured two
+    ways on fresh state slots (the ring is restored first, outside every
+    event):
 
     * per launch: ``n`` step launches, each between its own pair of CUDA
       events on the launching stream, after one untimed launch (so the first
@@ -465,10 +498,10 @@ def time_step_kernel(pipe, stream, n=KERNEL_TIMING_LAUNCHES):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     pipe.restore()
     torch.cuda.synchronize()
-    rc = pipe.launch_step(0, stream)
+    rc = launch(0, stream)
     for k in range(n):
         ev[k][0].record()
-        rc |= pipe.launch_step(k + 1, stream)
+        rc |= launch(k + 1, stream)
         ev[k][1].record()
     torch.cuda.synchronize()
     per_launch = [a.elapsed_time(b) for a, b in ev]
@@ -476,10 +509,10 @@ def time_step_kernel(pipe, stream, n=KERNEL_TIMING_LAUNCHES):
     b0 = torch.cuda.Event(enable_timing=True)
     b1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    rc |= pipe.launch_step(0, stream)
+    rc |= launch(0, stream)
     b0.record()
     for k in range(n):
-        rc |= pipe.launch_step(k + 1, stream)
+        rc |= launch(k + 1, stream)
     b1.record()
     torch.cuda.synchronize()
     if rc:
@@ -537,9 +570,11 @@ def run_gpu(args, rank, world, local_rank, dist):
     torch.cuda.synchronize()
     if dist is not None and dist.is_initialized():
         dist.barrier()
-    # the step kernel alone, for the roofline (outside the timed pipeline
-    # region, so that its events do not slow the pipeline down)
-    kernel = time_step_kernel(pipe, sh)
+    # the step kernel as the pipeline launches it, for the roofline, and the
+    # step without the commit beside it (outside the timed pipeline region,
+    # so that their events do not slow the pipeline down)
+    kernel = time_step_kernel(pipe, sh, pipe.launch_step_commit if pipe.fused else pipe.launch_step)
+    step_only = time_step_kernel(pipe, sh, pipe.launch_step) if pipe.fused else None
     clocks = sampler.stop()
     err = dllm.get_device_error(device)
     if err:
@@ -547,10 +582,28 @@ def run_gpu(args, rank, world, local_rank, dist):
     total_ms = t0.elapsed_time(t1)
     units, seconds = aggregate(pipe.M * K, total_ms / 1e3, dist)
     res = {
-        "pipe": pipe, "units": units, "seconds": seconds, "total_ms": total_ms, "kernel": kernel,
+        "pipe": pipe, "units": units, "seconds": seconds, "total_ms": total_ms, "kernel": kernel, "step_only": step_only,
         "clocks": clocks, "cfg": cfg, "inp": inp, "device": device,
     }
     return res
+
+
+def measure_h2d_gbs(dst, src, reps=5):
+    """Plain host-to-device bandwidth of this box's link: ``src`` (pinned
+    host) copied into ``dst`` with one cudaMemcpyAsync, timed with CUDA
+    events on the current stream; the median of ``reps`` copies, in GB/s."""
+    torch = __import__("torch")
+    stream = torch.cuda.current_stream(dst.device)
+    vals = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        vals.append(src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return statistics.median(vals)
 
 
 def run_e2e(pipe, steps, rounds=E2E_ROUNDS):
@@ -558,44 +611,72 @@ def run_e2e(pipe, steps, rounds=E2E_ROUNDS):
     copies its inputs host->device (the masked positions' logits rows, which
     are all the step reads, through dllm_step_compact; the batch state) and
     reads its results back (the slot's output block and the updated
-    input_ids | conf_state).  ``rounds`` rounds of ``steps`` steps are timed;
-    the value is the median round (a host stall of tens of ms in one round
-    moves the mean of a 10-step round by half)."""
+    input_ids | conf_state).  The uploads are double-buffered: step k + 1's
+    inputs cross the link on a copy stream while step k runs and its results
+    come back (two logits buffers, two state slots, events between the
+    streams).  ``rounds`` rounds of ``steps`` steps are timed; the value is
+    the median round (a host stall of tens of ms in one round moves the mean
+    of a 10-step round by half).  The link's own bandwidth (a plain pinned
+    copy of the same logits bytes) and the rate it allows are reported
+    beside it."""
     torch = pipe.torch
     dev = pipe.device
     rows_d = torch.from_numpy(pipe.masked_rows).to(dev)
-    compact_d = pipe.logits[rows_d].contiguous()
-    logits_h = torch.empty(compact_d.shape, dtype=compact_d.dtype, pin_memory=True)
-    logits_h.copy_(compact_d)
+    bufs = [pipe.logits[rows_d].contiguous()]
+    bufs.append(torch.empty_like(bufs[0]))
+    logits_h = torch.empty(bufs[0].shape, dtype=bufs[0].dtype, pin_memory=True)
+    logits_h.copy_(bufs[0])
     state_h = torch.from_numpy(pipe.slot_host.copy()).pin_memory()
     n_state = pipe.words["ids"] + pipe.words["cs"]   # adjacent in the slot: ids | cs
     assert pipe.off["cs"] == pipe.off["ids"] + pipe.words["ids"]
-    state_out = pipe.state[0, pipe.off["ids"]:pipe.off["ids"] + n_state]
     out_h = torch.empty(pipe.out_bytes, dtype=torch.uint8, pin_memory=True)
     state_out_h = torch.empty(n_state, dtype=torch.int32, pin_memory=True)
     stream = torch.cuda.current_stream(dev)
+    copy_stream = torch.cuda.Stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
+    rows = bufs[0].shape[0]
+    up_done = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [torch.cuda.Event(), torch.cuda.Event()]   # the last step on slot i no longer reads its inputs
 
-    def one():
-        compact_d.copy_(logits_h, non_blocking=True)
-        pipe.state[0].copy_(state_h, non_blocking=True)
-        pipe.run(0, sh, compact=(compact_d, compact_d.shape[0]))
-        out_h.copy_(pipe.out[0], non_blocking=True)
-        state_out_h.copy_(state_out, non_blocking=True)
-        stream.synchronize()
+    def upload(i):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(used[i])
+            bufs[i].copy_(logits_h, non_blocking=True)
+            pipe.state[i].copy_(state_h, non_blocking=True)
+            up_done[i].record(copy_stream)
 
-    one()
+    def run_round(n):
+        for i in (0, 1):
+            used[i].record(stream)
+        upload(0)
+        for k in range(n):
+            i = k % 2
+            stream.wait_event(up_done[i])
+            pipe.run(i, sh, compact=(bufs[i], rows))
+            used[i].record(stream)
+            if k + 1 < n:
+                upload((k + 1) % 2)            # crosses the link while step k runs
+            out_h.copy_(pipe.out[i], non_blocking=True)
+            state_out_h.copy_(pipe.state[i, pipe.off["ids"]:pipe.off["ids"] + n_state], non_blocking=True)
+            stream.synchronize()
+
+    run_round(2)
     torch.cuda.synchronize()
     vals = []
     for _ in range(rounds):
         t = time.perf_counter()
-        for _ in range(steps):
-            one()
+        run_round(steps)
         vals.append(pipe.M * steps / (time.perf_counter() - t))
-    h2d = compact_d.numel() * 2 + pipe.slot_words * 4
+    torch.cuda.synchronize()
+    h2d = bufs[0].numel() * 2 + pipe.slot_words * 4
     d2h = pipe.out_bytes + n_state * 4
-    return {"value": statistics.median(vals), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "rounds": [round(v, 1) for v in vals], "statistic": "median round"}
+    link = measure_h2d_gbs(bufs[1], logits_h)
+    bound = pipe.M / (h2d / (link * 1e9))
+    value = statistics.median(vals)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "rounds": [round(v, 1) for v in vals], "statistic": "median round",
+            "uploads": "double-buffered on a copy stream",
+            "link_h2d_gbs": link, "link_bound_value": bound, "frac_of_link_bound": value / bound}
 
 
 # ---------------------------------------------------------------------------
@@ -912,12 +993,12 @@ def main():
     res = run_gpu(args, rank, world, local_rank, dist)
     pipe, cfg = res["pipe"], res["cfg"]
     K = args.steps
-    kern = res["kernel"]
+    kern, step_only = res["kernel"], res["step_only"]
     step_ms = kern["mean_ms"]
-    alg = algorithmic_bytes(cfg, pipe.M)
+    alg = algorithmic_bytes(cfg, pipe.M) + (pipe.commit_bytes_bound() if pipe.fused else 0)
     achieved = alg / (step_ms / 1e3) / 1e9
     peak, peak_src = load_peaks()
-    # the committed capture is of the Dream-shaped dllm_step launch only
+    # the committed capture is of the Dream-shaped step launch only
     traffic = load_traffic(step_source_sha()) if args.workload == "dream" else None
     value = res["units"] / res["seconds"]
     e2e = run_e2e(pipe, args.e2e_steps)
@@ -933,8 +1014,9 @@ def main():
             "ms_per_step": res["seconds"] * 1e3 / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16", "data": "synthetic",
             "config": workload_config(args.workload, cfg, res["inp"], pipe.W, pipe.cost, fixed),
-            "timing": {"step": (f"admit (host) + pack + step + advance/compact: "
-                                f"{pipe.launches_per_step()} kernel launches"),
+            "timing": {"step": (f"admit (host) + pack + step + block commit + compaction: "
+                                f"{pipe.launches_per_step()} kernel launches"
+                                + (" (the commit and compaction inside the step's launch)" if pipe.fused else "")),
                        "l2": "inputs larger than L2: 0.62 GB of masked logits rows per step, no flush",
                        "state_ring": RING,
                        "roofline": (f"{kern['n']} step launches after the timed region, each between "
@@ -946,14 +1028,21 @@ def main():
             "step_kernel_ms_max": kern["max_ms"],
             "step_kernel_samples": kern["n"],
             "step_kernel_back_to_back_ms": kern["back_to_back_mean_ms"],
+            "step_only_kernel_ms": None if step_only is None else step_only["mean_ms"],
+            "step_only_kernel_back_to_back_ms": None if step_only is None else step_only["back_to_back_mean_ms"],
+            "step_only_frac": (None if step_only is None else
+                               algorithmic_bytes(cfg, pipe.M) / (step_only["mean_ms"] / 1e3) / 1e9 / peak),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,
                          "all_rows_logits_bytes_per_launch": cfg.B * cfg.L * cfg.V * 2,
-                         "kernel": ("step_kernel (dllm_step_quota)" if fixed else
-                                    "4 x step_kernel (dllm_step_shard) + merge_kernel" if pipe.shards else
-                                    "step_kernel (dllm_step)"),
-                         "algorithmic_bytes_per_launch": alg},
+                         "kernel": ("4 x step_kernel (dllm_step_shard) + merge_kernel" if pipe.shards else
+                                    "step_kernel with the fused commit (dllm_step_commit" +
+                                    (", fixed-steps quota)" if fixed else ")")),
+                         "algorithmic_bytes_per_launch": alg,
+                         "algorithmic_bytes_note": ("masked logits rows + per-position state + per-request I/O"
+                                                    + (" + the commit at its bound (every row committed and moved)"
+                                                       if pipe.fused else ""))},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": pipe.launches_per_step() * K,

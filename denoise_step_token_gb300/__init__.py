@@ -136,6 +136,8 @@ _SIGNATURES = {
     "dllm_loop_info": (ctypes.c_int, [_p, ctypes.POINTER(LoopInfo)]),
     "dllm_loop_rows": (ctypes.c_int, [_p, _p, _p, _p]),
     "dllm_advance_compact": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), ctypes.POINTER(CompactArgs), _p]),
+    "dllm_step_commit": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p, ctypes.c_int64, ctypes.POINTER(AdvanceArgs),
+                                        ctypes.POINTER(CompactArgs), _p]),
     "dllm_advance": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), _p]),
     "dllm_compact_workspace_size": (_sz, [_i32, _i32, _p]),
     "dllm_compact": (ctypes.c_int, [ctypes.POINTER(CompactArgs), _p]),

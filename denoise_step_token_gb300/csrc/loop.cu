@@ -10,11 +10,11 @@
 //     (dllm_pack, or dllm_pack_block when the last step committed nothing);
 //   dllm_loop_end: the step over the caller's logits and the done-flag
 //     readback (the one host round trip), then the host mirrors.  In FDFO
-//     mode the block commit and compaction (one launch) follow the step on
-//     the stream before the readback: they read the done flags on the
-//     device and leave the batch as it is when no block finished.  In sync
-//     mode the host decides after the readback (a commit needs every block
-//     done).
+//     mode the block commit and compaction run in the step's own launch
+//     (dllm_step_commit), before the readback: they use the done flags on
+//     the device and leave the batch as it is when no block finished.  In
+//     sync mode the host decides after the readback (a commit needs every
+//     block done) and launches the commit.
 // The host keeps only what admission needs (prompt lengths, block indices,
 // steps in the current block) and a small pinned staging block for the
 // per-iteration copies; every array the kernels read lives in the caller's
@@ -102,17 +102,15 @@ int staging_used(dllm_loop* lp, cudaStream_t s) {
     return DLLM_OK;
 }
 
-// Block commit and compaction of the A active rows in one launch: rows whose
-// device done flag is set advance (a fresh block, or eviction after their
-// last block); the survivors are compacted in order.
-int launch_commit(dllm_loop* lp, int32_t A, void* stream) {
+// Arguments of the block commit and compaction of the A active rows: rows
+// whose device done flag is set advance (a fresh block, or eviction after
+// their last block); the survivors are compacted in order.
+void commit_args(dllm_loop* lp, int32_t A, dllm_advance_args& aa, dllm_compact_args& ca) {
     const dllm_loop_config& c = lp->c;
-    dllm_advance_args aa;
     memset(&aa, 0, sizeof(aa));
     aa.A = A; aa.L = c.L; aa.mask_id = c.mask_id; aa.advance = lp->done; aa.rid = lp->rid; aa.K = lp->K; aa.b = lp->b;
     aa.input_ids = lp->ids; aa.conf_state = lp->cs; aa.gen_tokens = lp->gen; aa.ld_gen = (int64_t)lp->Kmax * c.L;
     aa.evict = lp->evict;
-    dllm_compact_args ca;
     memset(&ca, 0, sizeof(ca));
     ca.A = A; ca.n_arrays = 7; ca.evict = lp->evict; ca.new_index = lp->new_index; ca.src_row = lp->src_row;
     ca.A_out = lp->A_out;
@@ -125,6 +123,13 @@ int launch_commit(dllm_loop* lp, int32_t A, void* stream) {
     }
     ca.workspace = lp->compact_ws;
     ca.workspace_bytes = lp->compact_ws_bytes;
+}
+
+// The commit and compaction as their own launch (sync mode).
+int launch_commit(dllm_loop* lp, int32_t A, void* stream) {
+    dllm_advance_args aa;
+    dllm_compact_args ca;
+    commit_args(lp, A, aa, ca);
     return dllm_advance_compact(&aa, &ca, stream);
 }
 
@@ -350,6 +355,7 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
     sa.input_ids = lp->ids; sa.thr = lp->thr; sa.conf_state = lp->cs; sa.done = lp->done; sa.accept_len = lp->accept;
     sa.n_new = lp->n_new; sa.feats = lp->feats; sa.workspace = lp->step_ws; sa.workspace_bytes = lp->step_ws_bytes;
     int rc;
+    const int32_t* quota = nullptr;
     if (c.S > 0) {
         rc = staging_free(lp);
         if (rc != DLLM_OK) return rc;
@@ -357,19 +363,21 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
         DLLM_CUDA_TRY(cudaMemcpyAsync(lp->quota, lp->quota_h, (size_t)A * 4, cudaMemcpyHostToDevice, s));
         rc = staging_used(lp, s);
         if (rc != DLLM_OK) return rc;
-        rc = dllm_step_quota(&sa, lp->quota, stream);
-    } else {
-        rc = dllm_step(&sa, stream);
+        quota = lp->quota;
     }
-    if (rc != DLLM_OK) return rc;
-    // FDFO: every done row advances, so the commit and compaction can
-    // follow the step at once (the advance flags are the device's done
-    // flags; with none set they leave the batch unchanged)
+    // FDFO: every done row advances, so the commit and compaction run in
+    // the step's own launch (the advance flags are the device's done flags;
+    // with none set they leave the batch unchanged)
     const bool fdfo = c.mode == 0;
     if (fdfo) {
-        rc = launch_commit(lp, A, stream);
-        if (rc != DLLM_OK) return rc;
+        dllm_advance_args aa;
+        dllm_compact_args ca;
+        commit_args(lp, A, aa, ca);
+        rc = dllm_step_commit(&sa, quota, -1, &aa, &ca, stream);
+    } else {
+        rc = quota ? dllm_step_quota(&sa, quota, stream) : dllm_step(&sa, stream);
     }
+    if (rc != DLLM_OK) return rc;
     // the per-step readback: one byte per row
     DLLM_CUDA_TRY(cudaMemcpyAsync(lp->done_h, lp->done, (size_t)A, cudaMemcpyDeviceToHost, s));
     DLLM_CUDA_TRY(cudaStreamSynchronize(s));

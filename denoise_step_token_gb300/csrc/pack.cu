@@ -23,6 +23,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "compact.cuh"
 
 namespace dllm {
 namespace {
@@ -465,30 +466,18 @@ extern "C" int dllm_advance(const dllm_advance_args* a, void* stream) {
 
 // ---------------------------------------------------------------------------
 // dllm_advance_compact: dllm_advance then dllm_compact by its evict flags, in
-// one launch of one CTA.  Rows are compacted in place, in chunks of rows in
-// increasing order: a chunk's surviving rows are first staged in shared
-// memory, then written to their new rows.  A destination is never above its
-// source, so it lies in a chunk already staged (this one or an earlier one)
-// and nothing is overwritten before it is read.
+// one launch of one CTA (the compaction itself: compact.cuh).
 // ---------------------------------------------------------------------------
 namespace dllm {
 namespace {
 
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedStageBytes = 96 * 1024;
-constexpr int kFusedBatch = 8;   // global loads in flight per thread
-constexpr int kFusedMapWords = 2048;   // elements per staged row the element map covers
+constexpr int kFusedBatch = kCompactBatch;   // global loads in flight per thread
 
 struct FusedParams {
     AdvanceParams adv;
-    int n_arrays, chunk_rows, word;   // word: 4-byte elements (else bytes)
-    unsigned char* arrays[DLLM_COMPACT_MAX_ARRAYS];
-    long long row_bytes[DLLM_COMPACT_MAX_ARRAYS];
-    long long stage_off[DLLM_COMPACT_MAX_ARRAYS];   // per-row offset of each array in a staged row
-    long long row_total;                            // staged bytes per row
-    int* new_index;
-    int* src_row;
-    int* A_out;
+    CompactPlan cp;
 };
 
 // The block commit of dllm_advance for all rows, by one CTA, 1024 rows at a
@@ -550,121 +539,19 @@ __device__ __forceinline__ void advance_rows(const AdvanceParams& P, long long* 
     }
 }
 
-template <typename E>
-__device__ __forceinline__ void move_chunk(const FusedParams& P, unsigned char* stage, const int* s_src,
-                                           const int* s_dst, const short* s_arr, const int* s_off, int kept,
-                                           int tid) {
-    // Staged row k (all arrays side by side) at stage + k * row_total.  The
-    // chunk's elements over every array form one flat range (32-bit
-    // indices: the stage holds at most 96 KiB); s_arr / s_off map an
-    // element's place in a staged row to its array (-1: padding) and its
-    // byte offset in that array's row.  kFusedBatch loads per thread are in
-    // flight before their stores.
-    const int per_row = (int)(P.row_total / (long long)sizeof(E));
-    const int total = per_row * kept;
-    for (int t0 = tid; t0 < total; t0 += kFusedBatch * kFusedThreads) {
-        E v[kFusedBatch];
-#pragma unroll
-        for (int u = 0; u < kFusedBatch; ++u) {
-            const int t = t0 + u * kFusedThreads;
-            v[u] = E(0);
-            if (t < total) {
-                const int k = t / per_row;
-                const int w = t - k * per_row;
-                const int a = s_arr[w];
-                if (a >= 0) v[u] = *reinterpret_cast<const E*>(P.arrays[a] + (long long)s_src[k] * P.row_bytes[a] + s_off[w]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kFusedBatch; ++u) {
-            const int t = t0 + u * kFusedThreads;
-            if (t < total) reinterpret_cast<E*>(stage)[t] = v[u];
-        }
-    }
-    __syncthreads();
-    for (int t = tid; t < total; t += kFusedThreads) {
-        const int k = t / per_row;
-        const int w = t - k * per_row;
-        const int a = s_arr[w];
-        if (a >= 0)
-            *reinterpret_cast<E*>(P.arrays[a] + (long long)s_dst[k] * P.row_bytes[a] + s_off[w]) =
-                reinterpret_cast<const E*>(stage)[t];
-    }
-}
-
 __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __grid_constant__ FusedParams P) {
     extern __shared__ __align__(16) unsigned char stage[];
-    __shared__ int s_wsum[kFusedThreads / 32];
-    __shared__ int s_src[kFusedThreads], s_dst[kFusedThreads];
+    __shared__ CompactScratch<kFusedThreads> s_cp;
     __shared__ long long s_gen_dst[kFusedThreads];
     __shared__ uint8_t s_ev[kFusedThreads];
-    __shared__ short s_arr[kFusedMapWords];
-    __shared__ int s_off[kFusedMapWords];
-    __shared__ int s_skip;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int A = P.adv.A;
-    // element map of a staged row: array index (-1 in padding) and offset
-    // (launch parameters only: built before waiting on the previous kernel)
-    {
-        const int es = P.word ? 4 : 1;
-        const int per_row = (int)(P.row_total / es);
-        for (int w = tid; w < per_row; w += kFusedThreads) {
-            const long long off = (long long)w * es;
-            int arr = -1, o = 0;
-            for (int a = P.n_arrays - 1; a >= 0; --a) {
-                if (off >= P.stage_off[a]) {
-                    if (off - P.stage_off[a] < P.row_bytes[a]) {
-                        arr = a;
-                        o = (int)(off - P.stage_off[a]);
-                    }
-                    break;
-                }
-            }
-            s_arr[w] = (short)arr;
-            s_off[w] = o;
-        }
-    }
+    const int tid = threadIdx.x;
+    // the element map depends on launch parameters only: built before
+    // waiting on the previous kernel
+    compact_map<kFusedThreads>(P.cp, s_cp, tid);
     pdl_wait();
     pdl_release();
     advance_rows(P.adv, s_gen_dst, s_ev, tid);   // ends with a barrier: evict, ids, cs, b visible CTA-wide
-    int base = 0;      // survivors before the chunk
-    for (int c0 = 0; c0 < A; c0 += P.chunk_rows) {
-        const int i = c0 + tid;
-        const bool in = tid < P.chunk_rows && i < A;
-        const bool keep = in && P.adv.evict[i] == 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, keep);
-        if (lane == 0) s_wsum[warp] = __popc(bal);
-        if (tid == 0) s_skip = 0x7fffffff;
-        __syncthreads();
-        int before = 0, kept = 0;
-        for (int w = 0; w < kFusedThreads / 32; ++w) {
-            const int c = s_wsum[w];
-            if (w < warp) before += c;
-            kept += c;
-        }
-        const int rank = before + __popc(bal & ((1u << lane) - 1u));
-        // survivors ahead of the first evicted row keep their index: they
-        // are a prefix of the chunk's survivors and need no move
-        const bool moves = keep && base + rank != i;
-        const unsigned mv = __ballot_sync(0xffffffffu, moves);
-        if (mv && lane == __ffs(mv) - 1) atomicMin(&s_skip, rank);
-        if (in) {
-            const int ni = keep ? base + rank : -1;
-            if (P.new_index) P.new_index[i] = ni;
-            if (keep) {
-                if (P.src_row) P.src_row[ni] = i;
-                s_src[rank] = i;
-                s_dst[rank] = ni;
-            }
-        }
-        __syncthreads();
-        const int skip = min(s_skip, kept);
-        if (P.word) move_chunk<uint32_t>(P, stage, s_src + skip, s_dst + skip, s_arr, s_off, kept - skip, tid);
-        else move_chunk<uint8_t>(P, stage, s_src + skip, s_dst + skip, s_arr, s_off, kept - skip, tid);
-        __syncthreads();
-        base += kept;
-    }
-    if (tid == 0) *P.A_out = base;
+    compact_rows<kFusedThreads>(P.cp, s_cp, stage, P.adv.evict, P.adv.A, tid);
 }
 
 }  // namespace
@@ -672,7 +559,6 @@ __global__ void __launch_bounds__(kFusedThreads) advance_compact_kernel(const __
 
 extern "C" int dllm_advance_compact(const dllm_advance_args* a, const dllm_compact_args* c, void* stream) {
     if (!a || !c || a->A < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->ld_gen < 0 || c->A != a->A) return DLLM_ERR_INVAL;
-    if (c->n_arrays < 0 || c->n_arrays > DLLM_COMPACT_MAX_ARRAYS || !c->A_out) return DLLM_ERR_INVAL;
     if (a->A > 0 && (!a->advance || !a->rid || !a->K || !a->b || !a->input_ids || !a->conf_state ||
                      !a->gen_tokens || !a->evict))
         return DLLM_ERR_INVAL;
@@ -682,28 +568,11 @@ extern "C" int dllm_advance_compact(const dllm_advance_args* a, const dllm_compa
     P.adv.cs = a->conf_state; P.adv.gen = a->gen_tokens; P.adv.ld_gen = a->ld_gen; P.adv.evict = a->evict;
     P.adv.err = error_word_ptr();
     if (!P.adv.err) return DLLM_ERR_CUDA;
-    P.n_arrays = c->n_arrays;
-    P.row_total = 0;
-    bool word = true;
-    for (int k = 0; k < c->n_arrays; ++k) {
-        if ((a->A > 0 && !c->arrays[k]) || c->row_bytes[k] <= 0) return DLLM_ERR_INVAL;
-        P.arrays[k] = static_cast<unsigned char*>(c->arrays[k]);
-        P.row_bytes[k] = c->row_bytes[k];
-        word = word && (c->row_bytes[k] % 4 == 0) && (reinterpret_cast<uintptr_t>(c->arrays[k]) % 4 == 0);
-    }
-    for (int k = 0; k < c->n_arrays; ++k) {
-        P.stage_off[k] = P.row_total;
-        P.row_total += (c->row_bytes[k] + 3) & ~3ll;   // 4-byte aligned slots
-    }
-    if (P.row_total > kFusedStageBytes) return DLLM_ERR_UNSUPPORTED;
-    P.word = word ? 1 : 0;
-    if (P.row_total / (word ? 4 : 1) > kFusedMapWords) return DLLM_ERR_UNSUPPORTED;
-    P.chunk_rows = P.row_total > 0 ? (int)std::min<long long>(kFusedThreads, kFusedStageBytes / P.row_total)
-                                   : kFusedThreads;
-    P.new_index = c->new_index; P.src_row = c->src_row; P.A_out = c->A_out;
+    const int prc = make_compact_plan(c, kFusedThreads, kFusedStageBytes, &P.cp);
+    if (prc != DLLM_OK) return prc;
     // rows beyond one staging chunk: one CTA would serialise them; with a
     // compaction workspace, run the multi-CTA advance and compaction instead
-    if ((long long)a->A * P.row_total > kFusedStageBytes && c->workspace &&
+    if ((long long)a->A * P.cp.row_total > kFusedStageBytes && c->workspace &&
         c->workspace_bytes >= dllm_compact_workspace_size(c->A, c->n_arrays, c->row_bytes)) {
         const int rc = dllm_advance(a, stream);
         if (rc != DLLM_OK) return rc;

@@ -46,6 +46,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "compact.cuh"
 
 namespace dllm {
 namespace {
@@ -181,7 +182,25 @@ struct StepParams {
     int* row_tok;
     uint8_t* sel;
     int* err;
+    // fused commit (dllm_step_commit); commit == 0 otherwise
+    int commit;
+    const int* c_rid;   // [B] request id of each row
+    const int* c_K;     // [B] blocks of each request
+    int* c_b;           // [B] current block index (in/out)
+    int* c_gen;         // committed tokens, row rid at c_gen + rid * c_ld_gen
+    long long c_ld_gen;
+    uint8_t* c_evict;   // [B] out: the row leaves the batch
+    CompactPlan cp;     // stable compaction of the caller's row arrays by c_evict
 };
+
+// A deferred commit's list entry: the request, and whether its block is
+// reset for the next one (fused commit) rather than given its new tokens.
+constexpr int kDeferReset = 0x40000000;
+
+// The fused commit's compaction scratch and staging, in the copy rings.
+constexpr int kCommitScratchBytes = (int)((sizeof(CompactScratch<kThreads>) + 127) & ~size_t(127));
+constexpr long long kCommitStageBytes = (long long)kStreamWarps * kStages * kCopyBytes - kCommitScratchBytes;
+static_assert(kCommitStageBytes >= 16384, "the copy rings hold the commit's scratch and a useful stage");
 
 // Workspace layout.  The first quarter holds everything that must be zero
 // between calls (control words, counters, chunk partials); per-call data
@@ -507,9 +526,16 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
         cs_old[k] = valid ? P.cs[base + j] : 0.f;
         rw[k] = (valid && has_masked) ? ld_relaxed_gpu_u64(P.row_word + base + j) : 0ull;
     }
+    // the row's commit state (fused commit): issued with the block's loads
+    int c_blk = 0, c_K = 0, c_r = 0;
+    if (P.commit) {
+        c_blk = P.c_b[b];
+        c_K = P.c_K[b];
+        c_r = P.c_rid[b];
+    }
     // the scan count guards only the commit at the end: loaded after the
     // block's loads so that its acquire does not hold them back
-    const int scanned = (lane == 0 && has_masked && !direct) ? ld_acquire_gpu(P.ctl) : 0;
+    const int scanned = (lane == 0 && (has_masked || P.commit) && !direct) ? ld_acquire_gpu(P.ctl) : 0;
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
@@ -612,21 +638,60 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
     }
     if (P.feats) warp_features<NK>(val, inU, L, lane, P.feats + (long long)b * DLLM_NUM_FEATURES);
 
+    // Fused commit (dllm_step_commit): a finished block joins the request's
+    // committed tokens and the request moves to its next block, which
+    // starts fully masked, or leaves the batch after its last one (FDFO
+    // page, section "FDFO 的核心思想": a finished request commits at once;
+    // BlockServe page, Algorithm 1: b_i <- b_i + 1, evict when b_i >= K_i).
+    // Exactly dllm_advance with the step's done flags as its advance flags.
+    bool reset = false;
+    if (P.commit) {
+        bool ev = false;
+        if (done) {
+            if (c_blk < 0 || c_blk >= c_K || (long long)(c_blk + 1) * L > P.c_ld_gen) {
+                if (lane == 0) set_error(P.err, DLLM_DEVERR_BLOCK_INDEX);
+            } else {
+                int* g = P.c_gen + (long long)c_r * P.c_ld_gen + (long long)c_blk * L;
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    const int j = lane + 32 * k;
+                    if (j < L) g[j] = id[k];
+                }
+                ev = c_blk + 1 >= c_K;
+                reset = !ev;
+                if (lane == 0) P.c_b[b] = c_blk + 1;
+            }
+        }
+        if (lane == 0) P.c_evict[b] = ev ? 1 : 0;
+        if (reset) {
+#pragma unroll
+            for (int k = 0; k < NK; ++k) {
+                const int j = lane + 32 * k;
+                if (j < L) P.cs[base + j] = __int_as_float(0x7fc00000);
+            }
+        }
+    }
+
     // S4 commit of input_ids: only once every CTA has finished its scan;
     // before that the request goes on the deferred list, which the grid's
     // last CTA commits (the add's high half counts the list's entries).
-    if (!has_masked) return;
+    if (!has_masked && !reset) return;
     __syncwarp();   // lane 0's acquire of the scan count orders the warp's writes
     if (direct || __shfl_sync(0xffffffffu, scanned, 0) == (int)gridDim.x) {
 #pragma unroll
         for (int k = 0; k < NK; ++k) {
-            if (selk[k]) P.ids[base + lane + 32 * k] = id[k];
+            const int j = lane + 32 * k;
+            if (reset) {
+                if (j < L) P.ids[base + j] = P.mask_id;
+            } else if (selk[k]) {
+                P.ids[base + j] = id[k];
+            }
         }
     } else if (lane == 0) {
         const int slot = (int)((unsigned)atomicAdd(P.ctl + 1, 1 << 16) >> 16);
-        P.cnt[P.BL + P.B + slot] = b;
+        P.cnt[P.BL + P.B + slot] = b | (reset ? kDeferReset : 0);
     }
-    if (lane == 0) P.cnt[P.BL + b] = 0;   // request counter back to rest
+    if (lane == 0 && has_masked) P.cnt[P.BL + b] = 0;   // request counter back to rest
 }
 
 // direct: input_ids may be written at once (no other CTA still scans them).
@@ -795,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     int* s_zero = s_queue + 2 * P.list_cap;   // this CTA's requests without masked rows
     uint16_t* s_gmask = reinterpret_cast<uint16_t*>(s_zero + P.zero_cap);   // masked bits, 16 positions each
     __shared__ int s_wsum[kWarpsTotal];
-    __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last, s_next;
+    __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last, s_next, s_ring_busy;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -803,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (tid < kStreamWarps * kStages) mbar_init(smem_addr(&bars[tid]), 1);
     if (tid == 0) {
         s_next = 0;
+        s_ring_busy = 0;
         s_nzero = 0;
         s_qtail = 0;
         s_qhead = 0;
@@ -1155,7 +1221,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             // let this warp's copies in flight land before shared memory goes away
             while (consumed < issued) {
                 const int slot = consumed % kStages;
-                if (!mbar_wait_bounded(bar0 + slot * 8, (consumed / kStages) & 1u, 100000000ull)) break;
+                if (!mbar_wait_bounded(bar0 + slot * 8, (consumed / kStages) & 1u, 100000000ull)) {
+                    if (lane == 0) atomicExch(&s_ring_busy, 1);   // the ring may still be written
+                    break;
+                }
                 ++consumed;
             }
         }
@@ -1188,10 +1257,27 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const int n_def = s_last - 1;
         const int* list = P.cnt + P.BL + P.B;
         for (int i = tid; i < n_def; i += kThreads) {   // finalized before every CTA had scanned
-            const int b = __ldcg(list + i);
+            const int e = __ldcg(list + i);
+            const int b = e & 0xffff;
+            const bool rst = (e & kDeferReset) != 0;
             for (int j = 0; j < P.L; ++j) {
                 const long long idx = (long long)b * P.L + j;
-                if (P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
+                if (rst) P.ids[idx] = P.mask_id;
+                else if (P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
+            }
+        }
+        if (P.commit) {
+            // every request is committed: compact the caller's row arrays by
+            // the eviction flags, staged through the (now idle) copy rings
+            __syncthreads();
+            if (s_ring_busy) {
+                if (tid == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
+            } else {
+                auto& scratch = *reinterpret_cast<CompactScratch<kThreads>*>(smem);
+                unsigned char* stage = smem + kCommitScratchBytes;
+                compact_map<kThreads>(P.cp, scratch, tid);
+                __syncthreads();
+                compact_rows<kThreads>(P.cp, scratch, stage, P.c_evict, P.B, tid);
             }
         }
         if (tid == 0) {
@@ -1307,6 +1393,12 @@ struct ShardOut {
     int* idx;
 };
 
+// The block commit and compaction fused into a step (dllm_step_commit).
+struct CommitSpec {
+    const dllm_advance_args* adv;
+    const dllm_compact_args* cmp;
+};
+
 // A checked step launch: grid, block, shared memory and parameters.
 struct StepLaunch {
     bool empty;   // B == 0: nothing to launch
@@ -1320,7 +1412,7 @@ struct StepLaunch {
 // logits_rows >= 0 the compact layout; shard non-null S2 alone over a
 // vocabulary shard.
 int prepare_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
-                 StepLaunch* out) {
+                 StepLaunch* out, const CommitSpec* commit = nullptr) {
     out->empty = true;
     if (!a) return DLLM_ERR_INVAL;
     if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
@@ -1377,6 +1469,19 @@ int prepare_step(const dllm_step_args* a, const int32_t* quota, long long logits
     unsigned char* ws = static_cast<unsigned char*>(a->workspace);
     unsigned char* data = ws + ((a->workspace_bytes - w.data_bytes) & ~size_t(255));
     StepParams& P = out->P;
+    memset(&P, 0, sizeof(P));
+    if (commit) {
+        const dllm_advance_args* v = commit->adv;
+        P.commit = 1;
+        P.c_rid = v->rid;
+        P.c_K = v->K;
+        P.c_b = v->b;
+        P.c_gen = v->gen_tokens;
+        P.c_ld_gen = v->ld_gen;
+        P.c_evict = v->evict;
+        const int prc = make_compact_plan(commit->cmp, kThreads, kCommitStageBytes, &P.cp);
+        if (prc != DLLM_OK) return prc;
+    }
     P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
     P.list_cap = list_cap; P.static_cap = static_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
     P.div_nc = make_fastdiv((uint32_t)NC);
@@ -1412,9 +1517,9 @@ int launch_prepared(const StepLaunch& sl, void* stream) {
 }
 
 int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
-                void* stream) {
+                void* stream, const CommitSpec* commit = nullptr) {
     StepLaunch sl;
-    const int rc = prepare_step(a, quota, logits_rows, shard, &sl);
+    const int rc = prepare_step(a, quota, logits_rows, shard, &sl, commit);
     if (rc != DLLM_OK) return rc;
     return launch_prepared(sl, stream);
 }
@@ -1432,6 +1537,18 @@ extern "C" int dllm_step_quota(const dllm_step_args* a, const int32_t* quota, vo
 extern "C" int dllm_step_compact(const dllm_step_args* a, int64_t logits_rows, const int32_t* quota, void* stream) {
     if (logits_rows < 0) return DLLM_ERR_INVAL;
     return launch_step(a, quota, logits_rows, nullptr, stream);
+}
+
+extern "C" int dllm_step_commit(const dllm_step_args* a, const int32_t* quota, int64_t logits_rows,
+                                const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream) {
+    if (!a || !adv || !cmp) return DLLM_ERR_INVAL;
+    if (adv->A != a->B || cmp->A != a->B || adv->L != a->L || adv->mask_id != a->mask_id) return DLLM_ERR_INVAL;
+    if (adv->input_ids != a->input_ids || adv->conf_state != a->conf_state) return DLLM_ERR_INVAL;
+    if (adv->advance && adv->advance != a->done) return DLLM_ERR_INVAL;   // the step's done flags advance
+    if (a->B > 0 && (!adv->rid || !adv->K || !adv->b || !adv->gen_tokens || !adv->evict || adv->ld_gen < 0))
+        return DLLM_ERR_INVAL;
+    const CommitSpec commit{adv, cmp};
+    return launch_step(a, quota, logits_rows < 0 ? -1 : logits_rows, nullptr, stream, &commit);
 }
 
 extern "C" int dllm_step_shard(const dllm_step_args* a, int32_t v0, float* m, float* s, int32_t* idx, void* stream) {

@@ -471,6 +471,36 @@ typedef struct dllm_compact_args {
  * bytes. */
 int dllm_advance_compact(const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream);
 
+/* One FDFO iteration's step and batch tail in one launch: dllm_step (or
+ * dllm_step_quota when quota is not NULL; with logits_rows >= 0 the logits
+ * hold the masked positions' rows only, as for dllm_step_compact, and a
+ * negative logits_rows means the full [B*L][ldv] array) followed by
+ * dllm_advance with the
+ * step's done flags as the advance flags and dllm_compact by the eviction
+ * flags it sets -- the same results as dllm_step then dllm_advance_compact
+ * (FDFO page, section "FDFO 的核心思想": a request whose block is done
+ * commits it at once and starts its next block or leaves; BlockServe page,
+ * Algorithm 1).  Each request's finaliser commits its own block as soon as
+ * the step has decided it; the grid's last CTA then compacts the listed
+ * row arrays, staged through the step's shared memory.
+ *   - step: as dllm_step.  adv: adv->A == step->B, adv->L == step->L,
+ *     adv->mask_id == step->mask_id, adv->input_ids == step->input_ids,
+ *     adv->conf_state == step->conf_state, adv->advance NULL or
+ *     step->done; rid, K, b, gen_tokens, ld_gen and evict as for
+ *     dllm_advance.  cmp: cmp->A == step->B; arrays, row_bytes, new_index,
+ *     src_row and A_out as for dllm_compact (cmp->evict and the workspace
+ *     are not read); the arrays may include b, input_ids and conf_state.
+ *   - DLLM_ERR_INVAL when the pairs above differ, and every error of
+ *     dllm_step, dllm_advance and dllm_compact; DLLM_ERR_UNSUPPORTED when
+ *     a row of all the arrays holds more than 2048 elements (as for
+ *     dllm_advance_compact).
+ *   - Any number of rows: the last CTA compacts them in chunks of at most
+ *     480 rows, staged through about 150 KiB of shared memory.  A block
+ *     index outside [0, K) sets DLLM_DEVERR_BLOCK_INDEX and that row is not
+ *     advanced. */
+int dllm_step_commit(const dllm_step_args* step, const int32_t* quota, int64_t logits_rows,
+                     const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream);
+
 /* Workspace bytes for dllm_compact over these arrays (0 if invalid). */
 size_t dllm_compact_workspace_size(int32_t A, int32_t n_arrays, const int64_t* row_bytes);
 

@@ -259,3 +259,24 @@ def test_injection_countdown_without_a_gpu():
     assert lib.dllm_last_cuda_error(None) not in (0, OOM)
     assert lib.dllm_workspace_init(ctypes.c_void_p(0x100000), 256, None) == -3
     assert lib.dllm_last_cuda_error(None) == OOM
+
+
+def test_step_commit_argument_checks():
+    """dllm_step_commit rejects an advance or compaction that is not the
+    step's own batch before any CUDA call."""
+    lib = dllm.load()
+    sa = dllm.StepArgs(B=4, L=8, V=64, mask_id=63, ldv=64, logits=0x10000, input_ids=0x20000, thr=0x30000,
+                       conf_state=0x40000, done=0x50000, accept_len=0x60000, n_new=0x70000, workspace=0x100000,
+                       workspace_bytes=1 << 20)
+    ok = dict(A=4, L=8, mask_id=63, advance=0x50000, rid=0x80000, K=0x90000, b=0xa0000, input_ids=0x20000,
+              conf_state=0x40000, gen_tokens=0xb0000, ld_gen=32, evict=0xc0000)
+    ca = dllm.CompactArgs(A=4, n_arrays=0, A_out=0xd0000)
+    for k, v in (("A", 5), ("L", 4), ("mask_id", 1), ("input_ids", 0x20004), ("conf_state", 0x40004),
+                 ("advance", 0x50004), ("rid", None), ("ld_gen", -1)):
+        bad = dict(ok)
+        bad[k] = v
+        aa = dllm.AdvanceArgs(**bad)
+        assert lib.dllm_step_commit(ctypes.byref(sa), None, -1, ctypes.byref(aa), ctypes.byref(ca), None) == -1, k
+    ca_bad = dllm.CompactArgs(A=3, n_arrays=0, A_out=0xd0000)
+    assert lib.dllm_step_commit(ctypes.byref(sa), None, -1, ctypes.byref(dllm.AdvanceArgs(**ok)), ctypes.byref(ca_bad),
+                                None) == -1

@@ -26,6 +26,9 @@ def test_launches_per_step(B, L, shards, expected):
     # pack + the step (or each shard and the merge) + commit/compaction (one
     # launch while the rows fit the fused kernel's staging, else three)
     assert bench.Pipeline.launches_per_step(pipe) == expected
+    # with the commit inside the step's launch: pack + one launch
+    pipe.fused = True
+    assert bench.Pipeline.launches_per_step(pipe) == 2
 
 
 def test_traffic_only_for_the_profiled_source(tmp_path):
@@ -65,3 +68,11 @@ def test_clock_summary():
     out = bench.ClockSampler.summarize(lines)
     assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
     assert bench.ClockSampler.summarize([]) is None
+
+
+def test_commit_bytes_bound():
+    import bench
+    pipe = types.SimpleNamespace(B=128, L=32, rb_arr=[32 * 4, 32 * 4, 4, 4, 4, 4, 4])
+    # block tokens 4L, b / K / rid read 12, b and evict written 5, maps 8,
+    # each compacted row (276 bytes) read and written
+    assert bench.Pipeline.commit_bytes_bound(pipe) == 128 * (4 * 32 + 12 + 5 + 8 + 2 * 276)

@@ -1,0 +1,160 @@
+"""dllm_step_commit: the step with the FDFO block commit and the stable
+compaction in the same launch.
+
+Against the oracle (step, then oracle.loop.advance with the done flags as
+the advance flags, then oracle.compact) and, element for element, against
+the two-launch path it replaces (dllm_step, then dllm_advance_compact with
+advance = done): every output, the eviction flags, the compaction maps, the
+compacted arrays, the block indices and the committed tokens.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import compare_step, device_logits, enforce_margins, oracle_step
+from oracle.loop import advance as oracle_advance
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "ragged": synth.StepConfig("ragged", 8, 32, 40001, 12.0, "fraction", synth.THRESHOLD_SET, ldv=40016),
+    "dream_like": synth.StepConfig("dream_like", 48, 32, 20000, 12.0, "fraction", synth.THRESHOLD_SET),
+    "l64": synth.StepConfig("l64", 16, 64, 33000, 12.0, "fraction", synth.THRESHOLD_SET),
+    "all_masked": synth.StepConfig("all_masked", 6, 32, 9000, 12.0, "all", synth.THRESHOLD_SET),
+    # more rows than one 480-row compaction chunk
+    "many_rows": synth.StepConfig("many_rows", 600, 8, 3000, 8.0, "fraction", synth.THRESHOLD_SET),
+}
+
+
+@pytest.fixture(scope="module")
+def device(dllm):
+    import torch
+    return torch.device("cuda", 0)
+
+
+def _batch(cfg, seed):
+    """Step inputs with margins plus the rows' commit state: request ids (a
+    permutation), blocks K in 1..4, current block b < K, and committed tokens
+    of the earlier blocks."""
+    inp = synth.make_step_state(cfg, seed)
+    enforce_margins(inp)
+    rng = np.random.default_rng(seed + 100)
+    B, L = cfg.B, cfg.L
+    K = rng.integers(1, 5, size=B).astype(np.int32)
+    b = np.array([rng.integers(0, k) for k in K], dtype=np.int32)
+    rid = rng.permutation(B).astype(np.int32)
+    ld_gen = 4 * L
+    gen = rng.integers(0, cfg.V - 2, size=(B, ld_gen)).astype(np.int32)
+    return inp, rid, K, b, gen, ld_gen
+
+
+def _expected(cfg, inp, rid, K, b, gen):
+    ref = oracle_step(inp)
+    L = cfg.L
+    ids = ref["input_ids"].copy()
+    cs = ref["conf_state"].copy()
+    bb = b.astype(np.int64).copy()
+    o_gen = {int(r): gen[int(r)][: b[i] * L].astype(np.int64) for i, r in enumerate(rid)}
+    evict = oracle_advance(ref["done"].astype(bool), rid, bb, K, ids, cs, o_gen, cfg.mask_id)
+    new_index, src_row, A_out = oracle.compact(evict)
+    return ref, dict(ids=ids, cs=cs, b=bb, gen=o_gen, evict=evict, new_index=new_index, src_row=src_row, A_out=A_out)
+
+
+def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused):
+    import torch
+    lib = dllm.load()
+    B, L = cfg.B, cfg.L
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(device)
+    logits = device_logits(inp, device)
+    ids, thr, cs = t(inp.input_ids), t(inp.thr), t(inp.conf_state)
+    d_rid, d_K, d_b, d_gen = t(rid), t(K), t(b), t(gen)
+    p_arr = t(np.arange(B, dtype=np.int32) * 7)         # a row array the batch carries along
+    out = {
+        "done": torch.empty(B, dtype=torch.uint8, device=device),
+        "accept_len": torch.empty(B, dtype=torch.int32, device=device),
+        "n_new": torch.empty(B, dtype=torch.int32, device=device),
+        "feats": torch.empty((B, 6), dtype=torch.float32, device=device),
+        "conf": torch.empty((B, L), dtype=torch.float32, device=device),
+        "lse": torch.empty((B, L), dtype=torch.float32, device=device),
+        "tok": torch.empty((B, L), dtype=torch.int32, device=device),
+    }
+    evict = torch.full((B,), 7, dtype=torch.uint8, device=device)
+    new_index = torch.full((B,), -9, dtype=torch.int32, device=device)
+    src_row = torch.full((B,), -9, dtype=torch.int32, device=device)
+    A_out = torch.full((1,), -9, dtype=torch.int32, device=device)
+    ws = torch.zeros(lib.dllm_step_workspace_size(B, L, cfg.V), dtype=torch.uint8, device=device)
+    ptr = lambda x: ctypes.c_void_p(x.data_ptr())
+    sa = dllm.StepArgs(B=B, L=L, V=cfg.V, mask_id=cfg.mask_id, ldv=logits.shape[1], logits=ptr(logits),
+                       input_ids=ptr(ids), thr=ptr(thr), conf_state=ptr(cs), done=ptr(out["done"]),
+                       accept_len=ptr(out["accept_len"]), n_new=ptr(out["n_new"]), feats=ptr(out["feats"]),
+                       conf_out=ptr(out["conf"]), lse_out=ptr(out["lse"]), tok_out=ptr(out["tok"]),
+                       workspace=ptr(ws), workspace_bytes=ws.numel())
+    aa = dllm.AdvanceArgs(A=B, L=L, mask_id=cfg.mask_id, advance=ptr(out["done"]), rid=ptr(d_rid), K=ptr(d_K),
+                          b=ptr(d_b), input_ids=ptr(ids), conf_state=ptr(cs), gen_tokens=ptr(d_gen), ld_gen=ld_gen,
+                          evict=ptr(evict))
+    arrays = [ids, cs, thr, d_b, d_K, d_rid, p_arr]
+    rb = [L * 4, L * 4, 4, 4, 4, 4, 4]
+    arr = (ctypes.c_void_p * dllm.COMPACT_MAX_ARRAYS)(*[x.data_ptr() for x in arrays])
+    rbs = (ctypes.c_int64 * dllm.COMPACT_MAX_ARRAYS)(*rb)
+    cws = torch.empty(lib.dllm_compact_workspace_size(B, len(rb), ctypes.cast(rbs, ctypes.c_void_p)),
+                      dtype=torch.uint8, device=device)
+    ca = dllm.CompactArgs(A=B, n_arrays=len(arrays), evict=ptr(evict), new_index=ptr(new_index),
+                          src_row=ptr(src_row), A_out=ptr(A_out), arrays=arr, row_bytes=rbs, workspace=ptr(cws),
+                          workspace_bytes=cws.numel())
+    stream = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if fused:
+        rc = lib.dllm_step_commit(ctypes.byref(sa), None, -1, ctypes.byref(aa), ctypes.byref(ca), stream)
+        assert rc == 0, lib.dllm_strerror(rc)
+    else:
+        assert lib.dllm_step(ctypes.byref(sa), stream) == 0
+        assert lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream) == 0
+    h = {k: v.cpu().numpy() for k, v in out.items()}
+    h.update(ids=ids.cpu().numpy(), cs=cs.cpu().numpy(), thr=thr.cpu().numpy(), b=d_b.cpu().numpy(),
+             K=d_K.cpu().numpy(), rid=d_rid.cpu().numpy(), p=p_arr.cpu().numpy(), gen=d_gen.cpu().numpy(),
+             evict=evict.cpu().numpy(), new_index=new_index.cpu().numpy(), src_row=src_row.cpu().numpy(),
+             A_out=int(A_out.cpu().numpy()[0]))
+    assert dllm.get_device_error(device) == 0
+    return h
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_step_commit_matches_oracle_and_the_two_launch_path(dllm, device, name, seed):
+    cfg = CASES[name]
+    inp, rid, K, b, gen, ld_gen = _batch(cfg, seed)
+    ref, exp = _expected(cfg, inp, rid, K, b, gen)
+    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True)
+    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False)
+    B, L = cfg.B, cfg.L
+    # the step's own outputs against the oracle (its ids / conf_state are
+    # checked after the commit below)
+    compare_step(ref, got, list(range(B)), L, ref["input_ids"], ref["conf_state"].astype(np.float32))
+    # commit and compaction against the oracle
+    A = exp["A_out"]
+    assert got["A_out"] == A
+    np.testing.assert_array_equal(got["evict"].astype(bool), exp["evict"])
+    np.testing.assert_array_equal(got["new_index"], exp["new_index"])
+    np.testing.assert_array_equal(got["src_row"][:A], exp["src_row"])
+    src = exp["src_row"]
+    np.testing.assert_array_equal(got["ids"][:A], exp["ids"][src])
+    cs_ref = exp["cs"][src]
+    assert np.array_equal(np.isnan(got["cs"][:A]), np.isnan(cs_ref))
+    np.testing.assert_allclose(got["cs"][:A][~np.isnan(cs_ref)], cs_ref[~np.isnan(cs_ref)], rtol=0, atol=1e-5)
+    np.testing.assert_array_equal(got["b"][:A], exp["b"][src])
+    np.testing.assert_array_equal(got["K"][:A], K[src])
+    np.testing.assert_array_equal(got["rid"][:A], rid[src])
+    np.testing.assert_array_equal(got["p"][:A], (np.arange(B) * 7)[src])
+    np.testing.assert_array_equal(got["thr"][:A], inp.thr[src])
+    for r, toks in exp["gen"].items():
+        np.testing.assert_array_equal(got["gen"][r][: len(toks)], toks)
+    # and everything element for element against the two-launch path
+    for k in ("done", "accept_len", "n_new", "tok", "evict", "new_index", "gen"):
+        np.testing.assert_array_equal(got[k], two[k], err_msg=k)
+    for k in ("feats", "conf", "lse", "cs", "thr"):
+        assert np.array_equal(got[k].view(np.uint32), two[k].view(np.uint32)), k
+    assert got["A_out"] == two["A_out"]
+    for k in ("ids", "b", "K", "rid", "p", "src_row"):
+        np.testing.assert_array_equal(got[k][:A], two[k][:A], err_msg=k)
