@@ -154,7 +154,7 @@ def load_traffic(step_src_sha, path=TRAFFIC_JSON):
 def step_source_sha():
     import hashlib
     h = hashlib.sha256()
-    for fn in ("step.cu", "common.cuh"):
+    for fn in ("step.cu", "common.cuh", "compact.cuh"):
         with open(os.path.join(ROOT, "denoise_step_token_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -960,6 +960,63 @@ def _fill_loop_logits(logits, pool, rows, seed, pool_rows, device):
     logits[flat] = pool[pick]
 
 
+READ_CEILING_SHAPES = [(14, 3, 4096), (16, 3, 4096), (8, 3, 8192), (12, 2, 8192), (4, 3, 16384), (8, 2, 4096),
+                       (24, 2, 4096)]   # (warps per CTA, ring slots, bytes per bulk copy)
+
+
+def run_read_ceiling(local_rank, gib=2, reps=5):
+    """The GPU's read-bandwidth ceiling, for the roofline of the step
+    kernel: a ``gib`` GiB device buffer read once per launch with no
+    arithmetic, by bulk copies into per-warp shared-memory rings (the step
+    kernel's way of reading logits; several ring shapes) and by plain 16-byte
+    loads; the best of ``reps`` launches each, CUDA events."""
+    import torch
+    from denoise_step_token_gb300 import _build
+    import denoise_step_token_gb300 as dllm
+    dllm.load()
+    lib = ctypes.CDLL(_build.PROBE_LIB_PATH)
+    p = ctypes.c_void_p
+    lib.dllm_probe_bulk_read.argtypes = [p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p]
+    lib.dllm_probe_load_read.argtypes = [p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, p, p]
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    nbytes = gib << 30
+    buf = torch.ones(nbytes, dtype=torch.uint8, device=device)
+    sink = torch.zeros(2, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = p(stream.cuda_stream)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+
+    def best(launch):
+        out = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = launch()
+            e1.record(stream)
+            e1.synchronize()
+            if rc:
+                raise RuntimeError(f"probe launch failed: {rc}")
+            out.append(nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        return max(out)
+
+    rows = []
+    for w, st, cb in READ_CEILING_SHAPES:
+        gbs = best(lambda: lib.dllm_probe_bulk_read(p(buf.data_ptr()), nbytes, sms, w, st, cb, p(sink.data_ptr()), sh))
+        rows.append({"kind": "bulk copies", "warps": w, "slots": st, "copy_bytes": cb,
+                     "in_flight_per_sm": w * st * cb, "gbs": gbs})
+    for threads, per_sm in ((1024, 2), (512, 8)):
+        gbs = best(lambda: lib.dllm_probe_load_read(p(buf.data_ptr()), nbytes, sms * per_sm, threads,
+                                                    p(sink.data_ptr()), sh))
+        rows.append({"kind": "16-byte loads", "threads": threads, "ctas_per_sm": per_sm, "gbs": gbs})
+    if int(sink[1].item()) != 0:
+        raise RuntimeError("a probe wait ran out")
+    peak, src = load_peaks()
+    return {"read_ceiling": rows, "max_gbs": max(r["gbs"] for r in rows), "buffer_bytes": nbytes,
+            "measured_copy_peak_gbs": peak, "peak_source": src}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -968,12 +1025,19 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--read-ceiling", action="store_true",
+                    help="measure the GPU's read-bandwidth ceiling (bulk copies and plain loads) instead")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dream",
                     help="dream (default, the headline), dream_fixed_steps, llada, stress, tiny, or the blockserve loop")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local_rank = dist_info()
+
+    if args.read_ceiling:
+        if rank == 0:
+            print(json.dumps(run_read_ceiling(local_rank)), flush=True)
+        return 0
 
     if args.impl == "reference":
         if rank != 0:

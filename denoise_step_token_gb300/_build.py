@@ -17,6 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libdllm.so")
+PROBE_DIR = os.path.join(PKG, "probe")
+PROBE_LIB_PATH = os.path.join(PKG, "libdllm_probe.so")   # bench.py's read-ceiling probe
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-ffp-contract=off", "--expt-relaxed-constexpr",
@@ -34,19 +36,24 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+def probe_sources():
+    return sorted(glob.glob(os.path.join(PROBE_DIR, "*.cu")))
+
+
 def _inputs():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
 def up_to_date():
-    if not os.path.exists(LIB_PATH):
+    if not os.path.exists(LIB_PATH) or not os.path.exists(PROBE_LIB_PATH):
         return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    t = min(os.path.getmtime(LIB_PATH), os.path.getmtime(PROBE_LIB_PATH))
+    return all(os.path.getmtime(f) <= t for f in _inputs() + probe_sources())
 
 
 def build(force=False, verbose=False, extra_flags=()):
-    """Compile every CUDA source for sm_103a and link libdllm.so."""
+    """Compile every CUDA source for sm_103a and link libdllm.so (and the
+    read-ceiling probe, libdllm_probe.so)."""
     if not force and up_to_date():
         return LIB_PATH
     nvcc = nvcc_path()
@@ -60,6 +67,12 @@ def build(force=False, verbose=False, extra_flags=()):
             print(" ".join(cmd))
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
         objs.append(obj)
+    probe_objs = []
+    for src in probe_sources():
+        obj = os.path.join(BUILD_DIR, "probe_" + os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+        probe_objs.append(obj)
     errors = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -69,12 +82,13 @@ def build(force=False, verbose=False, extra_flags=()):
             print(out.decode(errors="replace"))
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs]
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
+    for path, group in ((LIB_PATH, objs), (PROBE_LIB_PATH, probe_objs)):
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *group]
+        if verbose:
+            print(" ".join(cmd))
+        subprocess.check_call(cmd)
+        os.replace(tmp, path)
     return LIB_PATH
 
 

@@ -14,7 +14,10 @@
  *     Nothing is thrown across the ABI.  dllm_strerror() names a code.
  *   - "device" pointers are caller-owned CUDA device memory on the current
  *     device; "host" pointers are ordinary host memory.  The library never
- *     allocates or frees memory and never keeps a pointer after returning.
+ *     allocates or frees device memory, and no entry point keeps a pointer
+ *     after returning -- except the native loop object (dllm_loop_create:
+ *     host memory and a small pinned staging block of its own, and the
+ *     caller's workspace, all held until dllm_loop_destroy).
  *   - Device entry points are asynchronous on `stream` (a cudaStream_t passed
  *     as void*; NULL is the legacy default stream).  Only
  *     dllm_get_device_error() synchronises.
