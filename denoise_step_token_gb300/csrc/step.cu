@@ -1252,6 +1252,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const unsigned old = (unsigned)atom_add_acqrel_gpu(P.ctl + 1, 1);
         s_last = ((int)(old & 0xffffu) == G - 1) ? 1 + (int)(old >> 16) : 0;   // 1 + deferred commits
     }
+    // the fused commit's element map depends on launch parameters only:
+    // every CTA builds it in its idle rings while the exit add is in flight
+    if (P.commit && !s_ring_busy)
+        compact_map<kThreads>(P.cp, *reinterpret_cast<CompactScratch<kThreads>*>(smem), tid);
     __syncthreads();
     if (s_last) {
         const int n_def = s_last - 1;
@@ -1275,8 +1279,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             } else {
                 auto& scratch = *reinterpret_cast<CompactScratch<kThreads>*>(smem);
                 unsigned char* stage = smem + kCommitScratchBytes;
-                compact_map<kThreads>(P.cp, scratch, tid);
-                __syncthreads();
                 compact_rows<kThreads>(P.cp, scratch, stage, P.c_evict, P.B, tid);
             }
         }

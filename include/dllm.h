@@ -468,10 +468,10 @@ typedef struct dllm_compact_args {
  * not read.  The compacted arrays may
  * include adv's b / input_ids / conf_state (they are compacted after the
  * commit).  Errors as the two calls, plus DLLM_ERR_INVAL when cmp->A !=
- * adv->A and DLLM_ERR_UNSUPPORTED when a row of all the arrays (each
- * array's part rounded up to 4 bytes) holds more than 2048 elements: 4-byte
- * elements when every row size and array address is a multiple of 4, else
- * bytes. */
+ * adv->A and DLLM_ERR_UNSUPPORTED when a row of all the arrays holds more
+ * than 2048 elements of one size: each array's row moves in 16-byte
+ * elements when its row size and address are multiples of 16, else 4-byte
+ * elements when they are multiples of 4, else bytes. */
 int dllm_advance_compact(const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream);
 
 /* One FDFO iteration's step and batch tail in one launch: dllm_step (or
@@ -495,10 +495,10 @@ int dllm_advance_compact(const dllm_advance_args* adv, const dllm_compact_args* 
  *     are not read); the arrays may include b, input_ids and conf_state.
  *   - DLLM_ERR_INVAL when the pairs above differ, and every error of
  *     dllm_step, dllm_advance and dllm_compact; DLLM_ERR_UNSUPPORTED when
- *     a row of all the arrays holds more than 2048 elements (as for
- *     dllm_advance_compact).
+ *     a row of all the arrays holds more than 2048 elements of one size (as
+ *     for dllm_advance_compact).
  *   - Any number of rows: the last CTA compacts them in chunks of at most
- *     480 rows, staged through about 150 KiB of shared memory.  A block
+ *     480 rows, staged through about 140 KiB of shared memory.  A block
  *     index outside [0, K) sets DLLM_DEVERR_BLOCK_INDEX and that row is not
  *     advanced. */
 int dllm_step_commit(const dllm_step_args* step, const int32_t* quota, int64_t logits_rows,

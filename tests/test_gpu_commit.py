@@ -29,6 +29,11 @@ CASES = {
 }
 
 
+# cases whose batch also carries a 5-byte row array (moved byte by byte,
+# beside the 16-byte and 4-byte elements of the others)
+WITH_BYTES = {"ragged", "many_rows"}
+
+
 @pytest.fixture(scope="module")
 def device(dllm):
     import torch
@@ -63,7 +68,7 @@ def _expected(cfg, inp, rid, K, b, gen):
     return ref, dict(ids=ids, cs=cs, b=bb, gen=o_gen, evict=evict, new_index=new_index, src_row=src_row, A_out=A_out)
 
 
-def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused):
+def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=None):
     import torch
     lib = dllm.load()
     B, L = cfg.B, cfg.L
@@ -97,6 +102,11 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused):
                           evict=ptr(evict))
     arrays = [ids, cs, thr, d_b, d_K, d_rid, p_arr]
     rb = [L * 4, L * 4, 4, 4, 4, 4, 4]
+    d_extra = None
+    if extra is not None:
+        d_extra = t(extra)
+        arrays.append(d_extra)
+        rb.append(extra.shape[1])
     arr = (ctypes.c_void_p * dllm.COMPACT_MAX_ARRAYS)(*[x.data_ptr() for x in arrays])
     rbs = (ctypes.c_int64 * dllm.COMPACT_MAX_ARRAYS)(*rb)
     cws = torch.empty(lib.dllm_compact_workspace_size(B, len(rb), ctypes.cast(rbs, ctypes.c_void_p)),
@@ -115,7 +125,7 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused):
     h.update(ids=ids.cpu().numpy(), cs=cs.cpu().numpy(), thr=thr.cpu().numpy(), b=d_b.cpu().numpy(),
              K=d_K.cpu().numpy(), rid=d_rid.cpu().numpy(), p=p_arr.cpu().numpy(), gen=d_gen.cpu().numpy(),
              evict=evict.cpu().numpy(), new_index=new_index.cpu().numpy(), src_row=src_row.cpu().numpy(),
-             A_out=int(A_out.cpu().numpy()[0]))
+             A_out=int(A_out.cpu().numpy()[0]), extra=None if d_extra is None else d_extra.cpu().numpy())
     assert dllm.get_device_error(device) == 0
     return h
 
@@ -126,8 +136,10 @@ def test_step_commit_matches_oracle_and_the_two_launch_path(dllm, device, name, 
     cfg = CASES[name]
     inp, rid, K, b, gen, ld_gen = _batch(cfg, seed)
     ref, exp = _expected(cfg, inp, rid, K, b, gen)
-    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True)
-    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False)
+    extra = (np.random.default_rng(seed + 200).integers(0, 255, (cfg.B, 5)).astype(np.uint8)
+             if name in WITH_BYTES else None)
+    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True, extra=extra)
+    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False, extra=extra)
     B, L = cfg.B, cfg.L
     # the step's own outputs against the oracle (its ids / conf_state are
     # checked after the commit below)
@@ -148,6 +160,9 @@ def test_step_commit_matches_oracle_and_the_two_launch_path(dllm, device, name, 
     np.testing.assert_array_equal(got["rid"][:A], rid[src])
     np.testing.assert_array_equal(got["p"][:A], (np.arange(B) * 7)[src])
     np.testing.assert_array_equal(got["thr"][:A], inp.thr[src])
+    if extra is not None:
+        np.testing.assert_array_equal(got["extra"][:A], extra[src])
+        np.testing.assert_array_equal(two["extra"][:A], extra[src])
     for r, toks in exp["gen"].items():
         np.testing.assert_array_equal(got["gen"][r][: len(toks)], toks)
     # and everything element for element against the two-launch path
