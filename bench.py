@@ -300,7 +300,8 @@ class Pipeline:
         self.box_pad = torch.empty(B, dtype=torch.int32, device=device)
         self.box_start = torch.empty(B, dtype=torch.int32, device=device)
         # workspaces
-        ws_bytes = self.lib.dllm_step_workspace_size(B, L, V)
+        # a vocabulary-sharded step has one more partial chunk per shard boundary
+        ws_bytes = self.lib.dllm_step_workspace_size(B, L, V + 8192 * (int(vocab_shards or 1) - 1))
         self.step_ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
         rb = [L * 4, L * 4, 4, 4, 4, 4, 4]
         self.rb_arr = (ctypes.c_int64 * dllm.COMPACT_MAX_ARRAYS)(*rb)
@@ -316,21 +317,17 @@ class Pipeline:
         # fixed-steps rule: request b has taken L - (its masked count) steps
         # of its block (one token per step at S = L), so its quota is
         # transfer_quota(L, S, that step)
-        # vocabulary shards: S2 shard by shard (dllm_step_shard), then one merge
+        # vocabulary shards: column slices of the logits array, all stepped in
+        # one launch (dllm_step_vocab_shards)
         self.shards = None
         if vocab_shards:
             n = int(vocab_shards)
             width = -(-(cfg.V // n) // 8) * 8
             bounds = [min(k * width, cfg.V) for k in range(n)] + [cfg.V]
-            BL = B * L
-            self.trip = [torch.empty((n, BL), dtype=dt, device=device) for dt in (torch.float32, torch.float32,
-                                                                                  torch.int32)]
-            self.shards = []
+            self.shards = (dllm.VocabShard * n)()
             for k in range(n):
-                a = dllm.StepArgs.from_buffer_copy(self.args[0][1])
-                a.V = bounds[k + 1] - bounds[k]
-                a.logits = ctypes.c_void_p(self.logits.data_ptr() + bounds[k] * 2)
-                self.shards.append((bounds[k], a))
+                self.shards[k] = dllm.VocabShard(logits=ctypes.c_void_p(self.logits.data_ptr() + bounds[k] * 2),
+                                                 ldv=self.logits.shape[1], v0=bounds[k], V=bounds[k + 1] - bounds[k])
         self.fused = self.shards is None   # the vocabulary-sharded step keeps its separate commit
         self.quota = None
         if fixed_steps is not None:
@@ -420,19 +417,16 @@ class Pipeline:
 
     def launch_step(self, slot, stream, compact=None):
         """The step of one pipeline step on state slot ``slot`` (dllm_step,
-        dllm_step_quota, the vocabulary shards plus their merge, or
-        dllm_step_compact); returns the OR of the status codes."""
+        dllm_step_quota, dllm_step_vocab_shards or dllm_step_compact);
+        returns the OR of the status codes."""
         lib = self.lib
         sa = self.args[slot][1]
         rc = 0
         if self.shards is not None and compact is None:
-            for k, (v0, a) in enumerate(self.shards):
-                a.input_ids = sa.input_ids
-                rc |= lib.dllm_step_shard(ctypes.byref(a), v0, *(ctypes.c_void_p(t[k].data_ptr()) for t in self.trip),
-                                          stream)
-            rc |= lib.dllm_step_merge(ctypes.byref(sa), len(self.shards), ctypes.c_void_p(self.trip[0].data_ptr()),
-                                      ctypes.c_void_p(self.trip[1].data_ptr()), ctypes.c_void_p(self.trip[2].data_ptr()),
-                                      self.B * self.L, None, stream)
+            saved = sa.logits
+            sa.logits = None
+            rc |= lib.dllm_step_vocab_shards(ctypes.byref(sa), len(self.shards), self.shards, None, stream)
+            sa.logits = saved
         elif compact is not None:
             buf, rows = compact
             saved = sa.logits
@@ -451,13 +445,12 @@ class Pipeline:
 
     def launches_per_step(self):
         """Kernels one ``run`` launches: pack, then either the step with the
-        fused commit (one launch), or the step (one launch per vocabulary
-        shard plus the merge) and advance + compaction (one launch while the
-        state rows fit its staging buffer, else advance, scatter and
-        copy-back)."""
+        fused commit (one launch), or the step over the vocabulary shards
+        (one launch) and advance + compaction (one launch while the state
+        rows fit its staging buffer, else advance, scatter and copy-back)."""
         if getattr(self, "fused", False):
             return 2
-        step = len(self.shards) + 1 if self.shards is not None else 1
+        step = 1
         row_total = sum(self.rb_arr[k] for k in range(7))
         commit = 1 if self.B * row_total <= FUSED_STAGE_BYTES else 3
         return 1 + step + commit
@@ -1100,7 +1093,7 @@ def main():
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,
                          "all_rows_logits_bytes_per_launch": cfg.B * cfg.L * cfg.V * 2,
-                         "kernel": ("4 x step_kernel (dllm_step_shard) + merge_kernel" if pipe.shards else
+                         "kernel": ("step_kernel over 4 vocabulary shards (dllm_step_vocab_shards)" if pipe.shards else
                                     "step_kernel with the fused commit (dllm_step_commit" +
                                     (", fixed-steps quota)" if fixed else ")")),
                          "algorithmic_bytes_per_launch": alg,

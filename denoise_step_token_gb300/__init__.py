@@ -76,6 +76,13 @@ class AdvanceArgs(ctypes.Structure):
                 ("gen_tokens", _p), ("ld_gen", _i64), ("evict", _p)]
 
 
+class VocabShard(ctypes.Structure):
+    _fields_ = [("logits", _p), ("ldv", _i64), ("v0", _i32), ("V", _i32)]
+
+
+MAX_VOCAB_SHARDS = 8
+
+
 class LoopConfig(ctypes.Structure):
     _fields_ = [("R", _i32), ("L", _i32), ("V", _i32), ("mask_id", _i32), ("pad_id", _i32), ("mode", _i32),
                 ("reloop", _i32), ("S", _i32), ("capacity", _i32), ("pad0", _i32), ("budget", _i64)]
@@ -114,6 +121,8 @@ _SIGNATURES = {
     "dllm_step_shard": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int32, _p, _p, _p, _p]),
     "dllm_step_merge": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int32, _p, _p, _p, ctypes.c_int64, _p,
                                        _p]),
+    "dllm_step_vocab_shards": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int32, ctypes.POINTER(VocabShard),
+                                              _p, _p]),
     "dllm_predict_steps_stub": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_int32, _p, _p, _p, _p]),
     "dllm_load_control": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_double, _p]),
     "dllm_slo_thresholds": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p, _p, _p]),
@@ -177,7 +186,8 @@ def load(build=True):
             fn.argtypes = args
         if lib.dllm_abi_version() != ABI_VERSION:
             raise RuntimeError(f"libdllm ABI version {lib.dllm_abi_version()}, binding expects {ABI_VERSION}")
-        for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs, LoopConfig, LoopInfo)):
+        for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs, LoopConfig, LoopInfo,
+                                     VocabShard)):
             if lib.dllm_struct_size(which) != ctypes.sizeof(cls):
                 raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {lib.dllm_struct_size(which)} "
                                    f"bytes, binding {ctypes.sizeof(cls)}")
@@ -373,6 +383,50 @@ def step_sharded(logits, input_ids, thr, conf_state, *, V, mask_id, bounds, feat
                  workspace_bytes=ws.numel())
     _check("dllm_step_merge", lib.dllm_step_merge(ctypes.byref(a), n, _ptr(tm), _ptr(ts), _ptr(ti), BL, _ptr(quota),
                                                   _stream(dev)))
+    return out
+
+
+def step_vocab_shards(shards, input_ids, thr, conf_state, *, mask_id, feats=True, debug=False, quota=None,
+                      workspace=None):
+    """The step over logits held as vocabulary shards on this device, in one
+    launch (dllm_step_vocab_shards): ``shards`` is a list of (logits, v0, V)
+    with logits a 16-bit CUDA tensor of B*L rows holding global tokens
+    [v0, v0 + V) in its first V columns (a column slice of a wider array is
+    fine: its row stride is taken from the tensor), shards in vocabulary
+    order from 0.  Returns the outputs of ``step`` (equal, bit for bit, to
+    ``step_sharded`` over the same shards)."""
+    torch = _torch()
+    dev = _require_cuda(input_ids, conf_state, thr, quota)
+    B, L = input_ids.shape
+    n = len(shards)
+    if not 1 <= n <= MAX_VOCAB_SHARDS:
+        raise ValueError(f"1 to {MAX_VOCAB_SHARDS} shards")
+    V = sum(w for _, _, w in shards)
+    arr = (VocabShard * n)()
+    for k, (t, v0, w) in enumerate(shards):
+        if not t.is_cuda or t.device != dev:
+            raise ValueError("each shard is a CUDA tensor on the device of input_ids")
+        if t.element_size() != 2 or t.dim() != 2 or t.shape[0] != B * L or t.stride(1) != 1 or t.shape[1] < w:
+            raise ValueError("each shard holds B*L rows of 16-bit logits, at least V columns, unit column stride")
+        arr[k] = VocabShard(logits=_ptr(t), ldv=t.stride(0), v0=v0, V=w)
+    out = {"done": torch.empty(B, dtype=torch.uint8, device=dev),
+           "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "n_new": torch.empty(B, dtype=torch.int32, device=dev)}
+    if feats:
+        out["feats"] = torch.empty((B, NUM_FEATURES), dtype=torch.float32, device=dev)
+    if debug:
+        out["conf"] = torch.empty((B, L), dtype=torch.float32, device=dev)
+        out["lse"] = torch.empty((B, L), dtype=torch.float32, device=dev)
+        out["tok"] = torch.empty((B, L), dtype=torch.int32, device=dev)
+    lib = load()
+    need = int(lib.dllm_step_workspace_size(B, L, V + 8192 * (n - 1)))
+    ws = workspace if workspace is not None else _step_ws.get(dev, need)
+    a = StepArgs(B=B, L=L, V=V, mask_id=mask_id, ldv=0, logits=None, input_ids=_ptr(input_ids), thr=_ptr(thr),
+                 conf_state=_ptr(conf_state), done=_ptr(out["done"]), accept_len=_ptr(out["accept_len"]),
+                 n_new=_ptr(out["n_new"]), feats=_ptr(out.get("feats")), conf_out=_ptr(out.get("conf")),
+                 lse_out=_ptr(out.get("lse")), tok_out=_ptr(out.get("tok")), workspace=_ptr(ws),
+                 workspace_bytes=ws.numel())
+    _check("dllm_step_vocab_shards", lib.dllm_step_vocab_shards(ctypes.byref(a), n, arr, _ptr(quota), _stream(dev)))
     return out
 
 

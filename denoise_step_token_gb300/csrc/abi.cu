@@ -102,6 +102,7 @@ extern "C" size_t dllm_struct_size(int which) {
         case 4: return sizeof(dllm_refill_args);
         case 5: return sizeof(dllm_loop_config);
         case 6: return sizeof(dllm_loop_info_t);
+        case 7: return sizeof(dllm_vocab_shard);
         default: return 0;
     }
 }

@@ -191,7 +191,34 @@ struct StepParams {
     long long c_ld_gen;
     uint8_t* c_evict;   // [B] out: the row leaves the batch
     CompactPlan cp;     // stable compaction of the caller's row arrays by c_evict
+    // vocabulary shards in one launch (dllm_step_vocab_shards); n_shards == 0
+    // otherwise.  A row's chunks are shard 0's, then shard 1's, ...: shard k
+    // holds chunks [sh_c0[k], sh_c0[k + 1]).
+    int n_shards;
+    const uint16_t* sh_logits[DLLM_MAX_VOCAB_SHARDS];
+    long long sh_ldv[DLLM_MAX_VOCAB_SHARDS];
+    int sh_v0[DLLM_MAX_VOCAB_SHARDS];
+    int sh_V[DLLM_MAX_VOCAB_SHARDS];
+    int sh_c0[DLLM_MAX_VOCAB_SHARDS + 1];
 };
+
+// Where chunk c of a row lives: its logits array and row stride, its first
+// element within that array's row, its length, and its vocabulary shard
+// (-1 without shards).
+struct ChunkRef {
+    const uint16_t* base;
+    long long ldv;
+    int start, len, shard;
+};
+__device__ __forceinline__ ChunkRef chunk_ref(const StepParams& P, int c) {
+    if (P.n_shards == 0) return ChunkRef{P.logits, P.ldv, c * kChunkElems, min(kChunkElems, P.V - c * kChunkElems), -1};
+    int k = 0;
+#pragma unroll
+    for (int i = 1; i < DLLM_MAX_VOCAB_SHARDS; ++i)
+        if (i < P.n_shards && c >= P.sh_c0[i]) k = i;
+    const int start = (c - P.sh_c0[k]) * kChunkElems;
+    return ChunkRef{P.sh_logits[k], P.sh_ldv[k], start, min(kChunkElems, P.sh_V[k] - start), k};
+}
 
 // A deferred commit's list entry: the request, and whether its block is
 // reset for the next one (fused commit) rather than given its new tokens.
@@ -214,9 +241,8 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline bool ws_layout(long long B, long long L, long long V, size_t bytes, WsLayout* w) {
+inline bool ws_layout_nc(long long B, long long L, long long NC, size_t bytes, WsLayout* w) {
     const long long BL = B * L;
-    const long long NC = (V + kChunkElems - 1) / kChunkElems;
     w->off_part = align256(64 + 4 * size_t(BL + 2 * B));
     w->off_row = align256(w->off_part + size_t(BL * NC) * 8);
     w->counters_bytes = w->off_row + size_t(BL) * 8;
@@ -226,6 +252,10 @@ inline bool ws_layout(long long B, long long L, long long V, size_t bytes, WsLay
     w->data_bytes = d;
     w->front = (bytes / 4) & ~size_t(255);
     return w->counters_bytes <= w->front && w->data_bytes + w->front <= bytes;
+}
+
+inline bool ws_layout(long long B, long long L, long long V, size_t bytes, WsLayout* w) {
+    return ws_layout_nc(B, L, (V + kChunkElems - 1) / kChunkElems, bytes, w);
 }
 
 inline size_t ws_required(long long B, long long L, long long V) {
@@ -705,6 +735,70 @@ __device__ __forceinline__ void finalize_request(const StepParams& P, int b, boo
 }
 
 // ---------------------------------------------------------------------------
+// The fold of a row's chunk partials [c0, c1) (a whole row, or one
+// vocabulary shard of it): each lane folds chunks c0 + lane, c0 + lane + 32,
+// ... in order, then the lanes combine in a fixed butterfly; the order
+// depends only on c1 - c0.  key: (chunk - c0) * batches + batch of the first
+// maximum, or INT64_MAX when no chunk holds a finite value.  Each word is
+// cleared once read, ready for the next call.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fold_row_chunks(const StepParams& P, int row, int c0, int c1, int lane, float& M,
+                                                float& S, long long& key) {
+    M = -INFINITY;
+    S = 0.f;
+    key = 0x7fffffffffffffffLL;
+    for (int c = c0 + lane; c < c1; c += 32) {
+        unsigned long long* wp = P.part + (long long)row * P.NC + c;
+        unsigned long long w = ld_relaxed_gpu_u64(wp);
+        if (w == 0ull) w = poll_word(wp, P.err);
+        *wp = 0ull;
+        float pm, ps;
+        int pk;
+        unpack_partial(w, pm, ps, pk);
+        const long long kc = (long long)(c - c0) * kBatchesPerChunk + min(max(pk, 0), kBatchesPerChunk - 1);
+        if (pm > M) key = kc;
+        combine(M, S, pm, ps);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, M, off);
+        const float so = __shfl_xor_sync(0xffffffffu, S, off);
+        const long long ko = __shfl_xor_sync(0xffffffffu, key, off);
+        if (mo > M || (mo == M && ko < key)) key = ko;
+        combine(M, S, mo, so);
+    }
+}
+
+// The argmax: the first element equal to M inside the 2048-element batch
+// `key` of the row at rp (Vr elements); each lane loads all of its vectors
+// at once, then scans them in order.  0xffffffff when there is none (no
+// finite maximum: nothing is read).
+__device__ __forceinline__ unsigned first_max_in_batch_at(const uint16_t* rp, int Vr, long long key, float M,
+                                                          int lane) {
+    if (key == 0x7fffffffffffffffLL) return 0xffffffffu;
+    const long long start = key * kBatchElems;
+    uint4 v[kBatchVecs];
+#pragma unroll
+    for (int k = 0; k < kBatchVecs; ++k) {
+        const long long e = start + (long long)(lane + 32 * k) * 8;
+        v[k] = (e < Vr) ? __ldg(reinterpret_cast<const uint4*>(rp + e))
+                        : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+    unsigned best = 0xffffffffu;
+#pragma unroll
+    for (int k = kBatchVecs - 1; k >= 0; --k) {
+        const long long e = start + (long long)(lane + 32 * k) * 8;
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int h = 7; h >= 0; --h) {
+            const float x = (h & 1) ? bf16_hi(w[h >> 1]) : bf16_lo(w[h >> 1]);
+            if (e + h < Vr && x == M) best = (unsigned)(e + h);
+        }
+    }
+    return __reduce_min_sync(0xffffffffu, best);
+}
+
+// ---------------------------------------------------------------------------
 // Row finisher: fold the chunk partials of `row` in a fixed order, write the
 // row results, then count the row towards its request.
 // ---------------------------------------------------------------------------
@@ -734,53 +828,38 @@ __device__ __noinline__ void finish_row(const StepParams& P, const uint16_t* s_g
 #pragma unroll
         for (int off = 16; off; off >>= 1) mb += __shfl_xor_sync(0xffffffffu, mb, off);
     }
-    // each lane folds chunks lane, lane + 32, ... in order, then the lanes
-    // combine in a fixed butterfly; the order depends only on NC
-    float M = -INFINITY, S = 0.f;
-    long long key = 0x7fffffffffffffffLL;   // chunk * batches + batch of the first maximum
-    for (int c = lane; c < NC; c += 32) {
-        unsigned long long* wp = P.part + (long long)row * NC + c;
-        unsigned long long w = ld_relaxed_gpu_u64(wp);
-        if (w == 0ull) w = poll_word(wp, P.err);
-        *wp = 0ull;
-        float pm, ps;
-        int pk;
-        unpack_partial(w, pm, ps, pk);
-        const long long kc = (long long)c * kBatchesPerChunk + min(max(pk, 0), kBatchesPerChunk - 1);
-        if (pm > M) key = kc;
-        combine(M, S, pm, ps);
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, M, off);
-        const float so = __shfl_xor_sync(0xffffffffu, S, off);
-        const long long ko = __shfl_xor_sync(0xffffffffu, key, off);
-        if (mo > M || (mo == M && ko < key)) key = ko;
-        combine(M, S, mo, so);
-    }
-    // argmax: first element equal to M inside that 2048-element batch; each
-    // lane loads all of its vectors at once, then scans them in order
-    const long long start = key * kBatchElems;
-    const uint16_t* rp = P.logits + (long long)lrow * P.ldv;
-    uint4 v[kBatchVecs];
-#pragma unroll
-    for (int k = 0; k < kBatchVecs; ++k) {
-        const long long e = start + (long long)(lane + 32 * k) * 8;
-        v[k] = (e < P.V) ? __ldg(reinterpret_cast<const uint4*>(rp + e))
-                         : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-    }
-    unsigned best = 0xffffffffu;
-#pragma unroll
-    for (int k = kBatchVecs - 1; k >= 0; --k) {
-        const long long e = start + (long long)(lane + 32 * k) * 8;
-        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-        for (int h = 7; h >= 0; --h) {
-            const float x = (h & 1) ? bf16_hi(w[h >> 1]) : bf16_lo(w[h >> 1]);
-            if (e + h < P.V && x == M) best = (unsigned)(e + h);
+    float M, S;
+    long long key;
+    const uint16_t* rp;
+    int Vr, v0 = 0;
+    if (P.n_shards == 0) {
+        fold_row_chunks(P, row, 0, NC, lane, M, S, key);
+        rp = P.logits + (long long)lrow * P.ldv;
+        Vr = P.V;
+    } else {
+        // each shard folded as a launch over that shard alone folds it, then
+        // the shards merged in order as dllm_step_merge merges their triples:
+        // the token comes from the first shard attaining the maximum
+        M = -INFINITY;
+        S = 0.f;
+        key = 0x7fffffffffffffffLL;
+        int ks = -1;
+        for (int k = 0; k < P.n_shards; ++k) {
+            float mk, sk;
+            long long kk;
+            fold_row_chunks(P, row, P.sh_c0[k], P.sh_c0[k + 1], lane, mk, sk, kk);
+            if (mk > M || ks < 0) {
+                ks = k;
+                key = kk;
+            }
+            combine(M, S, mk, sk);
         }
+        rp = P.sh_logits[ks] + (long long)lrow * P.sh_ldv[ks];
+        Vr = P.sh_V[ks];
+        v0 = P.sh_v0[ks];
     }
-    best = __reduce_min_sync(0xffffffffu, best);
+    const unsigned best0 = first_max_in_batch_at(rp, Vr, key, M, lane);
+    const unsigned best = (best0 == 0xffffffffu || P.n_shards == 0) ? best0 : best0 + (unsigned)v0;
     const float conf = __fdiv_rn(1.0f, S);
     const float lse = M + logf(S);
     if (P.shard) {   // S2 of a vocabulary shard: the row's triple, nothing else
@@ -946,7 +1025,17 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const int mk = Ms * k;
         int r = fast_div(mk, P.div_g);
         const int e = fast_div(V * (mk - r * G), P.div_g);
-        int cc = (e + kChunkElems - 1) / kChunkElems;
+        // the first chunk starting at or after element e of the row (shard
+        // by shard when the row is split into vocabulary shards)
+        int cc;
+        if (P.n_shards == 0) {
+            cc = (e + kChunkElems - 1) / kChunkElems;
+        } else {
+            int k = 0;
+            for (int i = 1; i < P.n_shards; ++i)
+                if (e >= P.sh_v0[i]) k = i;
+            cc = P.sh_c0[k] + (e - P.sh_v0[k] + kChunkElems - 1) / kChunkElems;
+        }
         if (cc >= NC) {
             r += 1;
             cc = 0;
@@ -997,7 +1086,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
     const int n_units = u1 - u0;   // this CTA's chunks: unit k is chunk u0 + k
     const int u_first = u0;
-    const int V32 = P.V;
     // masked position of unit gu's row (units of the tail have their own slots)
     auto row_of = [&](int gu) -> int {
         const int rr = fast_div(gu, P.div_nc);
@@ -1059,7 +1147,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
         // producer side: the chunk being issued
         int p_unit = 0, p_left = 0, p_q = 0, p_len = 0;
-        long long p_src = 0;
+        const uint16_t* p_src = nullptr;
         bool p_done = false;
         // groups whose copies are issued but not yet folded, oldest first
         int fifo_u[kStages + 1], fifo_k[kStages + 1];
@@ -1073,8 +1161,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const int lrow = P.compact ? rr : row_of(gu);   // compact logits are indexed by rank
             p_unit = gu;
             p_q = 0;
-            p_len = min(kChunkElems, V32 - c * kChunkElems);
-            p_src = (long long)lrow * P.ldv + (long long)c * kChunkElems;
+            const ChunkRef cr = chunk_ref(P, c);
+            p_len = cr.len;
+            p_src = cr.base + (long long)lrow * cr.ldv + cr.start;
         };
         auto issue = [&]() {
             if (p_done) return;
@@ -1105,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const int slot = issued % kStages;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar0 + slot * 8, bytes);
-                bulk_g2s(stage0 + slot * kCopyBytes, P.logits + p_src + (long long)p_q * kCopyElems, bytes,
+                bulk_g2s(stage0 + slot * kCopyBytes, p_src + (long long)p_q * kCopyElems, bytes,
                          bar0 + slot * 8, pol);
             }
             ++issued;
@@ -1151,7 +1240,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
 #pragma unroll 1
             for (int j = 0; j < k && !failed; ++j) {
-                const int clen = min(kChunkElems, V32 - (c0 + j) * kChunkElems);
+                const int clen = chunk_ref(P, c0 + j).len;
                 const int ncp = (clen + kCopyElems - 1) / kCopyElems;
                 float m = -INFINITY, s = 0.f;
                 int kb = kBatchesPerChunk;
@@ -1401,6 +1490,13 @@ struct CommitSpec {
     const dllm_compact_args* cmp;
 };
 
+// Vocabulary shards reduced in one launch (dllm_step_vocab_shards), already
+// checked to tile [0, V) in order.
+struct ShardTable {
+    int n;
+    const dllm_vocab_shard* s;
+};
+
 // A checked step launch: grid, block, shared memory and parameters.
 struct StepLaunch {
     bool empty;   // B == 0: nothing to launch
@@ -1414,20 +1510,26 @@ struct StepLaunch {
 // logits_rows >= 0 the compact layout; shard non-null S2 alone over a
 // vocabulary shard.
 int prepare_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
-                 StepLaunch* out, const CommitSpec* commit = nullptr) {
+                 StepLaunch* out, const CommitSpec* commit = nullptr, const ShardTable* vs = nullptr) {
     out->empty = true;
     if (!a) return DLLM_ERR_INVAL;
-    if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || a->ldv < a->V) return DLLM_ERR_INVAL;
+    if (a->B < 0 || a->L < 1 || a->L > DLLM_MAX_L || a->V < 1 || (!vs && a->ldv < a->V)) return DLLM_ERR_INVAL;
     if (a->B == 0) return DLLM_OK;
     if ((long long)a->B * a->L > 0x7fffffffLL || a->B >= (1 << 16)) return DLLM_ERR_UNSUPPORTED;
-    if (!a->logits || !a->input_ids) return DLLM_ERR_INVAL;
+    if ((!vs && !a->logits) || !a->input_ids) return DLLM_ERR_INVAL;
     if (!shard && ((!quota && !a->thr) || !a->conf_state || !a->done || !a->accept_len || !a->n_new))
         return DLLM_ERR_INVAL;
     if (shard && (!shard->m || !shard->s || !shard->idx || shard->v0 < 0)) return DLLM_ERR_INVAL;
-    if ((a->ldv % 8) != 0 || (reinterpret_cast<uintptr_t>(a->logits) & 15u) != 0) return DLLM_ERR_ALIGN;
+    if (!vs && ((a->ldv % 8) != 0 || (reinterpret_cast<uintptr_t>(a->logits) & 15u) != 0)) return DLLM_ERR_ALIGN;
     if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return DLLM_ERR_WORKSPACE;
+    // chunks per row: the row's, or each shard's in turn
+    long long nc_ll = (a->V + kChunkElems - 1) / kChunkElems;
+    if (vs) {
+        nc_ll = 0;
+        for (int k = 0; k < vs->n; ++k) nc_ll += (vs->s[k].V + kChunkElems - 1) / kChunkElems;
+    }
     WsLayout w;
-    if (!ws_layout(a->B, a->L, a->V, a->workspace_bytes, &w)) return DLLM_ERR_WORKSPACE;
+    if (!ws_layout_nc(a->B, a->L, nc_ll, a->workspace_bytes, &w)) return DLLM_ERR_WORKSPACE;
 
     int dev = 0;
     DLLM_CUDA_TRY(cudaGetDevice(&dev));
@@ -1435,7 +1537,8 @@ int prepare_step(const dllm_step_args* a, const int32_t* quota, long long logits
     if (G <= 0) return DLLM_ERR_CUDA;
     if (G >= (1 << 15)) return DLLM_ERR_UNSUPPORTED;   // the exit counter's low half counts CTAs
     const int BL = a->B * a->L;
-    const int NC = (a->V + kChunkElems - 1) / kChunkElems;
+    if ((long long)BL * nc_ll > 0x7fffffffLL) return DLLM_ERR_UNSUPPORTED;
+    const int NC = (int)nc_ll;
     if ((long long)BL * NC > 0x7fffffffLL || (long long)BL * G > 0x7fffffffLL || (long long)a->V * G > 0x7fffffffLL)
         return DLLM_ERR_UNSUPPORTED;
     // rows one CTA touches: its static share (< BL / G + 3 rows) plus the
@@ -1484,6 +1587,19 @@ int prepare_step(const dllm_step_args* a, const int32_t* quota, long long logits
         const int prc = make_compact_plan(commit->cmp, kThreads, kCommitStageBytes, &P.cp);
         if (prc != DLLM_OK) return prc;
     }
+    if (vs) {
+        P.n_shards = vs->n;
+        int c0 = 0;
+        for (int k = 0; k < vs->n; ++k) {
+            P.sh_logits[k] = vs->s[k].logits;
+            P.sh_ldv[k] = vs->s[k].ldv;
+            P.sh_v0[k] = vs->s[k].v0;
+            P.sh_V[k] = vs->s[k].V;
+            P.sh_c0[k] = c0;
+            c0 += (vs->s[k].V + kChunkElems - 1) / kChunkElems;
+        }
+        for (int k = vs->n; k <= DLLM_MAX_VOCAB_SHARDS; ++k) P.sh_c0[k] = c0;
+    }
     P.B = a->B; P.L = a->L; P.V = a->V; P.NC = NC; P.BL = BL; P.mask_id = a->mask_id;
     P.list_cap = list_cap; P.static_cap = static_cap; P.zero_cap = zero_cap; P.ldv = a->ldv;
     P.div_nc = make_fastdiv((uint32_t)NC);
@@ -1519,9 +1635,9 @@ int launch_prepared(const StepLaunch& sl, void* stream) {
 }
 
 int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_rows, const ShardOut* shard,
-                void* stream, const CommitSpec* commit = nullptr) {
+                void* stream, const CommitSpec* commit = nullptr, const ShardTable* vs = nullptr) {
     StepLaunch sl;
-    const int rc = prepare_step(a, quota, logits_rows, shard, &sl, commit);
+    const int rc = prepare_step(a, quota, logits_rows, shard, &sl, commit, vs);
     if (rc != DLLM_OK) return rc;
     return launch_prepared(sl, stream);
 }
@@ -1551,6 +1667,22 @@ extern "C" int dllm_step_commit(const dllm_step_args* a, const int32_t* quota, i
         return DLLM_ERR_INVAL;
     const CommitSpec commit{adv, cmp};
     return launch_step(a, quota, logits_rows < 0 ? -1 : logits_rows, nullptr, stream, &commit);
+}
+
+extern "C" int dllm_step_vocab_shards(const dllm_step_args* a, int32_t n_shards, const dllm_vocab_shard* shards,
+                                      const int32_t* quota, void* stream) {
+    if (!a || !shards || n_shards < 1 || n_shards > DLLM_MAX_VOCAB_SHARDS) return DLLM_ERR_INVAL;
+    long long next = 0;
+    for (int k = 0; k < n_shards; ++k) {
+        const dllm_vocab_shard& sh = shards[k];
+        if (!sh.logits || sh.V < 1 || sh.v0 != next || sh.ldv < sh.V) return DLLM_ERR_INVAL;
+        next += sh.V;
+    }
+    if (next != a->V) return DLLM_ERR_INVAL;
+    for (int k = 0; k < n_shards; ++k)
+        if (shards[k].ldv % 8 != 0 || (reinterpret_cast<uintptr_t>(shards[k].logits) & 15u) != 0) return DLLM_ERR_ALIGN;
+    const ShardTable vs{n_shards, shards};
+    return launch_step(a, quota, -1, nullptr, stream, nullptr, &vs);
 }
 
 extern "C" int dllm_step_shard(const dllm_step_args* a, int32_t v0, float* m, float* s, int32_t* idx, void* stream) {

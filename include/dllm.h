@@ -75,7 +75,7 @@ int dllm_last_cuda_error(const char** name);
 /* sizeof() of the argument structs below, for binding self-checks:
  * which = 0 dllm_step_args, 1 dllm_pack_args, 2 dllm_compact_args,
  * 3 dllm_advance_args, 4 dllm_refill_args, 5 dllm_loop_config,
- * 6 dllm_loop_info_t.  Returns 0 for an unknown `which`. */
+ * 6 dllm_loop_info_t, 7 dllm_vocab_shard.  Returns 0 for an unknown `which`. */
 size_t dllm_struct_size(int which);
 
 /* Fault injection for tests of the status plumbing (host only; nothing
@@ -222,6 +222,35 @@ int dllm_step_shard(const dllm_step_args* args, int32_t v0, float* m, float* s, 
  * DLLM_ERR_INVAL for n_shards < 1, shard_stride < B * L or NULL triples. */
 int dllm_step_merge(const dllm_step_args* args, int32_t n_shards, const float* m, const float* s,
                     const int32_t* idx, int64_t shard_stride, const int32_t* quota, void* stream);
+
+/* The step over logits held as vocabulary shards, all on this device, in
+ * one launch: what dllm_step_shard on every shard followed by
+ * dllm_step_merge computes, bit for bit, without the triples' round trip or
+ * the per-launch start-up and tail paid once per shard (an LM head computed
+ * in vocabulary chunks into separate buffers, or the shards of a
+ * vocabulary-parallel head gathered on one GPU).
+ *   - shards[k]: logits (device bf16 [B*L][ldv], 16-byte aligned, ldv a
+ *     multiple of 8 and >= V) holding global tokens [v0, v0 + V); shard 0
+ *     starts at v0 = 0, each next one where the previous ends, and their
+ *     widths add up to args->V.  1 <= n_shards <= DLLM_MAX_VOCAB_SHARDS.
+ *   - args as for dllm_step; args->logits and args->ldv are not read.  quota
+ *     NULL: the threshold rule, else the fixed-steps rule.
+ *   - Each shard is reduced in its own chunks (a shard's reduction order
+ *     depends only on its width), so the workspace must hold
+ *     dllm_step_workspace_size(B, L, V + 8192 * (n_shards - 1)) bytes.
+ *   - DLLM_ERR_INVAL for a shard list that does not tile [0, V) in order or
+ *     a NULL shard, DLLM_ERR_ALIGN as dllm_step per shard, and every error
+ *     of dllm_step. */
+#define DLLM_MAX_VOCAB_SHARDS 8
+typedef struct dllm_vocab_shard {
+    const uint16_t* logits;   /* device [B*L][ldv] */
+    int64_t ldv;              /* row stride in elements */
+    int32_t v0;               /* first global token of the shard */
+    int32_t V;                /* tokens in the shard (>= 1) */
+} dllm_vocab_shard;
+
+int dllm_step_vocab_shards(const dllm_step_args* args, int32_t n_shards, const dllm_vocab_shard* shards,
+                           const int32_t* quota, void* stream);
 
 /* Host.  The fixed-steps quota of step s (0-based) of a block (BlockServe
  * page, section II-E): L spread evenly over S steps, floor(L / S) per step

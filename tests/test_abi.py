@@ -38,7 +38,7 @@ def test_library_exports_every_declared_function():
 def test_struct_sizes_match_binding():
     lib = dllm.load()
     for which, cls in enumerate((dllm.StepArgs, dllm.PackArgs, dllm.CompactArgs, dllm.AdvanceArgs, dllm.RefillArgs,
-                                 dllm.LoopConfig, dllm.LoopInfo)):
+                                 dllm.LoopConfig, dllm.LoopInfo, dllm.VocabShard)):
         assert lib.dllm_struct_size(which) == ctypes.sizeof(cls)
     assert lib.dllm_struct_size(99) == 0
 
@@ -280,3 +280,26 @@ def test_step_commit_argument_checks():
     ca_bad = dllm.CompactArgs(A=3, n_arrays=0, A_out=0xd0000)
     assert lib.dllm_step_commit(ctypes.byref(sa), None, -1, ctypes.byref(dllm.AdvanceArgs(**ok)), ctypes.byref(ca_bad),
                                 None) == -1
+
+
+def test_vocab_shards_argument_checks():
+    """dllm_step_vocab_shards rejects a shard list that does not tile [0, V)
+    in order, NULL or misaligned shards, before any CUDA call."""
+    lib = dllm.load()
+    a = _args(V=40, ldv=0, logits=None)
+
+    def call(specs, n=None):
+        arr = (dllm.VocabShard * max(len(specs), 1))()
+        for k, (ptr, ldv, v0, V) in enumerate(specs):
+            arr[k] = dllm.VocabShard(logits=ptr, ldv=ldv, v0=v0, V=V)
+        return lib.dllm_step_vocab_shards(ctypes.byref(a), len(specs) if n is None else n, arr, None, None)
+
+    ok = [(0x10000, 16, 0, 16), (0x20000, 24, 16, 24)]
+    assert call(ok[:1] + [(0x20000, 24, 17, 24)]) == -1          # gap between shards
+    assert call([(0x10000, 16, 0, 16), (0x20000, 24, 16, 20)]) == -1   # widths do not add up to V
+    assert call([(None, 16, 0, 16), ok[1]]) == -1                 # NULL shard
+    assert call([(0x10000, 8, 0, 16), ok[1]]) == -1               # row stride below the width
+    assert call([(0x10000, 16, 0, 0), (0x20000, 40, 0, 40)]) == -1   # empty shard
+    assert call(ok, n=0) == -1 and call(ok, n=9) == -1
+    assert call([(0x10008, 16, 0, 16), ok[1]]) == -2              # misaligned shard
+    assert call([(0x10000, 20, 0, 16), ok[1]]) == -2              # stride not a multiple of 8

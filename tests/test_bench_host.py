@@ -17,14 +17,14 @@ def test_algorithmic_bytes_dream():
     assert bench.algorithmic_bytes(cfg, 1851) == 562537344
 
 
-@pytest.mark.parametrize("B,L,shards,expected", [(128, 32, None, 3), (512, 64, None, 5), (128, 32, 4, 7),
+@pytest.mark.parametrize("B,L,shards,expected", [(128, 32, None, 3), (512, 64, None, 5), (128, 32, 4, 3),
                                                  (3000, 8, None, 5)])
 def test_launches_per_step(B, L, shards, expected):
     import bench
     pipe = types.SimpleNamespace(B=B, shards=list(range(shards)) if shards else None,
                                  rb_arr=[L * 4, L * 4, 4, 4, 4, 4, 4])
-    # pack + the step (or each shard and the merge) + commit/compaction (one
-    # launch while the rows fit the fused kernel's staging, else three)
+    # pack + the step (all vocabulary shards in one launch) + commit/compaction
+    # (one launch while the rows fit the fused kernel's staging, else three)
     assert bench.Pipeline.launches_per_step(pipe) == expected
     # with the commit inside the step's launch: pack + one launch
     pipe.fused = True

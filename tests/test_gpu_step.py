@@ -441,3 +441,89 @@ def test_pipeline_captured_in_a_cuda_graph(dllm, device):
         results.append((pipe.state[0].cpu().numpy(), pipe.done[0].cpu().numpy(), pipe.box_ids.cpu().numpy()))
     for a, b2 in zip(results[0], results[1]):
         np.testing.assert_array_equal(a, b2)
+
+
+def _bits(a):
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+@pytest.mark.parametrize("name,bounds", [("ragged", [0, 16000, 40001]), ("l64", [0, 8, 4096, 20000, 33000]),
+                                         ("all_masked", [0, 20000]), ("tiny", [0, 512, 1024])])
+def test_vocab_shards_in_one_launch(dllm, device, name, bounds):
+    """dllm_step_vocab_shards over views of one logits array: bit for bit the
+    per-shard launches plus the merge, and the oracle within tolerance."""
+    cfg = SMALL_CASES[name] if name in SMALL_CASES else synth.STEP_CONFIGS[name]
+    inp = synth.make_step_state(cfg, 13)
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    logits = device_logits(inp, device)
+    ids_a, thr, cs_a = device_state(inp, device)
+    multi = dllm.step_sharded(logits, ids_a, thr, cs_a, V=cfg.V, mask_id=cfg.mask_id, bounds=bounds, debug=True)
+    ids_b, _, cs_b = device_state(inp, device)
+    # each shard a column slice of the one array: its first column at v0, the array's row stride
+    shards = [(logits[:, v0:v1], v0, v1 - v0) for v0, v1 in zip(bounds[:-1], bounds[1:])]
+    out = dllm.step_vocab_shards(shards, ids_b, thr, cs_b, mask_id=cfg.mask_id, debug=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    want = {k: v.cpu().numpy() for k, v in multi.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids_b.cpu().numpy(), cs_b.cpu().numpy())
+    m = inp.masked
+    for k in ("tok", "conf", "lse"):
+        assert np.array_equal(_bits(got[k][m]), _bits(want[k][m])), k
+    for k in ("done", "accept_len", "n_new", "feats"):
+        assert np.array_equal(_bits(got[k]), _bits(want[k])), k
+    assert np.array_equal(ids_b.cpu().numpy(), ids_a.cpu().numpy())
+    assert np.array_equal(_bits(cs_b.cpu().numpy()), _bits(cs_a.cpu().numpy()))
+
+
+@pytest.mark.parametrize("widths", [[40001], [5, 40000 - 5 - 3, 3, 1], [5000] * 7 + [5001], [2047, 2049, 35905]])
+@pytest.mark.parametrize("fixed_steps", [False, True])
+def test_vocab_shards_in_separate_buffers(dllm, device, widths, fixed_steps):
+    """Shards in buffers of their own, of any width (a shard narrower than one
+    2048-element batch, one of a single token, eight shards), each with its
+    own row stride: equal to the oracle under either selection rule."""
+    import torch
+    cfg = SMALL_CASES["ragged"]
+    assert sum(widths) == cfg.V
+    inp = synth.make_step_state(cfg, 21)
+    quota = None
+    if fixed_steps:
+        quota = np.random.default_rng(22).integers(0, cfg.L + 1, size=cfg.B).astype(np.int32)
+    enforce_margins(inp, quota=quota)
+    ref = oracle_step(inp, quota=quota)
+    full = device_logits(inp, device)
+    shards, v0 = [], 0
+    for w in widths:
+        ldv = -(-w // 8) * 8 + 8                       # a stride of its own, wider than the shard
+        t = torch.full((cfg.B * cfg.L, ldv), -1, dtype=torch.int16, device=device)
+        t[:, :w] = full[:, v0:v0 + w]
+        shards.append((t, v0, w))
+        v0 += w
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step_vocab_shards(shards, ids, thr, cs, mask_id=cfg.mask_id, debug=True,
+                                 quota=None if quota is None else torch.from_numpy(quota).to(device))
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
+
+
+def test_vocab_shards_in_one_launch_dream_full_size(dllm, device):
+    """The Dream-shaped batch over four shards of a tensor-parallel LM head
+    in one launch: every request against the oracle."""
+    cfg = synth.STEP_CONFIGS["dream"]
+    inp = synth.make_step_state(cfg, 15)
+    enforce_margins(inp)
+    ref = oracle_step(inp)
+    logits = device_logits(inp, device)
+    bounds = [0, 37984, 75968, 113952, cfg.V]
+    import torch
+    shards = []
+    for v0, v1 in zip(bounds[:-1], bounds[1:]):
+        t = torch.empty((cfg.B * cfg.L, -(-(v1 - v0) // 8) * 8), dtype=torch.int16, device=device)
+        t[:, :v1 - v0] = logits[:, v0:v1]
+        shards.append((t, v0, v1 - v0))
+    ids, thr, cs = device_state(inp, device)
+    out = dllm.step_vocab_shards(shards, ids, thr, cs, mask_id=cfg.mask_id, debug=True)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert dllm.get_device_error(device) == 0
+    compare_step(ref, got, list(range(cfg.B)), cfg.L, ids.cpu().numpy(), cs.cpu().numpy())
