@@ -531,6 +531,11 @@ __device__ __forceinline__ void warp_features(const float (&val)[NK], const bool
 // rows at entry (then every one of them has its row results in the
 // workspace).
 // ---------------------------------------------------------------------------
+// Set once a warp of this CTA has seen every CTA's scan signal (with a
+// gpu-scope acquire); later finalisations in the CTA read it with a CTA-scope
+// acquire instead, which does not hold back their stores.
+__shared__ int s_all_scanned;
+
 template <int NK>
 __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool has_masked, int lane, bool direct) {
     // Row results arrive as zero-at-rest words (polled until they land);
@@ -564,8 +569,17 @@ __device__ __noinline__ void finalize_request_t(const StepParams& P, int b, bool
         c_r = P.c_rid[b];
     }
     // the scan count guards only the commit at the end: loaded after the
-    // block's loads so that its acquire does not hold them back
-    const int scanned = (lane == 0 && (has_masked || P.commit) && !direct) ? ld_acquire_gpu(P.ctl) : 0;
+    // block's loads so that its acquire does not hold them back, and only
+    // until the CTA has seen it complete
+    int scanned = 0;
+    if (lane == 0 && (has_masked || P.commit) && !direct) {
+        if (ld_acquire_cta_shared(&s_all_scanned)) {
+            scanned = (int)gridDim.x;
+        } else {
+            scanned = ld_acquire_gpu(P.ctl);
+            if (scanned == (int)gridDim.x) st_release_cta_shared(&s_all_scanned, 1);
+        }
+    }
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
         const int j = lane + 32 * k;
@@ -940,12 +954,21 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     uint16_t* s_gmask = reinterpret_cast<uint16_t*>(s_zero + P.zero_cap);   // masked bits, 16 positions each
     __shared__ int s_wsum[kWarpsTotal];
     __shared__ int s_nzero, s_qtail, s_qhead, s_ndone, s_last, s_next, s_ring_busy;
+    // The row finishers, request finalisation and the exit read many launch
+    // parameters once each, late in the launch, when the constant cache no
+    // longer holds them: they read this copy instead.
+    __shared__ __align__(16) StepParams s_P;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = gridDim.x, cta = blockIdx.x;
+    static_assert(sizeof(StepParams) % 4 == 0, "copied as words");
+    for (int i = tid; i < (int)(sizeof(StepParams) / 4); i += kThreads)
+        reinterpret_cast<int*>(&s_P)[i] = reinterpret_cast<const int*>(&P)[i];
+    const StepParams& FP = s_P;
 
     if (tid < kStreamWarps * kStages) mbar_init(smem_addr(&bars[tid]), 1);
     if (tid == 0) {
+        s_all_scanned = 0;
         s_next = 0;
         s_ring_busy = 0;
         s_nzero = 0;
@@ -1322,7 +1345,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             __threadfence_block();
             atomicAdd(&s_ndone, 1);
         }
-        drain_queue(P, s_gmask, s_queue, &s_qhead, &s_ndone, lane);   // help with the backlog
+        drain_queue(FP, s_gmask, s_queue, &s_qhead, &s_ndone, lane);   // help with the backlog
     } else {
         // ---- finisher warps: scan signal, requests without masked rows, queue
         if (warp == kFirstFinisher && lane == 0) {
@@ -1331,50 +1354,50 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
         if (!P.shard)
             for (int k = warp - kFirstFinisher; k < s_nzero; k += kFinishWarps)
-                finalize_request(P, s_zero[k], false, lane);
-        drain_queue(P, s_gmask, s_queue, &s_qhead, &s_ndone, lane);
+                finalize_request(FP, s_zero[k], false, lane);
+        drain_queue(FP, s_gmask, s_queue, &s_qhead, &s_ndone, lane);
     }
 
     // ---- exit: the last CTA commits deferred requests and resets ----------
     __syncthreads();
     if (tid == 0) {
-        const unsigned old = (unsigned)atom_add_acqrel_gpu(P.ctl + 1, 1);
+        const unsigned old = (unsigned)atom_add_acqrel_gpu(FP.ctl + 1, 1);
         s_last = ((int)(old & 0xffffu) == G - 1) ? 1 + (int)(old >> 16) : 0;   // 1 + deferred commits
     }
     // the fused commit's element map depends on launch parameters only:
     // every CTA builds it in its idle rings while the exit add is in flight
-    if (P.commit && !s_ring_busy)
-        compact_map<kThreads>(P.cp, *reinterpret_cast<CompactScratch<kThreads>*>(smem), tid);
+    if (FP.commit && !s_ring_busy)
+        compact_map<kThreads>(FP.cp, *reinterpret_cast<CompactScratch<kThreads>*>(smem), tid);
     __syncthreads();
     if (s_last) {
         const int n_def = s_last - 1;
-        const int* list = P.cnt + P.BL + P.B;
+        const int* list = FP.cnt + FP.BL + FP.B;
         for (int i = tid; i < n_def; i += kThreads) {   // finalized before every CTA had scanned
             const int e = __ldcg(list + i);
             const int b = e & 0xffff;
             const bool rst = (e & kDeferReset) != 0;
-            for (int j = 0; j < P.L; ++j) {
-                const long long idx = (long long)b * P.L + j;
-                if (rst) P.ids[idx] = P.mask_id;
-                else if (P.sel[idx]) P.ids[idx] = __ldcg(P.row_tok + idx);
+            for (int j = 0; j < FP.L; ++j) {
+                const long long idx = (long long)b * FP.L + j;
+                if (rst) FP.ids[idx] = FP.mask_id;
+                else if (FP.sel[idx]) FP.ids[idx] = __ldcg(FP.row_tok + idx);
             }
         }
-        if (P.commit) {
+        if (FP.commit) {
             // every request is committed: compact the caller's row arrays by
             // the eviction flags, staged through the (now idle) copy rings
             __syncthreads();
             if (s_ring_busy) {
-                if (tid == 0) set_error(P.err, DLLM_DEVERR_TIMEOUT);
+                if (tid == 0) set_error(FP.err, DLLM_DEVERR_TIMEOUT);
             } else {
                 auto& scratch = *reinterpret_cast<CompactScratch<kThreads>*>(smem);
                 unsigned char* stage = smem + kCommitScratchBytes;
-                compact_rows<kThreads>(P.cp, scratch, stage, P.c_evict, P.B, tid);
+                compact_rows<kThreads>(FP.cp, scratch, stage, FP.c_evict, FP.B, tid);
             }
         }
         if (tid == 0) {
-            P.ctl[0] = 0;
-            P.ctl[1] = 0;
-            P.ctl[2] = 0;
+            FP.ctl[0] = 0;
+            FP.ctl[1] = 0;
+            FP.ctl[2] = 0;
         }
     }
 }
