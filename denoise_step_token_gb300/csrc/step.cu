@@ -941,6 +941,62 @@ __device__ __forceinline__ void drain_queue(const StepParams& P, const uint16_t*
 }
 
 // ---------------------------------------------------------------------------
+// A CTA's pool of n units (chunks u_first .. u_first + n - 1) in groups: up to
+// kGroup consecutive chunks of one row, except the last `single` units, which
+// go one at a time so that the warps finish together.  Groups are numbered in
+// unit order, so a warp takes the next group with one fetch-and-add on a
+// counter (a compare-and-swap loop over units costs every warp a round trip
+// per lost race, and all of a CTA's warps start their first grab together).
+// ---------------------------------------------------------------------------
+struct PoolGroups {
+    int n, z;       // pool size; units [0, z) go in groups of up to kGroup
+    int a0, ga0;    // units in [0, z) of the first row, and their groups
+    int f, gpr;     // whole rows after it in [0, z), groups per whole row
+    int p, gp;      // units of the last row in [0, z), and their groups
+};
+
+__device__ __forceinline__ PoolGroups make_pool_groups(int u_first, int n, int NC, const FastDiv& div_nc,
+                                                       int single) {
+    PoolGroups q;
+    q.n = n;
+    q.z = max(0, n - single);
+    const int lead = (fast_div(u_first, div_nc) + 1) * NC - u_first;   // units up to the first row's end
+    q.a0 = min(q.z, lead);
+    q.ga0 = (q.a0 + kGroup - 1) / kGroup;
+    q.gpr = (NC + kGroup - 1) / kGroup;
+    q.f = (q.z - q.a0) / NC;
+    q.p = q.z - q.a0 - q.f * NC;
+    q.gp = (q.p + kGroup - 1) / kGroup;
+    return q;
+}
+
+// Group g of the pool: its first unit (relative to u_first) and size, or -1.
+__device__ __forceinline__ int pool_group(const PoolGroups& q, int g, int NC, int& size) {
+    if (g < q.ga0) {
+        size = min(kGroup, q.a0 - g * kGroup);
+        return g * kGroup;
+    }
+    g -= q.ga0;
+    if (g < q.f * q.gpr) {
+        const int r = g / q.gpr, j = g - r * q.gpr;
+        size = min(kGroup, NC - j * kGroup);
+        return q.a0 + r * NC + j * kGroup;
+    }
+    g -= q.f * q.gpr;
+    if (g < q.gp) {
+        size = min(kGroup, q.p - g * kGroup);
+        return q.a0 + q.f * NC + g * kGroup;
+    }
+    g -= q.gp;
+    if (g < q.n - q.z) {
+        size = 1;
+        return q.z + g;
+    }
+    size = 0;
+    return -1;
+}
+
+// ---------------------------------------------------------------------------
 // The step kernel: kStreamWarps streaming warps and kFinishWarps finisher
 // warps per CTA.
 // ---------------------------------------------------------------------------
@@ -1118,8 +1174,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (warp < kStreamWarps) {
         // ---- S2: stream groups of chunks through this warp's ring ----------
         // A group is up to kGroup consecutive chunks of one row, taken from
-        // the CTA's pool; near the end of the pool groups shrink to one chunk
-        // so that the warps finish together.  Each chunk keeps its own
+        // the CTA's pool (PoolGroups); near the end of the pool groups shrink
+        // to one chunk so that the warps finish together.  Each chunk keeps its own
         // partial (the reduction order depends only on V); the group's
         // partials are reduced across the warp together and published with
         // one add on the row counter.
@@ -1127,6 +1183,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const uint32_t bar0 = smem_addr(&bars[warp * kStages]);
         const uint64_t pol = l2_policy_evict_first();
         const int tail_units = 2 * kStreamWarps;   // single-chunk grabs below this many left
+        const PoolGroups pool = make_pool_groups(u_first, n_units, NC, P.div_nc, tail_units);
 
         // Take the next group: returns its first unit (or -1) and its size.
         // Once the CTA's pool is spent, units come one at a time from the
@@ -1138,22 +1195,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         auto grab = [&](int& k) -> int {
             int got = -1, kk = 0;
             if (lane == 0) {
-                int cur = *reinterpret_cast<volatile int*>(&s_next);
-                while (cur < n_units) {
-                    const int gu = u_first + cur;
-                    const int row_end = (fast_div(gu, P.div_nc) + 1) * NC - u_first;   // first unit of the next row
-                    const int left = n_units - cur;
-                    int want = left > tail_units ? kGroup : 1;
-                    want = min(want, min(row_end - cur, left));
-                    const int old = atomicCAS(&s_next, cur, cur + want);
-                    if (old == cur) {
-                        got = gu;
-                        kk = want;
-                        if (n_tail > 0 && t_ahead < 0 && left - want <= tail_units)
-                            t_ahead = atomicAdd(P.ctl + 2, 1);
-                        break;
-                    }
-                    cur = old;
+                int want;
+                const int st = pool_group(pool, atomicAdd(&s_next, 1), NC, want);
+                if (st >= 0) {
+                    got = u_first + st;
+                    kk = want;
+                    // the pool is nearly spent: draw the first tail ticket now
+                    if (n_tail > 0 && t_ahead < 0 && st + want >= pool.z) t_ahead = atomicAdd(P.ctl + 2, 1);
                 }
                 if (got < 0 && n_tail > 0) {
                     const int t = (t_ahead >= 0) ? t_ahead : atomicAdd(P.ctl + 2, 1);
