@@ -328,7 +328,7 @@ class Pipeline:
             for k in range(n):
                 self.shards[k] = dllm.VocabShard(logits=ctypes.c_void_p(self.logits.data_ptr() + bounds[k] * 2),
                                                  ldv=self.logits.shape[1], v0=bounds[k], V=bounds[k + 1] - bounds[k])
-        self.fused = self.shards is None   # the vocabulary-sharded step keeps its separate commit
+        self.fused = True   # the step, block commit and compaction in one launch
         self.quota = None
         if fixed_steps is not None:
             steps = L - inp.masked.sum(axis=1)
@@ -402,10 +402,18 @@ class Pipeline:
             raise RuntimeError("a dllm call failed inside the timed loop")
 
     def launch_step_commit(self, slot, stream, compact=None):
-        """The step with its block commit and compaction (dllm_step_commit)
-        on state slot ``slot``; returns the status code."""
+        """The step with its block commit and compaction (dllm_step_commit,
+        or dllm_step_vocab_shards_commit over vocabulary shards) on state
+        slot ``slot``; returns the status code."""
         pa, sa, aa, ca = self.args[slot]
         quota = self.quota_ptr if self.quota is not None else None
+        if self.shards is not None and compact is None:
+            saved = sa.logits
+            sa.logits = None
+            rc = self.lib.dllm_step_vocab_shards_commit(ctypes.byref(sa), len(self.shards), self.shards, quota,
+                                                        ctypes.byref(aa), ctypes.byref(ca), stream)
+            sa.logits = saved
+            return rc
         if compact is None:
             return self.lib.dllm_step_commit(ctypes.byref(sa), quota, -1, ctypes.byref(aa), ctypes.byref(ca), stream)
         buf, rows = compact
@@ -1093,7 +1101,8 @@ def main():
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,
                          "all_rows_logits_bytes_per_launch": cfg.B * cfg.L * cfg.V * 2,
-                         "kernel": ("step_kernel over 4 vocabulary shards (dllm_step_vocab_shards)" if pipe.shards else
+                         "kernel": ("step_kernel over 4 vocabulary shards with the fused commit (dllm_step_vocab_shards_commit)"
+                                    if pipe.shards else
                                     "step_kernel with the fused commit (dllm_step_commit" +
                                     (", fixed-steps quota)" if fixed else ")")),
                          "algorithmic_bytes_per_launch": alg,

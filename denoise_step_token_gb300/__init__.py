@@ -147,6 +147,9 @@ _SIGNATURES = {
     "dllm_advance_compact": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), ctypes.POINTER(CompactArgs), _p]),
     "dllm_step_commit": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p, ctypes.c_int64, ctypes.POINTER(AdvanceArgs),
                                         ctypes.POINTER(CompactArgs), _p]),
+    "dllm_step_vocab_shards_commit": (ctypes.c_int, [ctypes.POINTER(StepArgs), ctypes.c_int32,
+                                                     ctypes.POINTER(VocabShard), _p, ctypes.POINTER(AdvanceArgs),
+                                                     ctypes.POINTER(CompactArgs), _p]),
     "dllm_advance": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), _p]),
     "dllm_compact_workspace_size": (_sz, [_i32, _i32, _p]),
     "dllm_compact": (ctypes.c_int, [ctypes.POINTER(CompactArgs), _p]),

@@ -1713,6 +1713,35 @@ int launch_step(const dllm_step_args* a, const int32_t* quota, long long logits_
     return launch_prepared(sl, stream);
 }
 
+// The fused commit's arguments against the step's: the same rows, block
+// length, mask id, input_ids and conf_state, and the step's done flags as
+// the advance flags.
+int check_commit(const dllm_step_args* a, const dllm_advance_args* adv, const dllm_compact_args* cmp) {
+    if (!a || !adv || !cmp) return DLLM_ERR_INVAL;
+    if (adv->A != a->B || cmp->A != a->B || adv->L != a->L || adv->mask_id != a->mask_id) return DLLM_ERR_INVAL;
+    if (adv->input_ids != a->input_ids || adv->conf_state != a->conf_state) return DLLM_ERR_INVAL;
+    if (adv->advance && adv->advance != a->done) return DLLM_ERR_INVAL;   // the step's done flags advance
+    if (a->B > 0 && (!adv->rid || !adv->K || !adv->b || !adv->gen_tokens || !adv->evict || adv->ld_gen < 0))
+        return DLLM_ERR_INVAL;
+    return DLLM_OK;
+}
+
+// A shard table: 1..DLLM_MAX_VOCAB_SHARDS shards tiling [0, V) in order,
+// each row at least its shard wide, 16-byte rows.
+int check_shards(const dllm_step_args* a, int32_t n_shards, const dllm_vocab_shard* shards) {
+    if (!a || !shards || n_shards < 1 || n_shards > DLLM_MAX_VOCAB_SHARDS) return DLLM_ERR_INVAL;
+    long long next = 0;
+    for (int k = 0; k < n_shards; ++k) {
+        const dllm_vocab_shard& sh = shards[k];
+        if (!sh.logits || sh.V < 1 || sh.v0 != next || sh.ldv < sh.V) return DLLM_ERR_INVAL;
+        next += sh.V;
+    }
+    if (next != a->V) return DLLM_ERR_INVAL;
+    for (int k = 0; k < n_shards; ++k)
+        if (shards[k].ldv % 8 != 0 || (reinterpret_cast<uintptr_t>(shards[k].logits) & 15u) != 0) return DLLM_ERR_ALIGN;
+    return DLLM_OK;
+}
+
 }  // namespace
 }  // namespace dllm
 
@@ -1730,30 +1759,31 @@ extern "C" int dllm_step_compact(const dllm_step_args* a, int64_t logits_rows, c
 
 extern "C" int dllm_step_commit(const dllm_step_args* a, const int32_t* quota, int64_t logits_rows,
                                 const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream) {
-    if (!a || !adv || !cmp) return DLLM_ERR_INVAL;
-    if (adv->A != a->B || cmp->A != a->B || adv->L != a->L || adv->mask_id != a->mask_id) return DLLM_ERR_INVAL;
-    if (adv->input_ids != a->input_ids || adv->conf_state != a->conf_state) return DLLM_ERR_INVAL;
-    if (adv->advance && adv->advance != a->done) return DLLM_ERR_INVAL;   // the step's done flags advance
-    if (a->B > 0 && (!adv->rid || !adv->K || !adv->b || !adv->gen_tokens || !adv->evict || adv->ld_gen < 0))
-        return DLLM_ERR_INVAL;
+    const int rc = check_commit(a, adv, cmp);
+    if (rc != DLLM_OK) return rc;
     const CommitSpec commit{adv, cmp};
     return launch_step(a, quota, logits_rows < 0 ? -1 : logits_rows, nullptr, stream, &commit);
 }
 
 extern "C" int dllm_step_vocab_shards(const dllm_step_args* a, int32_t n_shards, const dllm_vocab_shard* shards,
                                       const int32_t* quota, void* stream) {
-    if (!a || !shards || n_shards < 1 || n_shards > DLLM_MAX_VOCAB_SHARDS) return DLLM_ERR_INVAL;
-    long long next = 0;
-    for (int k = 0; k < n_shards; ++k) {
-        const dllm_vocab_shard& sh = shards[k];
-        if (!sh.logits || sh.V < 1 || sh.v0 != next || sh.ldv < sh.V) return DLLM_ERR_INVAL;
-        next += sh.V;
-    }
-    if (next != a->V) return DLLM_ERR_INVAL;
-    for (int k = 0; k < n_shards; ++k)
-        if (shards[k].ldv % 8 != 0 || (reinterpret_cast<uintptr_t>(shards[k].logits) & 15u) != 0) return DLLM_ERR_ALIGN;
+    const int rc = check_shards(a, n_shards, shards);
+    if (rc != DLLM_OK) return rc;
     const ShardTable vs{n_shards, shards};
     return launch_step(a, quota, -1, nullptr, stream, nullptr, &vs);
+}
+
+extern "C" int dllm_step_vocab_shards_commit(const dllm_step_args* a, int32_t n_shards,
+                                             const dllm_vocab_shard* shards, const int32_t* quota,
+                                             const dllm_advance_args* adv, const dllm_compact_args* cmp,
+                                             void* stream) {
+    int rc = check_shards(a, n_shards, shards);
+    if (rc != DLLM_OK) return rc;
+    rc = check_commit(a, adv, cmp);
+    if (rc != DLLM_OK) return rc;
+    const ShardTable vs{n_shards, shards};
+    const CommitSpec commit{adv, cmp};
+    return launch_step(a, quota, -1, nullptr, stream, &commit, &vs);
 }
 
 extern "C" int dllm_step_shard(const dllm_step_args* a, int32_t v0, float* m, float* s, int32_t* idx, void* stream) {

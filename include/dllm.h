@@ -533,6 +533,22 @@ int dllm_advance_compact(const dllm_advance_args* adv, const dllm_compact_args* 
 int dllm_step_commit(const dllm_step_args* step, const int32_t* quota, int64_t logits_rows,
                      const dllm_advance_args* adv, const dllm_compact_args* cmp, void* stream);
 
+/* dllm_step_vocab_shards followed by the batch tail of dllm_step_commit, in
+ * one launch: the step over logits held as vocabulary shards on this device,
+ * then each finished request's block commit and the compaction of the
+ * listed row arrays (FDFO page, section "FDFO 的核心思想"; BlockServe page,
+ * Algorithm 1).  The results equal dllm_step_vocab_shards then
+ * dllm_advance_compact with the step's done flags as the advance flags.
+ *   - step, n_shards, shards, quota: as dllm_step_vocab_shards (the
+ *     workspace holds dllm_step_workspace_size(B, L, V + 8192 *
+ *     (n_shards - 1)) bytes; step->logits and step->ldv are not read).
+ *   - adv, cmp: as dllm_step_commit.
+ *   - Errors: those of dllm_step_vocab_shards, then those of
+ *     dllm_step_commit. */
+int dllm_step_vocab_shards_commit(const dllm_step_args* step, int32_t n_shards, const dllm_vocab_shard* shards,
+                                  const int32_t* quota, const dllm_advance_args* adv, const dllm_compact_args* cmp,
+                                  void* stream);
+
 /* Workspace bytes for dllm_compact over these arrays (0 if invalid). */
 size_t dllm_compact_workspace_size(int32_t A, int32_t n_arrays, const int64_t* row_bytes);
 

@@ -303,3 +303,29 @@ def test_vocab_shards_argument_checks():
     assert call(ok, n=0) == -1 and call(ok, n=9) == -1
     assert call([(0x10008, 16, 0, 16), ok[1]]) == -2              # misaligned shard
     assert call([(0x10000, 20, 0, 16), ok[1]]) == -2              # stride not a multiple of 8
+
+
+def test_vocab_shards_commit_argument_checks():
+    """dllm_step_vocab_shards_commit applies both sets of checks -- the shard
+    table's and the commit's -- before any CUDA call."""
+    lib = dllm.load()
+    sa = dllm.StepArgs(B=4, L=8, V=64, mask_id=63, ldv=0, logits=None, input_ids=0x20000, thr=0x30000,
+                       conf_state=0x40000, done=0x50000, accept_len=0x60000, n_new=0x70000, workspace=0x100000,
+                       workspace_bytes=1 << 20)
+    ok = dict(A=4, L=8, mask_id=63, advance=0x50000, rid=0x80000, K=0x90000, b=0xa0000, input_ids=0x20000,
+              conf_state=0x40000, gen_tokens=0xb0000, ld_gen=32, evict=0xc0000)
+    ca = dllm.CompactArgs(A=4, n_arrays=0, A_out=0xd0000)
+
+    def call(specs, adv=ok, cmp=ca):
+        arr = (dllm.VocabShard * len(specs))()
+        for k, (ptr, ldv, v0, V) in enumerate(specs):
+            arr[k] = dllm.VocabShard(logits=ptr, ldv=ldv, v0=v0, V=V)
+        return lib.dllm_step_vocab_shards_commit(ctypes.byref(sa), len(specs), arr, None,
+                                                 ctypes.byref(dllm.AdvanceArgs(**adv)), ctypes.byref(cmp), None)
+
+    good = [(0x10000, 32, 0, 32), (0x20000, 32, 32, 32)]
+    assert call([(0x10000, 32, 0, 32), (0x20000, 32, 33, 31)]) == -1           # shards do not tile [0, V)
+    assert call([(0x10008, 32, 0, 32), (0x20000, 32, 32, 32)]) == -2           # misaligned shard
+    assert call(good, adv=dict(ok, A=5)) == -1                                 # not the step's batch
+    assert call(good, adv=dict(ok, input_ids=0x20004)) == -1
+    assert call(good, cmp=dllm.CompactArgs(A=3, n_arrays=0, A_out=0xd0000)) == -1

@@ -68,7 +68,11 @@ def _expected(cfg, inp, rid, K, b, gen):
     return ref, dict(ids=ids, cs=cs, b=bb, gen=o_gen, evict=evict, new_index=new_index, src_row=src_row, A_out=A_out)
 
 
-def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=None):
+def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=None, bounds=None):
+    """One step with its commit and compaction on the device: in one launch
+    (fused) or as the step then dllm_advance_compact; over vocabulary shards
+    [bounds[k], bounds[k+1]) of the logits (column slices) when bounds is
+    given."""
     import torch
     lib = dllm.load()
     B, L = cfg.B, cfg.L
@@ -90,7 +94,9 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=Non
     new_index = torch.full((B,), -9, dtype=torch.int32, device=device)
     src_row = torch.full((B,), -9, dtype=torch.int32, device=device)
     A_out = torch.full((1,), -9, dtype=torch.int32, device=device)
-    ws = torch.zeros(lib.dllm_step_workspace_size(B, L, cfg.V), dtype=torch.uint8, device=device)
+    n_sh = 1 if bounds is None else len(bounds) - 1
+    ws = torch.zeros(lib.dllm_step_workspace_size(B, L, cfg.V + 8192 * (n_sh - 1)), dtype=torch.uint8,
+                     device=device)
     ptr = lambda x: ctypes.c_void_p(x.data_ptr())
     sa = dllm.StepArgs(B=B, L=L, V=cfg.V, mask_id=cfg.mask_id, ldv=logits.shape[1], logits=ptr(logits),
                        input_ids=ptr(ids), thr=ptr(thr), conf_state=ptr(cs), done=ptr(out["done"]),
@@ -115,7 +121,19 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=Non
                           src_row=ptr(src_row), A_out=ptr(A_out), arrays=arr, row_bytes=rbs, workspace=ptr(cws),
                           workspace_bytes=cws.numel())
     stream = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
-    if fused:
+    if bounds is not None:
+        shards = (dllm.VocabShard * n_sh)()
+        for k in range(n_sh):
+            shards[k] = dllm.VocabShard(logits=ctypes.c_void_p(logits.data_ptr() + 2 * bounds[k]),
+                                        ldv=logits.shape[1], v0=bounds[k], V=bounds[k + 1] - bounds[k])
+        if fused:
+            rc = lib.dllm_step_vocab_shards_commit(ctypes.byref(sa), n_sh, shards, None, ctypes.byref(aa),
+                                                   ctypes.byref(ca), stream)
+            assert rc == 0, lib.dllm_strerror(rc)
+        else:
+            assert lib.dllm_step_vocab_shards(ctypes.byref(sa), n_sh, shards, None, stream) == 0
+            assert lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream) == 0
+    elif fused:
         rc = lib.dllm_step_commit(ctypes.byref(sa), None, -1, ctypes.byref(aa), ctypes.byref(ca), stream)
         assert rc == 0, lib.dllm_strerror(rc)
     else:
@@ -133,13 +151,28 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=Non
 @pytest.mark.parametrize("name", sorted(CASES))
 @pytest.mark.parametrize("seed", [0, 1])
 def test_step_commit_matches_oracle_and_the_two_launch_path(dllm, device, name, seed):
+    _check_commit(dllm, device, name, seed, None)
+
+
+# vocabulary shards (multiples of 8 wide, but the last): one launch against
+# the oracle and against dllm_step_vocab_shards then dllm_advance_compact
+SHARD_BOUNDS = {"ragged": [0, 8, 20000, 40001], "dream_like": [0, 4096, 12000, 20000],
+                "l64": [0, 33000], "all_masked": [0, 4000, 9000], "many_rows": [0, 1024, 2048, 3000]}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_vocab_shards_commit_matches_oracle_and_the_two_launch_path(dllm, device, name):
+    _check_commit(dllm, device, name, 3, SHARD_BOUNDS[name])
+
+
+def _check_commit(dllm, device, name, seed, bounds):
     cfg = CASES[name]
     inp, rid, K, b, gen, ld_gen = _batch(cfg, seed)
     ref, exp = _expected(cfg, inp, rid, K, b, gen)
     extra = (np.random.default_rng(seed + 200).integers(0, 255, (cfg.B, 5)).astype(np.uint8)
              if name in WITH_BYTES else None)
-    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True, extra=extra)
-    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False, extra=extra)
+    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True, extra=extra, bounds=bounds)
+    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False, extra=extra, bounds=bounds)
     B, L = cfg.B, cfg.L
     # the step's own outputs against the oracle (its ids / conf_state are
     # checked after the commit below)
