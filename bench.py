@@ -849,6 +849,17 @@ def run_loop_bench(args, rank, world, local_rank):
     }
     assert on["iters"] == off["iters"] == py["iters"] and on["masked"] == off["masked"] == py["masked"]
     out["threshold_control"] = time_threshold_control(lcfg, seed=3000 + rank)
+    # the native loop choosing every step's thresholds itself (DiLaServe
+    # controller, an affine step-latency model near the measured iteration)
+    from denoise_step_token_gb300.control import ThresholdController
+    ctl = ThresholdController.affine([0.5, 0.6, 0.7, 0.8, 0.9], L=lcfg.L, slo_s=2.0, tokens_per_s=1.0e7,
+                                     latency_s=2.0e-4, latency_per_row_s=8.0e-7)
+    cc = serve_queue(lcfg, 2000 + rank, device, reloop=True, native=True, controller=ctl)
+    out["native_threshold_control"] = {
+        "value": cc["masked"] / cc["secs"], "timed_s": cc["secs"], "iterations": cc["iters"],
+        "ms_per_step": cc["secs"] * 1e3 / cc["iters"], "masked_positions": cc["masked"],
+        "mean_threshold": cc["mean_threshold"],
+        "controller": "candidates 0.5..0.9, SLO 2 s, 1e7 tokens/s, step latency 0.2 ms + 0.8 us per row"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
@@ -879,10 +890,11 @@ def time_threshold_control(lcfg, seed, A=256, reps=200):
             "mean_threshold": float(thr.mean()), "capped_requests": int((cap < 4).sum())}
 
 
-def serve_queue(lcfg, seed, device, reloop, native=True, pool_rows=4096):
+def serve_queue(lcfg, seed, device, reloop, native=True, pool_rows=4096, controller=None):
     """Serve one generated queue to completion, with libdllm's native loop
-    (two calls per iteration) or the Python DeviceLoop; returns the timed
-    seconds, iterations, masked positions and re-loops."""
+    (two calls per iteration) or the Python DeviceLoop, optionally under a
+    threshold controller; returns the timed seconds, iterations, masked
+    positions and re-loops."""
     import torch
     from denoise_step_token_gb300.loop import DeviceLoop, NativeLoop
     reqs = synth.make_loop_requests(lcfg, seed)
@@ -894,12 +906,13 @@ def serve_queue(lcfg, seed, device, reloop, native=True, pool_rows=4096):
     cls = NativeLoop if native else DeviceLoop
     loop = cls(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=L, V=V,
                mask_id=lcfg.mask_id, pad_id=lcfg.pad_id, budget=lcfg.budget, device=device, mode="fdfo",
-               reloop=reloop)
+               reloop=reloop, controller=controller)
     logits = torch.empty((lcfg.R * L, ldv), dtype=torch.int16, device=device)
     ev = []
     active = []
     masked_total = 0
     iters = 0
+    thr_sum, thr_n = 0.0, 0
     if native:
         while not loop.finished():
             # timed: admission, refill, pack (dllm_loop_begin)
@@ -920,8 +933,12 @@ def serve_queue(lcfg, seed, device, reloop, native=True, pool_rows=4096):
             ev.append(t_begin + time.perf_counter() - t1)
             iters += 1
             masked_total += len(rows)
+            if controller is not None and inf.A:
+                thr_sum += float(loop.thresholds().sum())
+                thr_n += inf.A
         return {"secs": sum(ev), "iters": iters, "masked": masked_total, "reloops": loop.info().reloops,
-                "mean_A": float(np.mean(active)) if active else 0.0}
+                "mean_A": float(np.mean(active)) if active else 0.0,
+                "mean_threshold": thr_sum / thr_n if thr_n else None}
     while not loop.finished():
         # timed: admission (host) and refill
         torch.cuda.synchronize()

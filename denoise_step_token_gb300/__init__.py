@@ -96,6 +96,12 @@ class LoopInfo(ctypes.Structure):
                 ("n_new", _p), ("accept_len", _p), ("feats", _p)]
 
 
+class LoopControl(ctypes.Structure):
+    _fields_ = [("T", _i32), ("pad0", _i32), ("candidates", _p), ("slo_s", ctypes.c_double),
+                ("tokens_per_s", ctypes.c_double), ("latency_s", ctypes.c_double),
+                ("latency_per_row_s", ctypes.c_double)]
+
+
 class RefillArgs(ctypes.Structure):
     _fields_ = [("A0", _i32), ("n", _i32), ("L", _i32), ("mask_id", _i32),
                 ("new_rid", _p), ("new_p", _p), ("new_K", _p), ("new_thr", _p),
@@ -144,6 +150,8 @@ _SIGNATURES = {
     "dllm_loop_end": (ctypes.c_int, [_p, _p, _i64, _p]),
     "dllm_loop_info": (ctypes.c_int, [_p, ctypes.POINTER(LoopInfo)]),
     "dllm_loop_rows": (ctypes.c_int, [_p, _p, _p, _p]),
+    "dllm_loop_set_control": (ctypes.c_int, [_p, ctypes.POINTER(LoopControl)]),
+    "dllm_loop_thresholds": (ctypes.c_int, [_p, _p, _p]),
     "dllm_advance_compact": (ctypes.c_int, [ctypes.POINTER(AdvanceArgs), ctypes.POINTER(CompactArgs), _p]),
     "dllm_step_commit": (ctypes.c_int, [ctypes.POINTER(StepArgs), _p, ctypes.c_int64, ctypes.POINTER(AdvanceArgs),
                                         ctypes.POINTER(CompactArgs), _p]),
@@ -190,7 +198,7 @@ def load(build=True):
         if lib.dllm_abi_version() != ABI_VERSION:
             raise RuntimeError(f"libdllm ABI version {lib.dllm_abi_version()}, binding expects {ABI_VERSION}")
         for which, cls in enumerate((StepArgs, PackArgs, CompactArgs, AdvanceArgs, RefillArgs, LoopConfig, LoopInfo,
-                                     VocabShard)):
+                                     VocabShard, LoopControl)):
             if lib.dllm_struct_size(which) != ctypes.sizeof(cls):
                 raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {lib.dllm_struct_size(which)} "
                                    f"bytes, binding {ctypes.sizeof(cls)}")

@@ -41,6 +41,17 @@ class ThresholdController:
         self.slo_s = float(slo_s)
         self.tokens_per_s = float(tokens_per_s)
         self.step_latency_s = step_latency_s
+        self.latency_affine = None   # (a, b) when step_latency_s is a + b * A
+
+    @classmethod
+    def affine(cls, candidates, *, L, slo_s, tokens_per_s, latency_s, latency_per_row_s):
+        """A controller whose step latency at A rows is latency_s +
+        latency_per_row_s * A -- the form the native loop evaluates itself
+        (``dllm_loop_set_control``)."""
+        a, b = float(latency_s), float(latency_per_row_s)
+        ctl = cls(candidates, L=L, slo_s=slo_s, tokens_per_s=tokens_per_s, step_latency_s=lambda A: a + b * A)
+        ctl.latency_affine = (a, b)
+        return ctl
 
     def choose(self, feats, masked, blocks_left, total_tokens, elapsed_s):
         """Thresholds (float32 [A]) for the active rows, in arrival order.

@@ -103,6 +103,7 @@ extern "C" size_t dllm_struct_size(int which) {
         case 5: return sizeof(dllm_loop_config);
         case 6: return sizeof(dllm_loop_info_t);
         case 7: return sizeof(dllm_vocab_shard);
+        case 8: return sizeof(dllm_loop_control);
         default: return 0;
     }
 }

@@ -20,11 +20,13 @@
 // per-iteration copies; every array the kernels read lives in the caller's
 // device workspace.
 
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
 #include <algorithm>
 #include <functional>
+#include <limits>
 #include <vector>
 
 #include "common.cuh"
@@ -45,8 +47,22 @@ struct dllm_loop {
     uint8_t* done_h = nullptr;
     int32_t* quota_h = nullptr;
     int32_t* stage_h = nullptr;   // [4][n]: rid, p, K, thr bits of the admitted requests
+    float* thr_p = nullptr;       // thresholds of the next step (upload)
+    float* feat_p = nullptr;      // [A][6] block features of the last step (readback)
     cudaEvent_t staged = nullptr;
     bool staged_pending = false;
+    // threshold control (DiLaServe review, section 3.2): the controller's
+    // host inputs per active row, the modelled clock and scratch
+    bool ctl_on = false;
+    std::vector<double> ctl_cand;
+    double ctl_slo = 0, ctl_tps = 0, ctl_lat0 = 0, ctl_lat1 = 0;
+    double now = 0;                   // modelled clock, seconds
+    std::vector<double> admit_h;      // admission time per active row
+    std::vector<float> feat_h;        // [A][6] last step's features per active row
+    std::vector<float> thr_used;      // thresholds of the rows the last step ran on
+    std::vector<int32_t> c_masked, c_left, c_cap, c_choice;
+    std::vector<int64_t> c_total;
+    std::vector<double> c_elapsed, c_steps;
     int32_t A = 0, W = 0, admitted_last = 0, iteration = 0, reloops = 0;
     int64_t cost = 0;
     bool in_place = false, have_box = false;
@@ -194,6 +210,34 @@ bool shapes(const dllm_loop_config* c, const int32_t* p, const int32_t* K, int32
     return true;
 }
 
+// The controller's thresholds for the A active rows into thr_used.
+int choose_thresholds(dllm_loop* lp, int32_t A) {
+    const int32_t L = lp->c.L, T = (int32_t)lp->ctl_cand.size();
+    lp->c_masked.resize(A);
+    lp->c_left.resize(A);
+    lp->c_total.resize(A);
+    lp->c_elapsed.resize(A);
+    lp->c_cap.resize(A);
+    lp->c_choice.resize(A);
+    lp->c_steps.resize((size_t)A * T);
+    for (int32_t i = 0; i < A; ++i) {
+        const float* f = &lp->feat_h[(size_t)i * DLLM_NUM_FEATURES];
+        const float frac = isnan(f[0]) ? 0.0f : f[5];
+        lp->c_masked[i] = L - (int32_t)rintf(frac * (float)L);
+        const int32_t r = lp->rid_h[i];
+        lp->c_left[i] = lp->K_all[r] - lp->b_h[i] - 1;
+        lp->c_total[i] = (int64_t)lp->p_all[r] + (int64_t)lp->K_all[r] * L;
+        lp->c_elapsed[i] = lp->now - lp->admit_h[i];
+    }
+    const double lat = lp->ctl_lat0 + lp->ctl_lat1 * A;
+    const int rc = dllm_threshold_control(A, T, lp->ctl_cand.data(), L, lp->feat_h.data(), lp->c_masked.data(),
+                                          lp->c_left.data(), lp->c_total.data(), lp->c_elapsed.data(), lp->ctl_slo,
+                                          lp->ctl_tps, lat, lp->c_steps.data(), lp->c_cap.data(), lp->c_choice.data());
+    if (rc != DLLM_OK) return rc;
+    for (int32_t i = 0; i < A; ++i) lp->thr_used[i] = (float)lp->ctl_cand[lp->c_choice[i]];
+    return DLLM_OK;
+}
+
 }  // namespace
 
 extern "C" size_t dllm_loop_workspace_size(const dllm_loop_config* c, const int32_t* p, const int32_t* K) {
@@ -236,7 +280,9 @@ extern "C" int dllm_loop_create(const dllm_loop_config* c, const int32_t* p, con
     lp->admit_idx.resize(std::max(c->R, 1));
     {
         const size_t cap = (size_t)c->capacity;
-        if (cudaHostAlloc(&lp->pinned, al256(cap) + al256(cap * 4) + cap * 16, cudaHostAllocDefault) != cudaSuccess ||
+        const size_t pinned_bytes = al256(cap) + al256(cap * 4) + al256(cap * 16) + al256(cap * 4) +
+                                    cap * DLLM_NUM_FEATURES * 4;
+        if (cudaHostAlloc(&lp->pinned, pinned_bytes, cudaHostAllocDefault) != cudaSuccess ||
             cudaEventCreateWithFlags(&lp->staged, cudaEventDisableTiming) != cudaSuccess) {
             cudaGetLastError();
             delete lp;
@@ -246,6 +292,8 @@ extern "C" int dllm_loop_create(const dllm_loop_config* c, const int32_t* p, con
         lp->done_h = h;
         lp->quota_h = reinterpret_cast<int32_t*>(h + al256(cap));
         lp->stage_h = reinterpret_cast<int32_t*>(h + al256(cap) + al256(cap * 4));
+        lp->thr_p = reinterpret_cast<float*>(h + al256(cap) + al256(cap * 4) + al256(cap * 16));
+        lp->feat_p = reinterpret_cast<float*>(h + al256(cap) + al256(cap * 4) + al256(cap * 16) + al256(cap * 4));
     }
     // the step workspace must start zeroed (its counters are zero at rest)
     const int rc = dllm_workspace_init(lp->step_ws, lp->step_ws_bytes, stream);
@@ -310,6 +358,9 @@ extern "C" int dllm_loop_begin(dllm_loop* lp, void* stream) {
                 lp->b_h.push_back(0);
                 lp->s_h.push_back(0);
                 lp->wait_h.push_back(0);
+                lp->admit_h.push_back(lp->now);
+                for (int j = 0; j < DLLM_NUM_FEATURES; ++j)
+                    lp->feat_h.push_back(std::numeric_limits<float>::quiet_NaN());
             }
             lp->A += n;
             lp->admitted_last = n;
@@ -345,6 +396,7 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
     cudaStream_t s = dllm::as_stream(stream);
     const int32_t A = lp->A;
     if (A == 0) {
+        lp->thr_used.clear();
         ++lp->iteration;
         return DLLM_OK;
     }
@@ -356,14 +408,28 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
     sa.n_new = lp->n_new; sa.feats = lp->feats; sa.workspace = lp->step_ws; sa.workspace_bytes = lp->step_ws_bytes;
     int rc;
     const int32_t* quota = nullptr;
-    if (c.S > 0) {
+    // the thresholds of this step: the controller's, else the requests' own
+    lp->thr_used.resize(A);
+    if (lp->ctl_on) {
+        rc = choose_thresholds(lp, A);
+        if (rc != DLLM_OK) return rc;
+    } else {
+        for (int32_t i = 0; i < A; ++i) lp->thr_used[i] = lp->thr_all[lp->rid_h[i]];
+    }
+    if (c.S > 0 || lp->ctl_on) {
         rc = staging_free(lp);
         if (rc != DLLM_OK) return rc;
-        for (int32_t i = 0; i < A; ++i) lp->quota_h[i] = dllm_transfer_quota(c.L, c.S, lp->s_h[i]);
-        DLLM_CUDA_TRY(cudaMemcpyAsync(lp->quota, lp->quota_h, (size_t)A * 4, cudaMemcpyHostToDevice, s));
+        if (c.S > 0) {
+            for (int32_t i = 0; i < A; ++i) lp->quota_h[i] = dllm_transfer_quota(c.L, c.S, lp->s_h[i]);
+            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->quota, lp->quota_h, (size_t)A * 4, cudaMemcpyHostToDevice, s));
+            quota = lp->quota;
+        }
+        if (lp->ctl_on) {
+            memcpy(lp->thr_p, lp->thr_used.data(), (size_t)A * 4);
+            DLLM_CUDA_TRY(cudaMemcpyAsync(lp->thr, lp->thr_p, (size_t)A * 4, cudaMemcpyHostToDevice, s));
+        }
         rc = staging_used(lp, s);
         if (rc != DLLM_OK) return rc;
-        quota = lp->quota;
     }
     // FDFO: every done row advances, so the commit and compaction run in
     // the step's own launch (the advance flags are the device's done flags;
@@ -378,10 +444,18 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
         rc = quota ? dllm_step_quota(&sa, quota, stream) : dllm_step(&sa, stream);
     }
     if (rc != DLLM_OK) return rc;
-    // the per-step readback: one byte per row
+    // the per-step readback: one byte per row (and the block features when
+    // the controller needs them)
     DLLM_CUDA_TRY(cudaMemcpyAsync(lp->done_h, lp->done, (size_t)A, cudaMemcpyDeviceToHost, s));
+    if (lp->ctl_on)
+        DLLM_CUDA_TRY(cudaMemcpyAsync(lp->feat_p, lp->feats, (size_t)A * DLLM_NUM_FEATURES * 4,
+                                      cudaMemcpyDeviceToHost, s));
     DLLM_CUDA_TRY(cudaStreamSynchronize(s));
     lp->staged_pending = false;
+    if (lp->ctl_on) {
+        memcpy(lp->feat_h.data(), lp->feat_p, (size_t)A * DLLM_NUM_FEATURES * 4);
+        lp->now += lp->ctl_lat0 + lp->ctl_lat1 * A;
+    }
     bool all_done = true, any_done = false;
     for (int32_t i = 0; i < A; ++i) {
         all_done = all_done && lp->done_h[i];
@@ -419,12 +493,18 @@ extern "C" int dllm_loop_end(dllm_loop* lp, const uint16_t* logits, int64_t ldv,
         lp->b_h[kept] = bi;
         lp->s_h[kept] = si;
         lp->wait_h[kept] = wi;
+        lp->admit_h[kept] = lp->admit_h[i];
+        for (int j = 0; j < DLLM_NUM_FEATURES; ++j)   // a fresh block has nothing unmasked yet
+            lp->feat_h[(size_t)kept * DLLM_NUM_FEATURES + j] =
+                adv ? std::numeric_limits<float>::quiet_NaN() : lp->feat_h[(size_t)i * DLLM_NUM_FEATURES + j];
         ++kept;
     }
     lp->rid_h.resize(kept);
     lp->b_h.resize(kept);
     lp->s_h.resize(kept);
     lp->wait_h.resize(kept);
+    lp->admit_h.resize(kept);
+    lp->feat_h.resize((size_t)kept * DLLM_NUM_FEATURES);
     lp->A = kept;
     return DLLM_OK;
 }
@@ -464,5 +544,34 @@ extern "C" int dllm_loop_rows(const dllm_loop* lp, int32_t* rid, int32_t* b, int
         if (b) b[i] = lp->b_h[i];
         if (s) s[i] = lp->s_h[i];
     }
+    return DLLM_OK;
+}
+
+extern "C" int dllm_loop_set_control(dllm_loop* lp, const dllm_loop_control* ctl) {
+    if (!lp) return DLLM_ERR_INVAL;
+    if (!ctl) {
+        lp->ctl_on = false;
+        return DLLM_OK;
+    }
+    if (ctl->T < 1 || !ctl->candidates || !(ctl->slo_s > 0) || !(ctl->tokens_per_s >= 0) || !(ctl->latency_s >= 0) ||
+        !(ctl->latency_per_row_s >= 0))
+        return DLLM_ERR_INVAL;
+    for (int32_t k = 0; k < ctl->T; ++k) {
+        if (!(ctl->candidates[k] == ctl->candidates[k])) return DLLM_ERR_INVAL;   // NaN
+        if (k > 0 && !(ctl->candidates[k] > ctl->candidates[k - 1])) return DLLM_ERR_INVAL;
+    }
+    lp->ctl_cand.assign(ctl->candidates, ctl->candidates + ctl->T);
+    lp->ctl_slo = ctl->slo_s;
+    lp->ctl_tps = ctl->tokens_per_s;
+    lp->ctl_lat0 = ctl->latency_s;
+    lp->ctl_lat1 = ctl->latency_per_row_s;
+    lp->ctl_on = true;
+    return DLLM_OK;
+}
+
+extern "C" int dllm_loop_thresholds(const dllm_loop* lp, float* thr, int32_t* n) {
+    if (!lp || !n) return DLLM_ERR_INVAL;
+    *n = (int32_t)lp->thr_used.size();
+    if (thr && !lp->thr_used.empty()) memcpy(thr, lp->thr_used.data(), lp->thr_used.size() * 4);
     return DLLM_OK;
 }

@@ -227,10 +227,13 @@ class NativeLoop:
     """The same loop driven by libdllm's native loop (dllm_loop_*): two
     calls per iteration, ``begin()`` before the model forward and
     ``end(logits)`` after it; all of the loop's device arrays live in one
-    workspace tensor.  ``mode``, ``reloop`` and ``S`` as for DeviceLoop."""
+    workspace tensor.  ``mode``, ``reloop`` and ``S`` as for DeviceLoop.
+    ``controller``: a ``control.ThresholdController`` built with
+    ``ThresholdController.affine``; the native loop then picks every step's
+    thresholds itself (``dllm_loop_set_control``)."""
 
     def __init__(self, p, K, prompt_off, prompt_tokens, thr, *, L, V, mask_id, pad_id, budget, device,
-                 mode="fdfo", reloop=False, S=None, capacity=None):
+                 mode="fdfo", reloop=False, S=None, capacity=None, controller=None):
         import ctypes
         import torch
         from . import LoopConfig, LoopInfo, _check, load
@@ -260,6 +263,15 @@ class NativeLoop:
             ctypes.byref(self.cfg), vp(p.ctypes.data), vp(K.ctypes.data), vp(thr.ctypes.data),
             vp(self.prompt_off.data_ptr()), vp(self.prompt_tokens.data_ptr()) if self.prompt_tokens.numel() else None,
             vp(self.ws.data_ptr()), need, self._stream, ctypes.byref(self.handle)))
+        if controller is not None:
+            if controller.latency_affine is None:
+                raise ValueError("the native loop needs an affine step latency (ThresholdController.affine)")
+            from . import LoopControl
+            self._cand = np.ascontiguousarray(controller.cand, dtype=np.float64)
+            a, b = controller.latency_affine
+            lc = LoopControl(T=self._cand.size, candidates=vp(self._cand.ctypes.data), slo_s=controller.slo_s,
+                             tokens_per_s=controller.tokens_per_s, latency_s=a, latency_per_row_s=b)
+            _check("dllm_loop_set_control", self.lib.dllm_loop_set_control(self.handle, ctypes.byref(lc)))
 
     def __del__(self):
         if getattr(self, "handle", None) and self.handle.value:
@@ -296,6 +308,15 @@ class NativeLoop:
                                                               vp(s.ctypes.data)))
         return rid[:A], b[:A], s[:A]
 
+    def thresholds(self):
+        """The thresholds the last ``end`` gave the rows it stepped (float32,
+        in their order at that step)."""
+        ctypes = self.ctypes
+        out = np.empty(max(self.cfg.capacity, 1), dtype=np.float32)
+        n = ctypes.c_int32(0)
+        self._check("dllm_loop_thresholds", self.lib.dllm_loop_thresholds(
+            self.handle, ctypes.c_void_p(out.ctypes.data), ctypes.byref(n)))
+        return out[: n.value].copy()
     def masked_rows(self):
         """(row * L + j, rid, b, s, j) of every masked position."""
         inf = self.info()

@@ -677,6 +677,42 @@ int dllm_loop_info(const dllm_loop* loop, dllm_loop_info_t* out);
  * in the current block (A entries each; any pointer may be NULL). */
 int dllm_loop_rows(const dllm_loop* loop, int32_t* rid, int32_t* b, int32_t* s);
 
+/* Per-request threshold control inside the native loop (DiLaServe review,
+ * section 3.2): before every step, dllm_threshold_control picks each active
+ * row's threshold from `candidates` and dllm_loop_end uploads them, in place
+ * of the requests' fixed thresholds; after the step the rows' block features
+ * are read back with the done flags.  The controller's inputs are kept as
+ * the Python loop keeps them:
+ *   - features: the row's last step's (all NaN for a row admitted since, or
+ *     whose block advanced: nothing unmasked yet); masked positions
+ *     L - rint(f[5] * L) in float32, L when f[0] is NaN;
+ *   - blocks left K - b - 1; total tokens p + K * L;
+ *   - time since admission on a modelled clock that advances, after every
+ *     step over A rows, by the step latency latency_s + latency_per_row_s * A
+ *     (the review's one-off latency profile, as an affine fit), which is
+ *     also the latency the controller is given.
+ * control: T >= 1 ascending candidates (host, copied), slo_s > 0,
+ * tokens_per_s >= 0, both latency terms >= 0; NULL turns the control off
+ * (fixed thresholds again).  Rows stepped before the call count as having
+ * no features.  Host only; DLLM_ERR_INVAL for a NULL loop or invalid
+ * control.  The fixed-steps rule (config S > 0) ignores thresholds. */
+typedef struct dllm_loop_control {
+    int32_t T;                  /* candidate thresholds */
+    const double* candidates;   /* host [T], ascending */
+    double slo_s;               /* every request's latency SLO, seconds */
+    double tokens_per_s;        /* the instance's rate: capacity = tokens_per_s * slo_s */
+    double latency_s;           /* step latency at A rows: latency_s + latency_per_row_s * A */
+    double latency_per_row_s;
+} dllm_loop_control;
+
+int dllm_loop_set_control(dllm_loop* loop, const dllm_loop_control* control);
+
+/* The thresholds the last dllm_loop_end gave the rows it stepped, in their
+ * order at that step (before the commit compacted them): *n entries into
+ * thr (host, room for the loop's capacity).  Without control they are the
+ * requests' own thresholds. */
+int dllm_loop_thresholds(const dllm_loop* loop, float* thr, int32_t* n);
+
 #ifdef __cplusplus
 }
 #endif

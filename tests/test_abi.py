@@ -329,3 +329,16 @@ def test_vocab_shards_commit_argument_checks():
     assert call(good, adv=dict(ok, A=5)) == -1                                 # not the step's batch
     assert call(good, adv=dict(ok, input_ids=0x20004)) == -1
     assert call(good, cmp=dllm.CompactArgs(A=3, n_arrays=0, A_out=0xd0000)) == -1
+
+
+def test_native_loop_control_argument_checks():
+    """dllm_loop_set_control / dllm_loop_thresholds reject a NULL loop (the
+    host checks; a loop itself needs a device)."""
+    lib = dllm.load()
+    cand = (ctypes.c_double * 3)(0.5, 0.7, 0.9)
+    lc = dllm.LoopControl(T=3, candidates=ctypes.cast(cand, ctypes.c_void_p), slo_s=1.0, tokens_per_s=1e5,
+                          latency_s=0.001, latency_per_row_s=0.0)
+    assert lib.dllm_loop_set_control(None, ctypes.byref(lc)) == -1
+    n = ctypes.c_int32(0)
+    assert lib.dllm_loop_thresholds(None, None, ctypes.byref(n)) == -1
+    assert ctypes.sizeof(dllm.LoopControl) == lib.dllm_struct_size(8)

@@ -371,3 +371,101 @@ def test_native_loop_blockserve_full_vocabulary(dllm, device):
     assert (cfg.R, cfg.L, cfg.V, cfg.budget) == (256, 32, 126464, 1 << 20)
     ol, nl = _lockstep_native(dllm, device, cfg, "fdfo", seed=2000, reloop=True, per_request=True)
     assert ol.iteration > 0 and nl.masked_total >= cfg.R * cfg.gen
+
+
+@pytest.mark.parametrize("mode,reloop", [("fdfo", False), ("fdfo", True), ("sync", False)])
+def test_native_loop_threshold_control_matches_the_python_loop(dllm, device, mode, reloop):
+    """The native loop's own threshold control (dllm_loop_set_control) and
+    DeviceLoop with the same controller, over the same queue and logits:
+    identical thresholds at every step, identical batches and generated
+    tokens, and the thresholds change over the run.  (DeviceLoop under the
+    controller is pinned to the oracle loop by the lockstep test above;
+    both loops call the same dllm_threshold_control, pinned to the oracle's
+    control functions on the CPU.)"""
+    import torch
+    from denoise_step_token_gb300.control import ThresholdController
+    from denoise_step_token_gb300.loop import DeviceLoop, NativeLoop
+    cfg = SMALL
+    seed = 17
+    reqs = synth.make_loop_requests(cfg, seed)
+
+    def controller():
+        return ThresholdController.affine([0.5, 0.6, 0.7, 0.8, 0.9], L=cfg.L, slo_s=0.05, tokens_per_s=2.0e5,
+                                          latency_s=0.0005, latency_per_row_s=0.00002)
+
+    common = dict(L=cfg.L, V=cfg.V, mask_id=cfg.mask_id, pad_id=cfg.pad_id, budget=cfg.budget, device=device,
+                  mode=mode, reloop=reloop)
+    gl = DeviceLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, controller=controller(), **common)
+    nl = NativeLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, controller=controller(), **common)
+    salts, used, it = {}, [], 0
+    while not gl.finished() and it < 5000:
+        assert not nl.finished()
+        new = gl.admit_phase()
+        inf = nl.begin()
+        assert inf.admitted_last == len(new), it
+        gl.pack_phase()
+        rid, b, _ = nl.rows()
+        assert rid.tolist() == gl.rid_h.tolist() and b.tolist() == gl.b_h.tolist(), it
+        rows = gl.masked_rows()
+        assert rows == nl.masked_rows(), it
+        A = gl.A
+        # both loops step on the GPU with the same kernel, so no decision margin is needed between them
+        thr_rows = np.array([reqs.thr[r] for r in gl.rid_h], dtype=np.float32)
+        logits = _loop_logits(seed, rows, A, cfg.L, cfg.V, cfg.offset_max, cfg.mask_id, thr_rows, salts,
+                              cfg.row_stride)
+        d = torch.from_numpy(logits[: max(A, 1) * cfg.L].view(np.int16)).to(device)
+        done, _ = gl.step_phase(d)
+        nl.end(d)
+        if A:
+            t_nat = nl.thresholds()
+            t_py = np.asarray(gl.thr_log[-1], dtype=np.float32)
+            assert np.array_equal(t_nat.view(np.uint32), t_py.view(np.uint32)), it
+            used.append(t_nat)
+        gl.finish_phase(done)
+        inf = nl.info()
+        assert inf.A == gl.A and inf.iteration == gl.iteration, it
+        it += 1
+    assert gl.finished() and nl.finished()
+    g_py, g_nat = gl.generated(), nl.generated()
+    for r in range(cfg.R):
+        n = reqs.K[r] * cfg.L
+        np.testing.assert_array_equal(g_nat[r][:n], g_py[r][:n])
+        assert not (g_nat[r][:n] == cfg.mask_id).any()
+    assert len(np.unique(np.concatenate(used))) > 1
+    assert dllm.get_device_error(device) == 0
+
+
+def test_native_loop_control_rejects_invalid_settings(dllm, device):
+    """dllm_loop_set_control: candidates not strictly ascending, no
+    candidates, a non-positive SLO or a negative latency term are rejected;
+    NULL turns the control off (the requests' own thresholds again)."""
+    import ctypes
+    from denoise_step_token_gb300.loop import NativeLoop
+    cfg = SMALL
+    reqs = synth.make_loop_requests(cfg, 5)
+    nl = NativeLoop(reqs.p, reqs.K, reqs.prompt_off, reqs.prompt_tokens, reqs.thr, L=cfg.L, V=cfg.V,
+                    mask_id=cfg.mask_id, pad_id=cfg.pad_id, budget=cfg.budget, device=device)
+    lib = dllm.load()
+
+    def ctl(cands, slo=1.0, lat=0.001, per_row=0.0):
+        arr = (ctypes.c_double * max(len(cands), 1))(*cands)
+        keep.append(arr)
+        return dllm.LoopControl(T=len(cands), candidates=ctypes.cast(arr, ctypes.c_void_p), slo_s=slo,
+                                tokens_per_s=1e5, latency_s=lat, latency_per_row_s=per_row)
+
+    keep = []
+    for bad in (ctl([0.5, 0.5]), ctl([0.9, 0.5]), ctl([]), ctl([0.5], slo=0.0), ctl([0.5], lat=-1.0),
+                ctl([0.5], per_row=-1.0), ctl([float("nan")])):
+        assert lib.dllm_loop_set_control(nl.handle, ctypes.byref(bad)) == -1
+    assert lib.dllm_loop_set_control(nl.handle, ctypes.byref(ctl([0.5, 0.9]))) == 0
+    assert lib.dllm_loop_set_control(nl.handle, None) == 0
+    # off again: a step uses the requests' own thresholds
+    nl.begin()
+    A = nl.info().A
+    rows = nl.masked_rows()
+    logits = _loop_logits(5, rows, A, cfg.L, cfg.V, cfg.offset_max, cfg.mask_id,
+                          np.full(max(A, 1), 0.9, np.float32), {}, cfg.row_stride)
+    import torch
+    rid, _, _ = nl.rows()
+    nl.end(torch.from_numpy(logits[: max(A, 1) * cfg.L].view(np.int16)).to(device))
+    np.testing.assert_array_equal(nl.thresholds(), np.asarray(reqs.thr, np.float32)[rid])
