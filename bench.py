@@ -233,7 +233,8 @@ class ClockSampler:
 class Pipeline:
     """Device buffers and prebuilt C-ABI argument structs for one batch."""
 
-    def __init__(self, cfg, inp, reqs, b, gen, pending_p, device, ring=RING, fixed_steps=None, vocab_shards=None):
+    def __init__(self, cfg, inp, reqs, b, gen, pending_p, device, ring=RING, fixed_steps=None, vocab_shards=None,
+                 fused=True):
         import torch
         import denoise_step_token_gb300 as dllm
         self.torch, self.dllm, self.lib = torch, dllm, dllm.load()
@@ -328,7 +329,9 @@ class Pipeline:
             for k in range(n):
                 self.shards[k] = dllm.VocabShard(logits=ctypes.c_void_p(self.logits.data_ptr() + bounds[k] * 2),
                                                  ldv=self.logits.shape[1], v0=bounds[k], V=bounds[k + 1] - bounds[k])
-        self.fused = True   # the step, block commit and compaction in one launch
+        # the step, block commit and compaction in one launch; else the step,
+        # then dllm_advance_compact (the comparison pipeline)
+        self.fused = bool(fused)
         self.quota = None
         if fixed_steps is not None:
             steps = L - inp.masked.sum(axis=1)
@@ -472,6 +475,17 @@ class Pipeline:
         return self.B * (4 * self.L + 12 + 5 + 8 + 2 * row_total)
 
 
+def roofline_kernel_label(sharded, fused, fixed):
+    """Which launch the roofline times: the step kernel over one logits
+    array or over vocabulary shards, with the commit inside it or not."""
+    if sharded:
+        entry = "dllm_step_vocab_shards_commit" if fused else "dllm_step_vocab_shards"
+        return f"step_kernel over 4 vocabulary shards{' with the fused commit' if fused else ''} ({entry})"
+    entry = ("dllm_step_commit" if fused else ("dllm_step_quota" if fixed else "dllm_step"))
+    quota = ", fixed-steps quota" if fixed and fused else ""
+    return f"step_kernel{' with the fused commit' if fused else ''} ({entry}{quota})"
+
+
 FUSED_STAGE_BYTES = 96 * 1024   # state rows dllm_advance_compact stages in one CTA (one launch)
 KERNEL_TIMING_LAUNCHES = 48   # step launches timed alone for the roofline (fixed, whatever --steps is)
 ORACLE_SAMPLE_CPU_S = 12.0   # CPU time the oracle baseline runs for (whole passes)
@@ -533,7 +547,8 @@ def run_gpu(args, rank, world, local_rank, dist):
     cfg, inp, reqs, b, gen, pending_p = make_workload(1000 + rank, args.workload)
     pipe = Pipeline(cfg, inp, reqs, b, gen, pending_p, device,
                     fixed_steps=FIXED_STEPS_S if args.workload == "dream_fixed_steps" else None,
-                    vocab_shards=4 if args.workload == "dream_vocab4" else None)
+                    vocab_shards=4 if args.workload == "dream_vocab4" else None,
+                    fused=not args.separate_commit)
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     K, W = args.steps, args.warmup
@@ -1043,6 +1058,8 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-commit", action="store_true",
+                    help="commit and compact in a launch of their own after the step (the comparison pipeline)")
     ap.add_argument("--read-ceiling", action="store_true",
                     help="measure the GPU's read-bandwidth ceiling (bulk copies and plain loads) instead")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dream",
@@ -1118,10 +1135,7 @@ def main():
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "frac_of_nominal_8000_gbs": achieved / NOMINAL_HBM_GBS,
                          "all_rows_logits_bytes_per_launch": cfg.B * cfg.L * cfg.V * 2,
-                         "kernel": ("step_kernel over 4 vocabulary shards with the fused commit (dllm_step_vocab_shards_commit)"
-                                    if pipe.shards else
-                                    "step_kernel with the fused commit (dllm_step_commit" +
-                                    (", fixed-steps quota)" if fixed else ")")),
+                         "kernel": roofline_kernel_label(pipe.shards is not None, pipe.fused, fixed),
                          "algorithmic_bytes_per_launch": alg,
                          "algorithmic_bytes_note": ("masked logits rows + per-position state + per-request I/O"
                                                     + (" + the commit at its bound (every row committed and moved)"

@@ -342,3 +342,28 @@ def test_native_loop_control_argument_checks():
     n = ctypes.c_int32(0)
     assert lib.dllm_loop_thresholds(None, None, ctypes.byref(n)) == -1
     assert ctypes.sizeof(dllm.LoopControl) == lib.dllm_struct_size(8)
+
+
+def test_vocab_shards_workspace_holds_the_extra_chunks():
+    """Each shard is cut into chunks from its own start, so a sharded step
+    needs dllm_step_workspace_size(B, L, V + 8192 * (n_shards - 1)) bytes:
+    one sized for V alone is rejected (DLLM_ERR_WORKSPACE) before any CUDA
+    call, by both sharded entry points."""
+    lib = dllm.load()
+    B, L, V = 64, 32, 126464
+    bounds = [0, 32768, 65536, 98304, V]
+    arr = (dllm.VocabShard * 4)()
+    for k in range(4):
+        arr[k] = dllm.VocabShard(logits=0x100000 * (k + 1), ldv=32768, v0=bounds[k], V=bounds[k + 1] - bounds[k])
+    small = lib.dllm_step_workspace_size(B, L, V)
+    need = lib.dllm_step_workspace_size(B, L, V + 8192 * 3)
+    assert need > small
+    a = dllm.StepArgs(B=B, L=L, V=V, mask_id=0, ldv=0, logits=None, input_ids=0x20000, thr=0x30000,
+                      conf_state=0x40000, done=0x50000, accept_len=0x60000, n_new=0x70000, workspace=0x1000000,
+                      workspace_bytes=small)
+    assert lib.dllm_step_vocab_shards(ctypes.byref(a), 4, arr, None, None) == -3
+    adv = dllm.AdvanceArgs(A=B, L=L, mask_id=0, advance=0x50000, rid=0x80000, K=0x90000, b=0xa0000,
+                           input_ids=0x20000, conf_state=0x40000, gen_tokens=0xb0000, ld_gen=256, evict=0xc0000)
+    ca = dllm.CompactArgs(A=B, n_arrays=0, A_out=0xd0000)
+    assert lib.dllm_step_vocab_shards_commit(ctypes.byref(a), 4, arr, None, ctypes.byref(adv), ctypes.byref(ca),
+                                             None) == -3

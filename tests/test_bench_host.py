@@ -76,3 +76,14 @@ def test_commit_bytes_bound():
     # block tokens 4L, b / K / rid read 12, b and evict written 5, maps 8,
     # each compacted row (276 bytes) read and written
     assert bench.Pipeline.commit_bytes_bound(pipe) == 128 * (4 * 32 + 12 + 5 + 8 + 2 * 276)
+
+
+def test_roofline_kernel_label():
+    import bench
+    assert bench.roofline_kernel_label(False, True, False) == "step_kernel with the fused commit (dllm_step_commit)"
+    assert bench.roofline_kernel_label(False, True, True) == ("step_kernel with the fused commit "
+                                                              "(dllm_step_commit, fixed-steps quota)")
+    assert bench.roofline_kernel_label(False, False, True) == "step_kernel (dllm_step_quota)"
+    assert bench.roofline_kernel_label(True, True, False) == ("step_kernel over 4 vocabulary shards with the fused "
+                                                              "commit (dllm_step_vocab_shards_commit)")
+    assert bench.roofline_kernel_label(True, False, False) == "step_kernel over 4 vocabulary shards (dllm_step_vocab_shards)"
