@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import compare_step, device_logits, enforce_margins, oracle_step
+from helpers import compare_step, device_logits, device_logits_compact, enforce_margins, oracle_step
 from oracle.loop import advance as oracle_advance
 
 pytestmark = pytest.mark.gpu
@@ -40,12 +40,13 @@ def device(dllm):
     return torch.device("cuda", 0)
 
 
-def _batch(cfg, seed):
-    """Step inputs with margins plus the rows' commit state: request ids (a
-    permutation), blocks K in 1..4, current block b < K, and committed tokens
-    of the earlier blocks."""
+def _batch(cfg, seed, quota=None):
+    """Step inputs with margins (for the fixed-steps rule when ``quota`` is
+    given) plus the rows' commit state: request ids (a permutation), blocks K
+    in 1..4, current block b < K, and committed tokens of the earlier
+    blocks."""
     inp = synth.make_step_state(cfg, seed)
-    enforce_margins(inp)
+    enforce_margins(inp, quota=quota)
     rng = np.random.default_rng(seed + 100)
     B, L = cfg.B, cfg.L
     K = rng.integers(1, 5, size=B).astype(np.int32)
@@ -56,8 +57,8 @@ def _batch(cfg, seed):
     return inp, rid, K, b, gen, ld_gen
 
 
-def _expected(cfg, inp, rid, K, b, gen):
-    ref = oracle_step(inp)
+def _expected(cfg, inp, rid, K, b, gen, quota=None):
+    ref = oracle_step(inp, quota=quota)
     L = cfg.L
     ids = ref["input_ids"].copy()
     cs = ref["conf_state"].copy()
@@ -68,16 +69,22 @@ def _expected(cfg, inp, rid, K, b, gen):
     return ref, dict(ids=ids, cs=cs, b=bb, gen=o_gen, evict=evict, new_index=new_index, src_row=src_row, A_out=A_out)
 
 
-def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=None, bounds=None):
+def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=None, bounds=None, quota=None,
+                compact_logits=False):
     """One step with its commit and compaction on the device: in one launch
     (fused) or as the step then dllm_advance_compact; over vocabulary shards
     [bounds[k], bounds[k+1]) of the logits (column slices) when bounds is
-    given."""
+    given; under the fixed-steps rule when ``quota`` [B] is given; reading
+    the masked positions' rows only (plus three spare rows) when
+    ``compact_logits``."""
     import torch
     lib = dllm.load()
     B, L = cfg.B, cfg.L
     t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(device)
-    logits = device_logits(inp, device)
+    logits = device_logits_compact(inp, device, extra_rows=3) if compact_logits else device_logits(inp, device)
+    rows = logits.shape[0] if compact_logits else -1
+    d_quota = None if quota is None else t(np.asarray(quota, dtype=np.int32))
+    q_ptr = None if d_quota is None else ctypes.c_void_p(d_quota.data_ptr())
     ids, thr, cs = t(inp.input_ids), t(inp.thr), t(inp.conf_state)
     d_rid, d_K, d_b, d_gen = t(rid), t(K), t(b), t(gen)
     p_arr = t(np.arange(B, dtype=np.int32) * 7)         # a row array the batch carries along
@@ -134,10 +141,15 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=Non
             assert lib.dllm_step_vocab_shards(ctypes.byref(sa), n_sh, shards, None, stream) == 0
             assert lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream) == 0
     elif fused:
-        rc = lib.dllm_step_commit(ctypes.byref(sa), None, -1, ctypes.byref(aa), ctypes.byref(ca), stream)
+        rc = lib.dllm_step_commit(ctypes.byref(sa), q_ptr, rows, ctypes.byref(aa), ctypes.byref(ca), stream)
         assert rc == 0, lib.dllm_strerror(rc)
     else:
-        assert lib.dllm_step(ctypes.byref(sa), stream) == 0
+        if compact_logits:
+            assert lib.dllm_step_compact(ctypes.byref(sa), rows, q_ptr, stream) == 0
+        elif quota is not None:
+            assert lib.dllm_step_quota(ctypes.byref(sa), q_ptr, stream) == 0
+        else:
+            assert lib.dllm_step(ctypes.byref(sa), stream) == 0
         assert lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream) == 0
     h = {k: v.cpu().numpy() for k, v in out.items()}
     h.update(ids=ids.cpu().numpy(), cs=cs.cpu().numpy(), thr=thr.cpu().numpy(), b=d_b.cpu().numpy(),
@@ -165,14 +177,24 @@ def test_vocab_shards_commit_matches_oracle_and_the_two_launch_path(dllm, device
     _check_commit(dllm, device, name, 3, SHARD_BOUNDS[name])
 
 
-def _check_commit(dllm, device, name, seed, bounds):
+# the fixed-steps rule, the compact logits layout (masked rows only), and both
+@pytest.mark.parametrize("name", ["ragged", "l64", "many_rows"])
+@pytest.mark.parametrize("variant", ["quota", "compact", "compact_quota"])
+def test_step_commit_quota_and_compact_logits(dllm, device, name, variant):
+    _check_commit(dllm, device, name, 5, None, quota_rule="quota" in variant, compact_logits="compact" in variant)
+
+
+def _check_commit(dllm, device, name, seed, bounds, quota_rule=False, compact_logits=False):
     cfg = CASES[name]
-    inp, rid, K, b, gen, ld_gen = _batch(cfg, seed)
-    ref, exp = _expected(cfg, inp, rid, K, b, gen)
+    quota = (np.random.default_rng(seed + 300).integers(0, cfg.L + 1, size=cfg.B).astype(np.int32)
+             if quota_rule else None)
+    inp, rid, K, b, gen, ld_gen = _batch(cfg, seed, quota=quota)
+    ref, exp = _expected(cfg, inp, rid, K, b, gen, quota=quota)
     extra = (np.random.default_rng(seed + 200).integers(0, 255, (cfg.B, 5)).astype(np.uint8)
              if name in WITH_BYTES else None)
-    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True, extra=extra, bounds=bounds)
-    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False, extra=extra, bounds=bounds)
+    kw = dict(extra=extra, bounds=bounds, quota=quota, compact_logits=compact_logits)
+    got = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=True, **kw)
+    two = _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused=False, **kw)
     B, L = cfg.B, cfg.L
     # the step's own outputs against the oracle (its ids / conf_state are
     # checked after the commit below)
