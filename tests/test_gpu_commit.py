@@ -134,11 +134,11 @@ def _device_run(dllm, device, cfg, inp, rid, K, b, gen, ld_gen, fused, extra=Non
             shards[k] = dllm.VocabShard(logits=ctypes.c_void_p(logits.data_ptr() + 2 * bounds[k]),
                                         ldv=logits.shape[1], v0=bounds[k], V=bounds[k + 1] - bounds[k])
         if fused:
-            rc = lib.dllm_step_vocab_shards_commit(ctypes.byref(sa), n_sh, shards, None, ctypes.byref(aa),
+            rc = lib.dllm_step_vocab_shards_commit(ctypes.byref(sa), n_sh, shards, q_ptr, ctypes.byref(aa),
                                                    ctypes.byref(ca), stream)
             assert rc == 0, lib.dllm_strerror(rc)
         else:
-            assert lib.dllm_step_vocab_shards(ctypes.byref(sa), n_sh, shards, None, stream) == 0
+            assert lib.dllm_step_vocab_shards(ctypes.byref(sa), n_sh, shards, q_ptr, stream) == 0
             assert lib.dllm_advance_compact(ctypes.byref(aa), ctypes.byref(ca), stream) == 0
     elif fused:
         rc = lib.dllm_step_commit(ctypes.byref(sa), q_ptr, rows, ctypes.byref(aa), ctypes.byref(ca), stream)
@@ -173,8 +173,9 @@ SHARD_BOUNDS = {"ragged": [0, 8, 20000, 40001], "dream_like": [0, 4096, 12000, 2
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_vocab_shards_commit_matches_oracle_and_the_two_launch_path(dllm, device, name):
-    _check_commit(dllm, device, name, 3, SHARD_BOUNDS[name])
+@pytest.mark.parametrize("quota_rule", [False, True])
+def test_vocab_shards_commit_matches_oracle_and_the_two_launch_path(dllm, device, name, quota_rule):
+    _check_commit(dllm, device, name, 3, SHARD_BOUNDS[name], quota_rule=quota_rule)
 
 
 # the fixed-steps rule, the compact logits layout (masked rows only), and both
