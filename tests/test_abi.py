@@ -350,20 +350,25 @@ def test_vocab_shards_workspace_holds_the_extra_chunks():
     one sized for V alone is rejected (DLLM_ERR_WORKSPACE) before any CUDA
     call, by both sharded entry points."""
     lib = dllm.load()
+    ERR_WORKSPACE = -5
     B, L, V = 64, 32, 126464
-    bounds = [0, 32768, 65536, 98304, V]
+    # shards of 30000 tokens: 4 + 4 + 4 + 5 = 17 chunks per row, against 16 unsharded
+    bounds = [0, 30000, 60000, 90000, V]
     arr = (dllm.VocabShard * 4)()
     for k in range(4):
-        arr[k] = dllm.VocabShard(logits=0x100000 * (k + 1), ldv=32768, v0=bounds[k], V=bounds[k + 1] - bounds[k])
+        arr[k] = dllm.VocabShard(logits=0x100000 * (k + 1), ldv=36464, v0=bounds[k], V=bounds[k + 1] - bounds[k])
     small = lib.dllm_step_workspace_size(B, L, V)
     need = lib.dllm_step_workspace_size(B, L, V + 8192 * 3)
     assert need > small
     a = dllm.StepArgs(B=B, L=L, V=V, mask_id=0, ldv=0, logits=None, input_ids=0x20000, thr=0x30000,
                       conf_state=0x40000, done=0x50000, accept_len=0x60000, n_new=0x70000, workspace=0x1000000,
                       workspace_bytes=small)
-    assert lib.dllm_step_vocab_shards(ctypes.byref(a), 4, arr, None, None) == -3
+    assert lib.dllm_step_vocab_shards(ctypes.byref(a), 4, arr, None, None) == ERR_WORKSPACE
     adv = dllm.AdvanceArgs(A=B, L=L, mask_id=0, advance=0x50000, rid=0x80000, K=0x90000, b=0xa0000,
                            input_ids=0x20000, conf_state=0x40000, gen_tokens=0xb0000, ld_gen=256, evict=0xc0000)
     ca = dllm.CompactArgs(A=B, n_arrays=0, A_out=0xd0000)
     assert lib.dllm_step_vocab_shards_commit(ctypes.byref(a), 4, arr, None, ctypes.byref(adv), ctypes.byref(ca),
-                                             None) == -3
+                                             None) == ERR_WORKSPACE
+    # the size the header asks for passes the workspace check (and stops at the first CUDA call: no device here)
+    a.workspace_bytes = need
+    assert lib.dllm_step_vocab_shards(ctypes.byref(a), 4, arr, None, None) != ERR_WORKSPACE
