@@ -14,7 +14,10 @@
 //     (dllm_step_commit), before the readback: they use the done flags on
 //     the device and leave the batch as it is when no block finished.  In
 //     sync mode the host decides after the readback (a commit needs every
-//     block done) and launches the commit.
+//     block done) and launches the commit.  With threshold control
+//     (dllm_loop_set_control; DiLaServe review, section 3.2) the step's
+//     thresholds are chosen on the host just before it and uploaded, and
+//     the block features come back with the done flags.
 // The host keeps only what admission needs (prompt lengths, block indices,
 // steps in the current block) and a small pinned staging block for the
 // per-iteration copies; every array the kernels read lives in the caller's
